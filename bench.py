@@ -1,0 +1,421 @@
+"""Decode-step benchmark of libkvr on one B300 (or N independent replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama3.1-8b-32k|qwen3-4b-128k]
+
+One step is one speculative decode step of one attention layer over a batch
+of sequences: group similarity and correction decision, page scoring and
+top-k selection per KV head, then sparse GQA attention over the selected
+pages (two kernels).  Page summaries are built once per cache (prefill) and
+reported on their own.  Inputs are seeded synthetic caches with the layer
+shapes of Llama-3.1-8B (default) or Qwen3-4B; the queries follow the AR(1)
+trace of the speculative workload.  The cache, queries and state are resident
+in HBM before the timed region; four copies of the cache (--copies) rotate so
+that no step reads data a recent step left in L2.  Steps are replayed from a CUDA
+graph of 64 captured steps.
+
+Prints one JSON line (rank 0).  With --impl reference the fp64 oracle is
+timed instead, on the host's cores, over a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode steps/s and selected-KV GB/s (fraction of B300 HBM peak) per layer"
+WORKLOADS = {"llama3.1-8b-32k": (2, 4), "qwen3-4b-128k": (3, 5)}  # (cache workload, trace workload)
+TRACE_LEN = 64
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+# ---------------------------------------------------------------- distributed
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over all ranks (the slowest rank sets the time)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: int, seconds_per_rank: float, world: int):
+    """Whole-job throughput: units of all ranks / the slowest rank's time."""
+    t = max_over_ranks(seconds_per_rank, world)
+    return units_per_rank * world / t, t
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(index)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 7:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = max(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- oracle leg
+
+
+def cpu_baseline(wl_name: str, seconds: float = 12.0):
+    """The fp64 oracle (as it stands) on this host: full decode steps of the
+    workload (selection + attention, summaries precomputed) until `seconds`."""
+    import oracle
+    from kv_cache_page_build_b300 import synth
+    cid, tid = WORKLOADS[wl_name]
+    case = synth.make_case(cid)
+    tr = synth.make_trace(synth.WORKLOADS[tid], case)
+    summ = oracle.summaries(case.k_pool, case.page_table)
+    wl = case.wl
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode_step(tr.q[n % TRACE_LEN], case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads,
+                           wl.top_k, summ=summ)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": n / el, "unit": "steps/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{n} full decode steps (batch {wl.batch}, selection + attention, fp64) of the same "
+                      f"workload in {el:.1f} s; summaries built beforehand"}
+
+
+# ---------------------------------------------------------------- GPU leg
+
+
+def traffic_for(kernel: str, wl_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{wl_name}.traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("source_sha256") != source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "kv_cache_page_build_b300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+    from kv_cache_page_build_b300 import kvr, synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cid, tid = WORKLOADS[args.workload]
+    COPIES = max(1, args.copies)
+    wl_trace = synth.WORKLOADS[tid]
+    case = synth.make_case(cid)
+    tr = synth.make_trace(wl_trace, case)
+    wl = case.wl
+    B, Hq, H, D, P, N, k = (wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.page_size, wl.n_pages,
+                            wl.top_k)
+    d = kvr.kvr_dims(**wl.dims())
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    k_pools = [to_dev(case.k_pool.view(np.int16)) for _ in range(COPIES)]
+    v_pools = [to_dev(case.v_pool.view(np.int16)) for _ in range(COPIES)]
+    page_table = to_dev(case.page_table)
+    qs = to_dev(tr.q.view(np.int16))                               # [64][B][Hq][D]
+    summs = [torch.empty((B, H, N, 2, D), dtype=torch.int16, device=dev) for _ in range(COPIES)]
+    del case
+
+    # summaries (prefill-time): time one build per copy
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kvr.kvr_build_summaries(d, k_pools[0], page_table, summs[0])
+    torch.cuda.synchronize()
+    e0.record()
+    for c in range(COPIES):
+        kvr.kvr_build_summaries(d, k_pools[c], page_table, summs[c])
+    e1.record()
+    torch.cuda.synchronize()
+    summ_ms = e0.elapsed_time(e1) / COPIES
+    k_bytes = B * N * P * H * D * 2
+
+    # speculative state and outputs
+    q_prev = torch.zeros((B, Hq, D), dtype=torch.int16, device=dev)
+    sel_prev = torch.zeros((B, H, k), dtype=torch.int32, device=dev)
+    st = kvr.kvr_spec_state(q_prev.data_ptr(), sel_prev.data_ptr(), 0)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    corrected = torch.empty((B, H), dtype=torch.uint8, device=dev)
+    sel_used = torch.empty((B, H, k), dtype=torch.int32, device=dev)
+    sel_used_phys = torch.empty((B, H, k), dtype=torch.int32, device=dev)
+    ws_n = kvr.kvr_workspace_size(d, k, kvr.KVR_OP_SELECT)
+    wa_n = kvr.kvr_workspace_size(d, k, kvr.KVR_OP_ATTN)
+    ws = torch.zeros(ws_n, dtype=torch.uint8, device=dev)
+    wa = torch.zeros(wa_n, dtype=torch.uint8, device=dev)
+
+    def step(i, ev_mid=None, ev_end=None):
+        c = i % COPIES
+        kvr.kvr_speculative_select(d, st, qs[i % TRACE_LEN], summs[c], page_table, k, wl_trace.tau, corrected,
+                                   None, sel_used, sel_used_phys, ws, ws_n)
+        if ev_mid is not None:
+            ev_mid.record()
+        kvr.kvr_sparse_decode_attn(d, qs[i % TRACE_LEN], k_pools[c], v_pools[c], sel_used_phys, k, 0.0, out,
+                                   wa, wa_n)
+        if ev_end is not None:
+            ev_end.record()
+
+    # warm-up: eager steps (the first one is step 0 of the trace)
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    assert kvr.kvr_get_status() == 0
+
+    # capture L steps (starting at a trace position multiple of 64) into a graph
+    L = min(TRACE_LEN, args.steps)
+    ev_mid = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(L)]
+    ev_end = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(L)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(L):
+            step(i, ev_mid[i], ev_end[i])
+    rem = args.steps % L
+    graph_rem = None
+    if rem:
+        graph_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_rem):
+            for i in range(rem):
+                step(i)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    reps = args.steps // L
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    clocks = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or local))
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(reps):
+        graph.replay()
+    if graph_rem is not None:
+        graph_rem.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    elapsed = t0.elapsed_time(t1) / 1e3
+    status = kvr.kvr_get_status()
+    value, t_max = aggregate(args.steps, elapsed, world)
+
+    # per-launch device time of the two kernels, from the last replay
+    attn_ms = [ev_mid[i].elapsed_time(ev_end[i]) for i in range(L)]
+    sel_ms = [ev_end[i - 1].elapsed_time(ev_mid[i]) for i in range(1, L)]
+    attn_avg = sum(attn_ms) / len(attn_ms) / 1e3
+    sel_avg = sum(sel_ms) / len(sel_ms) / 1e3 if sel_ms else None
+
+    hbm, peak_kind = peaks()
+    attn_bytes = B * H * k * P * 2 * D * 2                 # selected K and V rows read per launch
+    summ_bytes = B * H * N * 2 * D * 2                     # summaries read by the selection
+    achieved = attn_bytes / attn_avg / 1e9
+    traffic = traffic_for("k_sparse_decode", args.workload)
+
+    # end to end through the public API with host buffers (eager calls)
+    q_host = torch.from_numpy(tr.q.view(np.int16).copy()).pin_memory()
+    out_host = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
+    q_dev = torch.empty((B, Hq, D), dtype=torch.int16, device=dev)
+    wstep = torch.zeros(kvr.kvr_workspace_size(d, k, kvr.KVR_OP_STEP), dtype=torch.uint8, device=dev)
+    st_e = kvr.kvr_spec_state(q_prev.data_ptr(), sel_prev.data_ptr(), 1)
+    n_e2e = min(args.steps, 2000)
+    barrier(world)
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for i in range(n_e2e):
+        c = i % COPIES
+        q_dev.copy_(q_host[i % TRACE_LEN], non_blocking=True)
+        kvr.kvr_speculative_step(d, st_e, q_dev, summs[c], page_table, k_pools[c], v_pools[c], k, wl_trace.tau,
+                                 0.0, out, corrected, None, sel_used, sel_used_phys, wstep, wstep.numel())
+        out_host.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = time.perf_counter() - w0
+    e2e_value, _ = aggregate(n_e2e, e2e_s, world)
+    status |= kvr.kvr_get_status()
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_max / args.steps * 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{args.workload}: {wl.batch} sequences x {Hq}/{H} heads, head_dim {D}, "
+                        f"context {wl.context}, page {P}, top-k {k} pages; speculative, tau {wl_trace.tau}",
+            "batch": B, "n_q_heads": Hq, "n_kv_heads": H, "head_dim": D, "context": wl.context,
+            "page_size": P, "top_k": k, "tau": wl_trace.tau, "storage": "bf16", "accumulate": "f32",
+            "parallelism": f"{world} independent replica(s)" if world > 1 else "1 GPU",
+            "l2": f"{COPIES} rotating cache copies: {(COPIES - 1) * (attn_bytes + summ_bytes) / 2**20:.0f} MiB "
+                  f"touched between reuses of one copy (L2 126 MB)",
+            "graph": f"steps replayed from a CUDA graph of {L} steps",
+        },
+        "selected_kv_gbs": round(achieved, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "k_sparse_decode", "bytes_per_launch": attn_bytes,
+                     "launch_us": round(attn_avg * 1e6, 3)},
+        "kernels": {
+            "k_sparse_decode": {"us": round(attn_avg * 1e6, 3), "bytes": attn_bytes,
+                                "gbs": round(achieved, 1)},
+            "k_score_select": {"us": round(sel_avg * 1e6, 3) if sel_avg else None, "bytes": summ_bytes,
+                               "gbs": round(summ_bytes / sel_avg / 1e9, 1) if sel_avg else None},
+            "k_build_summaries": {"us": round(summ_ms * 1e3, 3), "bytes": k_bytes + summ_bytes,
+                                  "gbs": round((k_bytes + summ_bytes) / (summ_ms / 1e3) / 1e9, 1),
+                                  "note": "once per cache (prefill), not in the step"},
+        },
+        "gpu_launches": 2 * args.steps,
+        "e2e": {"value": round(e2e_value, 2), "unit": "steps/s",
+                "h2d_bytes_per_step": B * Hq * D * 2, "d2h_bytes_per_step": B * Hq * D * 4,
+                "how": f"{n_e2e} eager kvr_speculative_step calls, q copied in from pinned host memory and "
+                       f"the fp32 output copied back every step, stream synchronised per step"},
+        "clocks": clk,
+        "device_status": status,
+    }
+    return result
+
+
+# ---------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64000)
+    ap.add_argument("--warmup", type=int, default=128)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama3.1-8b-32k", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--copies", type=int, default=4, help="rotating cache copies (L2-cold timing needs >= 3)")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # each timed step is one full oracle decode step; the run is bounded in time
+        secs = min(60.0, max(5.0, 0.5 * (args.steps + args.warmup)))
+        base = cpu_baseline(args.workload, seconds=secs)
+        line = {"impl": "reference", "metric": METRIC, "value": round(base["value"], 4), "unit": "steps/s",
+                "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(1e3 / base["value"], 3), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": args.workload, "parallelism": "host cores (OpenMP)"},
+                "cpu_baseline": base,
+                "e2e": {"value": round(base["value"], 4), "unit": "steps/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    res = run_gpu(args, world, rank, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(args.workload)
+        else:
+            res["cpu_baseline"] = None
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

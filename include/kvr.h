@@ -1,0 +1,261 @@
+/*
+ * kvr.h -- C ABI of libkvr: decode-step KV page retrieval and sparse GQA
+ * decode attention on one NVIDIA B300 (sm_103a).
+ *
+ * Sources of the operations (titles of the pages, section names):
+ *   [FreeKV]  "FreeKV: Boosting KV Cache Retrieval for Efficient LLM
+ *             Inference", technical summary: section 1 (Problem: KV retrieval
+ *             keeps the whole cache and uses only the part each step needs),
+ *             section 2.1 (Algorithm side: speculative retrieval, fine-grained
+ *             correction, group-consistent similarity) and section 2.2
+ *             (System side: hybrid NHD/HND layouts, streamed recall with
+ *             double buffering).
+ *   [KVwiki]  "Key-Value (KV) Cache" wiki page: decoding appends one token's
+ *             K/V per step and is memory-bandwidth bound; PagedAttention
+ *             stores the cache in fixed-size pages; grouped-query attention.
+ * The pages describe selection by page but print no page-score formula.  This
+ * library scores a page with the per-channel upper bound of q.k built from the
+ * page's per-channel key minimum and maximum (kvr_build_summaries,
+ * kvr_select_pages).
+ *
+ * Conventions for every call:
+ *   - bf16 tensors are passed as `uint16_t*` holding raw bfloat16 bits;
+ *     int32 and fp32 tensors as their own types.  All tensors are dense,
+ *     row-major, in DEVICE memory unless stated otherwise, and must start on
+ *     a 16-byte boundary.
+ *   - Shapes: B = batch, Hq = query heads, H = KV heads, G = Hq / H query
+ *     heads per KV head (query head h uses KV head h / G), D = head_dim,
+ *     P = page_size, N = logical pages per sequence, k = top_k.
+ *   - The K and V pools hold physical pages in token-major (NHD) order:
+ *     [n_phys_pages][P][H][D]; page_table [B][N] maps a sequence's logical
+ *     page to a physical page.
+ *   - Supported: D = 128; G in {1, 2, 4, 8}; P in {16, 32, 64};
+ *     1 <= k <= N <= 16384; H <= 64; B <= 65535.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call only enqueues work on its stream(s) and returns;
+ *     it never synchronises, except kvr_get_status.
+ *   - The caller allocates and owns every buffer, workspace, state and
+ *     stream.  The library allocates no device memory; its only device state
+ *     is a 32-bit status word (see kvr_get_status).
+ *   - Errors: a call returns KVR_OK (0) or a negative KVR_ERR_* code.
+ *     Argument checks happen before any launch, so a rejected call enqueues
+ *     nothing.  Conditions found on the device (an out-of-range page id, a
+ *     wait that timed out) set bits of the status word instead.
+ *   - A workspace (`ws`, `ws_bytes`) must be at least kvr_workspace_size()
+ *     bytes and zero-filled before its first use; every call leaves it
+ *     zero-filled again.  Calls that share a workspace must not overlap on
+ *     the GPU.
+ */
+#ifndef KVR_H
+#define KVR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVR_OK 0
+#define KVR_ERR_INVALID_ARG (-1)       /* null pointer, negative size, bad enum */
+#define KVR_ERR_UNSUPPORTED_SHAPE (-2) /* a dimension outside the supported set */
+#define KVR_ERR_ALIGN (-3)             /* a pointer not on a 16-byte boundary */
+#define KVR_ERR_WORKSPACE (-4)         /* workspace missing or too small */
+#define KVR_ERR_CUDA (-5)              /* a CUDA call or launch failed */
+#define KVR_ERR_TIMEOUT (-6)           /* a host-side wait ran past its deadline */
+
+/* status-word bits set by kernels */
+#define KVR_ST_BAD_INDEX 0x1u     /* a page id outside its pool was skipped */
+#define KVR_ST_WAIT_TIMEOUT 0x2u  /* a kernel gave up waiting for a copy */
+#define KVR_ST_NO_TOKENS 0x4u     /* an attention row had no valid token */
+#define KVR_ST_NO_FREE_SLOT 0x8u  /* recall found fewer free slots than misses */
+
+/* workspace kinds for kvr_workspace_size */
+#define KVR_OP_SELECT 1 /* kvr_select_pages, kvr_speculative_select */
+#define KVR_OP_ATTN 2   /* kvr_sparse_decode_attn */
+#define KVR_OP_STEP 3   /* kvr_speculative_step, kvr_speculative_step_recall */
+
+typedef struct kvr_dims {
+  int32_t batch;        /* B */
+  int32_t n_q_heads;    /* Hq */
+  int32_t n_kv_heads;   /* H */
+  int32_t head_dim;     /* D */
+  int32_t page_size;    /* P */
+  int32_t n_pages;      /* N, logical pages per sequence */
+  int32_t n_phys_pages; /* pages in the K/V pools */
+} kvr_dims;
+
+/* Bytes of workspace a call of kind `op` needs for these dims and top_k
+ * (0 for invalid arguments). */
+size_t kvr_workspace_size(const kvr_dims *dims, int32_t top_k, int32_t op);
+
+/* Page summaries.  For every sequence b, KV head g and logical page p, the
+ * per-channel minimum and maximum of the P keys of that page:
+ *   summ[b][g][p][0][c] = min_t K[page_table[b][p]][t][g][c]
+ *   summ[b][g][p][1][c] = max_t K[page_table[b][p]][t][g][c]
+ * k_pool [n_phys][P][H][D] bf16; page_table [B][N] int32; summ
+ * [B][H][N][2][D] bf16 (written; min and max of bf16 values are bf16, so the
+ * summary is exact).  Pages are the paged cache of [KVwiki] (PagedAttention);
+ * the summary feeds the page score of kvr_select_pages.  A page_table entry
+ * outside [0, n_phys) sets KVR_ST_BAD_INDEX and leaves that summary
+ * unwritten. */
+int kvr_build_summaries(const kvr_dims *dims, const uint16_t *k_pool,
+                        const int32_t *page_table, uint16_t *summ, void *stream);
+
+/* KV selection for one decode step ([FreeKV] section 1: select the needed
+ * part of the kept cache; section 2.1: selection per KV head, group-
+ * consistent).  For each (b, g) the page score is
+ *   S[b][g][p] = (1/G) * sum_{h in group g} sum_c max(q[b][h][c]*kmin_c, q[b][h][c]*kmax_c)
+ * accumulated in fp32 from exact bf16 products, and the top_k pages with the
+ * largest S are selected, ties to the lower page id.
+ * q [B][Hq][D] bf16; summ from kvr_build_summaries; page_table [B][N].
+ * Outputs: sel [B][H][k] int32 logical page ids in ascending order;
+ * sel_phys [B][H][k] int32 = page_table[b][sel] (may be NULL); scores_opt
+ * [B][H][N] fp32 copy of S (may be NULL).  Workspace kind KVR_OP_SELECT. */
+int kvr_select_pages(const kvr_dims *dims, const uint16_t *q,
+                     const uint16_t *summ, const int32_t *page_table,
+                     int32_t top_k, int32_t *sel, int32_t *sel_phys,
+                     float *scores_opt, void *ws, size_t ws_bytes, void *stream);
+
+/* Sparse GQA decode attention over the selected pages ([FreeKV] section
+ * 2.1: step i attends over the retrieved pages; [KVwiki]: GQA).  For query
+ * head h of sequence b with KV head g = h / G, over the tokens t of pages
+ * sel_phys[b][g][0..k) (physical ids into the pools):
+ *   out[b][h] = sum_t softmax_t(scale * q[b][h] . K_t) * V_t
+ * computed in fp32 (split over the selected pages, then merged with a
+ * log-sum-exp rescale).  scale <= 0 means 1/sqrt(D).  q [B][Hq][D] bf16;
+ * k_pool, v_pool [n_phys][P][H][D] bf16; sel_phys [B][H][k] int32; out
+ * [B][Hq][D] fp32.  An id outside [0, n_phys) is skipped and sets
+ * KVR_ST_BAD_INDEX.  Workspace kind KVR_OP_ATTN. */
+int kvr_sparse_decode_attn(const kvr_dims *dims, const uint16_t *q,
+                           const uint16_t *k_pool, const uint16_t *v_pool,
+                           const int32_t *sel_phys, int32_t top_k, float scale,
+                           float *out, void *ws, size_t ws_bytes, void *stream);
+
+/* State of the speculative mode, owned by the caller.  q_prev [B][Hq][D]
+ * bf16 and sel_prev [B][H][k] int32 are device buffers; `step` is a host
+ * counter that the library increments on every successful step (0 before
+ * the first).  Restoring the three restores the trace exactly. */
+typedef struct kvr_spec_state {
+  uint16_t *q_prev;
+  int32_t *sel_prev;
+  int32_t step;
+} kvr_spec_state;
+
+/* Speculative selection ([FreeKV] section 2.1).  Computes the selection of
+ * the current query (as kvr_select_pages) and, per (b, g), the group
+ * similarity C = mean over the group's query heads of cos(q_t, q_prev)
+ * (fp32; cosine 0 for a zero vector).  The KV head is corrected when
+ * step == 0 or C < tau; the selection used by this step is the current
+ * query's for corrected heads and the previous step's (sel_prev) for the
+ * others.  Then sel_prev <- current selection and q_prev <- q_t.
+ * Outputs: corrected [B][H] uint8; cbar_opt [B][H] fp32 (may be NULL);
+ * sel_used [B][H][k] logical ids ascending; sel_used_phys [B][H][k] =
+ * page_table[b][sel_used] (may be NULL).  Workspace kind KVR_OP_SELECT.
+ * Increments st->step on success. */
+int kvr_speculative_select(const kvr_dims *dims, kvr_spec_state *st,
+                           const uint16_t *q_t, const uint16_t *summ,
+                           const int32_t *page_table, int32_t top_k, float tau,
+                           uint8_t *corrected, float *cbar_opt,
+                           int32_t *sel_used, int32_t *sel_used_phys,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/* One speculative decode step: kvr_speculative_select followed by
+ * kvr_sparse_decode_attn over sel_used_phys (which must be non-NULL), both on
+ * `stream`.  Workspace kind KVR_OP_STEP. */
+int kvr_speculative_step(const kvr_dims *dims, kvr_spec_state *st,
+                         const uint16_t *q_t, const uint16_t *summ,
+                         const int32_t *page_table, const uint16_t *k_pool,
+                         const uint16_t *v_pool, int32_t top_k, float tau,
+                         float scale, float *out, uint8_t *corrected,
+                         float *cbar_opt, int32_t *sel_used,
+                         int32_t *sel_used_phys, void *ws, size_t ws_bytes,
+                         void *stream);
+
+/* Host-resident cache for streamed recall ([FreeKV] section 2.2, hybrid
+ * layouts: the host copy is head-major, HND).  k_host, v_host
+ * [B][H][N][P][D] bf16 in page-locked host memory (cudaHostAlloc /
+ * cudaHostRegister); each (b, g, p) page is one contiguous P*D block. */
+typedef struct kvr_host_kv {
+  const uint16_t *k_host;
+  const uint16_t *v_host;
+} kvr_host_kv;
+
+/* Device working set of recalled pages.  k_slots, v_slots
+ * [B][n_slots][P][H][D] bf16 (token-major, NHD, like the pools): slot s of
+ * sequence b holds, for each KV head g separately, the page
+ * slot2page[b][g][s].  page2slot [B][H][N] int32 (-1 = not resident) and
+ * slot2page [B][H][n_slots] int32 (-1 = empty) are device maps.  n_slots
+ * >= 2 * top_k (one set of slots read by the running step, one being
+ * filled: double buffering). */
+typedef struct kvr_working_set {
+  uint16_t *k_slots;
+  uint16_t *v_slots;
+  int32_t *page2slot;
+  int32_t *slot2page;
+  int32_t n_slots;
+} kvr_working_set;
+
+/* Empty the working set's maps (all -1) on `stream`. */
+int kvr_working_set_reset(const kvr_dims *dims, const kvr_working_set *wset,
+                          void *stream);
+
+/* Streamed recall ([FreeKV] section 2.2).  For every (b, g): the pages of
+ * sel_new [B][H][k] that are not resident are copied from the host cache
+ * into free slots, converting head-major host pages into the token-major
+ * slot layout on the way (kernel loads read the page-locked host memory
+ * directly).  Slots holding pages of sel_new or of protect [B][H][k] (the
+ * selection the running attention reads) are never reused; free slots are
+ * taken in ascending slot order for misses in ascending page order.  For
+ * the heads with corrected[b][g] != 0 it also writes sel_slot_out[b][g][i] =
+ * b * n_slots + page2slot[b][g][protect[b][g][i]] (for those heads protect
+ * is the new selection itself).  n_copied_opt (device, may be NULL) is
+ * incremented by the number of pages copied.  Runs on `stream` (normally a
+ * side stream). */
+int kvr_recall_pages(const kvr_dims *dims, const kvr_host_kv *host,
+                     const kvr_working_set *wset, const int32_t *sel_new,
+                     const int32_t *protect, const uint8_t *corrected,
+                     int32_t top_k, int32_t *sel_slot_out,
+                     uint32_t *n_copied_opt, void *stream);
+
+/* One speculative decode step with the cache in host memory ([FreeKV]
+ * sections 2.1 and 2.2).  On `stream`: speculative selection; the slots of
+ * the non-corrected heads' reused pages (already resident) go to
+ * sel_used_slot; record ev_select.  On `side_stream`: wait ev_select, recall
+ * the current selection (protecting sel_used), record ev_recall.  On
+ * `stream`: attention for the non-corrected heads (overlapping the recall),
+ * wait ev_recall, attention for the corrected heads.  ev_select and ev_recall
+ * are caller-created cudaEvent_t passed as void*.  The working set must have
+ * been reset before the first step.  Workspace kind KVR_OP_STEP. */
+int kvr_speculative_step_recall(const kvr_dims *dims, kvr_spec_state *st,
+                                const uint16_t *q_t, const uint16_t *summ,
+                                const kvr_host_kv *host,
+                                const kvr_working_set *wset, int32_t top_k,
+                                float tau, float scale, float *out,
+                                uint8_t *corrected, float *cbar_opt,
+                                int32_t *sel_used, int32_t *sel_used_slot,
+                                uint32_t *n_copied_opt, void *ws,
+                                size_t ws_bytes, void *stream,
+                                void *side_stream, void *ev_select,
+                                void *ev_recall);
+
+/* Synchronise `stream`, then read and clear the device status word (a bit
+ * set of KVR_ST_*).  Returns KVR_OK or KVR_ERR_CUDA. */
+int kvr_get_status(void *stream, uint32_t *status_out);
+
+/* Static description of an error code (never NULL).  For KVR_ERR_CUDA the
+ * text of the last CUDA error seen by the library is appended. */
+const char *kvr_error_string(int code);
+
+/* Bytes of a full K and V cache of one sequence:
+ *   2 * n_layers * n_kv_heads * head_dim * n_tokens * bytes_per_elem.
+ * ([KVwiki]: the cache grows linearly with context.)  0 on overflow or a
+ * negative argument. */
+uint64_t kvr_kv_bytes(int64_t n_layers, int64_t n_kv_heads, int64_t head_dim,
+                      int64_t n_tokens, int64_t bytes_per_elem);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVR_H */

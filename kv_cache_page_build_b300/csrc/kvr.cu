@@ -1,0 +1,584 @@
+// kvr.cu -- the C ABI of libkvr (declared in include/kvr.h).
+//
+// Host side only: argument checks (before anything is enqueued), workspace
+// carving, tensor-map encoding for the K/V pools, kernel dispatch over the
+// supported (G, P) instances and the event wiring of the recall step.  All
+// compute is in the kernels of the included .cuh files.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "attention.cuh"
+#include "common.cuh"
+#include "recall.cuh"
+#include "select.cuh"
+#include "summaries.cuh"
+
+namespace {
+
+using namespace kvr;
+
+thread_local char g_err_text[512];
+
+int cuda_fail(cudaError_t e, const char *where) {
+  std::snprintf(g_err_text, sizeof g_err_text, "CUDA error in %s: %s", where,
+                cudaGetErrorString(e));
+  return KVR_ERR_CUDA;
+}
+
+int check_launch(const char *where) {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? KVR_OK : cuda_fail(e, where);
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int check_dims(const kvr_dims *d) {
+  if (!d) return KVR_ERR_INVALID_ARG;
+  if (d->batch <= 0 || d->n_q_heads <= 0 || d->n_kv_heads <= 0 || d->head_dim <= 0 ||
+      d->page_size <= 0 || d->n_pages <= 0 || d->n_phys_pages <= 0)
+    return KVR_ERR_INVALID_ARG;
+  if (d->head_dim != kD) return KVR_ERR_UNSUPPORTED_SHAPE;
+  if (d->n_q_heads % d->n_kv_heads) return KVR_ERR_UNSUPPORTED_SHAPE;
+  const int G = d->n_q_heads / d->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return KVR_ERR_UNSUPPORTED_SHAPE;
+  if (d->page_size != 16 && d->page_size != 32 && d->page_size != 64)
+    return KVR_ERR_UNSUPPORTED_SHAPE;
+  if (d->n_pages > kMaxPages || d->n_kv_heads > 64 || d->batch > 65535)
+    return KVR_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<int64_t>(d->n_phys_pages) * d->page_size > (int64_t{1} << 31))
+    return KVR_ERR_UNSUPPORTED_SHAPE;
+  return KVR_OK;
+}
+
+int check_topk(const kvr_dims *d, int32_t top_k) {
+  if (top_k <= 0) return KVR_ERR_INVALID_ARG;
+  if (top_k > d->n_pages) return KVR_ERR_UNSUPPORTED_SHAPE;
+  return KVR_OK;
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device (cached).
+constexpr int kMaxDevices = 64;
+int ensure_smem(const void *kern, size_t bytes, int *max_set) {
+  if (bytes <= 48 * 1024) return KVR_OK;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return KVR_ERR_UNSUPPORTED_SHAPE;
+  if (max_set[dev] >= static_cast<int>(bytes)) return KVR_OK;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return cuda_fail(e, "dynamic shared memory attribute");
+  max_set[dev] = static_cast<int>(bytes);
+  return KVR_OK;
+}
+
+// ---------------------------------------------------------------- workspace
+
+struct SelectWs {
+  float *scores;
+  uint32_t *count;
+};
+struct AttnWs {
+  float *part_o;
+  float *part_ml;
+  uint32_t *count;
+};
+
+size_t select_ws_bytes(const kvr_dims *d) {
+  const size_t units = static_cast<size_t>(d->batch) * d->n_kv_heads;
+  return align_up(units * d->n_pages * sizeof(float)) + align_up(units * sizeof(uint32_t));
+}
+
+size_t attn_ws_bytes(const kvr_dims *d, int top_k) {
+  const size_t units = static_cast<size_t>(d->batch) * d->n_kv_heads;
+  const size_t G = d->n_q_heads / d->n_kv_heads;
+  const size_t splits = attn_splits(top_k, d->page_size);
+  return align_up(units * splits * G * kD * sizeof(float)) +
+         align_up(units * splits * G * 2 * sizeof(float)) + align_up(units * sizeof(uint32_t));
+}
+
+SelectWs carve_select(const kvr_dims *d, uint8_t *p) {
+  const size_t units = static_cast<size_t>(d->batch) * d->n_kv_heads;
+  SelectWs w;
+  w.scores = reinterpret_cast<float *>(p);
+  w.count = reinterpret_cast<uint32_t *>(p + align_up(units * d->n_pages * sizeof(float)));
+  return w;
+}
+
+AttnWs carve_attn(const kvr_dims *d, int top_k, uint8_t *p) {
+  const size_t units = static_cast<size_t>(d->batch) * d->n_kv_heads;
+  const size_t G = d->n_q_heads / d->n_kv_heads;
+  const size_t splits = attn_splits(top_k, d->page_size);
+  AttnWs w;
+  w.part_o = reinterpret_cast<float *>(p);
+  p += align_up(units * splits * G * kD * sizeof(float));
+  w.part_ml = reinterpret_cast<float *>(p);
+  p += align_up(units * splits * G * 2 * sizeof(float));
+  w.count = reinterpret_cast<uint32_t *>(p);
+  return w;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// The pool [n_phys][P][H][D] bf16 viewed as [tokens][H][D]; one box is one
+// head's P consecutive token rows of a page (D x 1 x P elements).
+int make_pool_map(CUtensorMap *map, const void *pool, const kvr_dims *d, int64_t n_phys) {
+  auto fn = encode_fn();
+  if (!fn) {
+    std::snprintf(g_err_text, sizeof g_err_text, "cuTensorMapEncodeTiled unavailable");
+    return KVR_ERR_CUDA;
+  }
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(d->n_kv_heads),
+                              static_cast<cuuint64_t>(n_phys * d->page_size)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
+                                 static_cast<cuuint64_t>(d->n_kv_heads) * kD * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), 1u,
+                             static_cast<cuuint32_t>(d->page_size)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r =
+      fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_err_text, sizeof g_err_text, "cuTensorMapEncodeTiled failed (%d)",
+                  static_cast<int>(r));
+    return KVR_ERR_CUDA;
+  }
+  return KVR_OK;
+}
+
+// ---------------------------------------------------------------- launches
+
+template <int G>
+int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
+                    const int32_t *ptab, int k, SelectWs w, int32_t *sel, int32_t *sel_phys,
+                    float *scores, const SpecArgs &spec, cudaStream_t st) {
+  const int n_chunks = (d->n_pages + kSelChunk - 1) / kSelChunk;
+  const size_t smem = std::max<size_t>(kSelStageBytes, static_cast<size_t>(d->n_pages) * 4);
+  auto kern = k_score_select<G>;
+  static int max_set[kMaxDevices] = {};
+  if (int rc = ensure_smem(reinterpret_cast<const void *>(kern), smem, max_set)) return rc;
+  const dim3 grid(n_chunks, d->n_kv_heads, d->batch);
+  kern<<<grid, kSelThreads, smem, st>>>(q, summ, ptab, d->n_kv_heads, d->n_pages, k, n_chunks,
+                                        w.scores, w.count, sel, sel_phys, scores, spec);
+  return check_launch("k_score_select");
+}
+
+int launch_select(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
+                  const int32_t *ptab, int k, SelectWs w, int32_t *sel, int32_t *sel_phys,
+                  float *scores, const SpecArgs &spec, cudaStream_t st) {
+  switch (d->n_q_heads / d->n_kv_heads) {
+    case 1: return launch_select_g<1>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st);
+    case 2: return launch_select_g<2>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st);
+    case 4: return launch_select_g<4>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st);
+    default: return launch_select_g<8>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st);
+  }
+}
+
+template <int G, int P>
+int launch_attn_gp(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &tv,
+                   const uint16_t *q, const int32_t *sel_phys, int k, int n_phys, float scale,
+                   const uint8_t *filter, int filter_mode, AttnWs w, float *out, cudaStream_t st) {
+  const int n_splits = attn_splits(k, P);
+  const size_t smem = 2 * static_cast<size_t>(kAttnTileBytes) + kAttnTokens * G * sizeof(float);
+  auto kern = k_sparse_decode<G, P>;
+  static int max_set[kMaxDevices] = {};
+  if (int rc = ensure_smem(reinterpret_cast<const void *>(kern), smem, max_set)) return rc;
+  const float scale_log2 = scale * 1.4426950408889634f;
+  const dim3 grid(n_splits, d->n_kv_heads, d->batch);
+  kern<<<grid, kAttnThreads, smem, st>>>(tk, tv, q, sel_phys, d->n_kv_heads, k, n_phys, n_splits,
+                                         scale_log2, filter, filter_mode, w.part_o, w.part_ml,
+                                         w.count, out);
+  return check_launch("k_sparse_decode");
+}
+
+template <int G>
+int launch_attn_g(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &tv,
+                  const uint16_t *q, const int32_t *sel_phys, int k, int n_phys, float scale,
+                  const uint8_t *filter, int filter_mode, AttnWs w, float *out, cudaStream_t st) {
+  switch (d->page_size) {
+    case 16:
+      return launch_attn_gp<G, 16>(d, tk, tv, q, sel_phys, k, n_phys, scale, filter, filter_mode,
+                                   w, out, st);
+    case 32:
+      return launch_attn_gp<G, 32>(d, tk, tv, q, sel_phys, k, n_phys, scale, filter, filter_mode,
+                                   w, out, st);
+    default:
+      return launch_attn_gp<G, 64>(d, tk, tv, q, sel_phys, k, n_phys, scale, filter, filter_mode,
+                                   w, out, st);
+  }
+}
+
+int launch_attn(const kvr_dims *d, const uint16_t *q, const uint16_t *k_pool,
+                const uint16_t *v_pool, int64_t n_phys, const int32_t *sel_phys, int k,
+                float scale, const uint8_t *filter, int filter_mode, AttnWs w, float *out,
+                cudaStream_t st) {
+  CUtensorMap tk, tv;
+  int rc = make_pool_map(&tk, k_pool, d, n_phys);
+  if (rc) return rc;
+  rc = make_pool_map(&tv, v_pool, d, n_phys);
+  if (rc) return rc;
+  if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(kD));
+  const int np = static_cast<int>(n_phys);
+  switch (d->n_q_heads / d->n_kv_heads) {
+    case 1: return launch_attn_g<1>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st);
+    case 2: return launch_attn_g<2>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st);
+    case 4: return launch_attn_g<4>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st);
+    default: return launch_attn_g<8>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st);
+  }
+}
+
+// Device address of page-locked host memory (the kernels read it directly).
+int mapped_host_pointer(const void *host, void **dev) {
+  cudaPointerAttributes a;
+  const cudaError_t e = cudaPointerGetAttributes(&a, host);
+  if (e != cudaSuccess) return cuda_fail(e, "host cache pointer attributes");
+  if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) {
+    std::snprintf(g_err_text, sizeof g_err_text, "host cache is not page-locked, mapped host memory");
+    return KVR_ERR_INVALID_ARG;
+  }
+  *dev = a.devicePointer;
+  return KVR_OK;
+}
+
+int launch_recall(const kvr_dims *d, const kvr_host_kv *host, const kvr_working_set *wset,
+                  const int32_t *sel_new, const int32_t *protect, const uint8_t *corrected,
+                  int k, int32_t *sel_slot_out, uint32_t *n_copied, cudaStream_t st) {
+  void *kh = nullptr, *vh = nullptr;
+  int rc = mapped_host_pointer(host->k_host, &kh);
+  if (rc) return rc;
+  if ((rc = mapped_host_pointer(host->v_host, &vh))) return rc;
+  const int S = wset->n_slots;
+  const size_t smem = (2 * static_cast<size_t>(S) + k) * sizeof(int32_t);
+  const dim3 grid(d->n_kv_heads, d->batch);
+#define KVR_RECALL(PP)                                                                          \
+  k_recall<PP><<<grid, kRecallThreads, smem, st>>>(                                             \
+      static_cast<const uint16_t *>(kh), static_cast<const uint16_t *>(vh), wset->k_slots,      \
+      wset->v_slots, wset->page2slot, wset->slot2page, S, sel_new, protect, corrected,          \
+      d->n_kv_heads, d->n_pages, k, sel_slot_out, n_copied)
+  switch (d->page_size) {
+    case 16: KVR_RECALL(16); break;
+    case 32: KVR_RECALL(32); break;
+    default: KVR_RECALL(64); break;
+  }
+#undef KVR_RECALL
+  return check_launch("k_recall");
+}
+
+int check_wset(const kvr_dims *d, const kvr_working_set *w, int32_t top_k) {
+  if (!w || !w->k_slots || !w->v_slots || !w->page2slot || !w->slot2page) return KVR_ERR_INVALID_ARG;
+  if (w->n_slots < 2 * top_k) return KVR_ERR_UNSUPPORTED_SHAPE;
+  if ((2 * static_cast<int64_t>(w->n_slots) + top_k) * 4 > 48 * 1024) return KVR_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<int64_t>(d->batch) * w->n_slots * d->page_size > (int64_t{1} << 31))
+    return KVR_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(w->k_slots) || !aligned16(w->v_slots) || !aligned16(w->page2slot) ||
+      !aligned16(w->slot2page))
+    return KVR_ERR_ALIGN;
+  return KVR_OK;
+}
+
+int check_ws(void *ws, size_t have, size_t need) {
+  if (!ws) return KVR_ERR_WORKSPACE;
+  if (have < need) return KVR_ERR_WORKSPACE;
+  if (!aligned16(ws)) return KVR_ERR_ALIGN;
+  return KVR_OK;
+}
+
+SpecArgs no_spec() {
+  SpecArgs s;
+  std::memset(&s, 0, sizeof s);
+  return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kvr_workspace_size(const kvr_dims *dims, int32_t top_k, int32_t op) {
+  if (check_dims(dims) || check_topk(dims, top_k)) return 0;
+  switch (op) {
+    case KVR_OP_SELECT: return select_ws_bytes(dims);
+    case KVR_OP_ATTN: return attn_ws_bytes(dims, top_k);
+    case KVR_OP_STEP: return select_ws_bytes(dims) + attn_ws_bytes(dims, top_k);
+    default: return 0;
+  }
+}
+
+int kvr_build_summaries(const kvr_dims *dims, const uint16_t *k_pool, const int32_t *page_table,
+                        uint16_t *summ, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (!k_pool || !page_table || !summ) return KVR_ERR_INVALID_ARG;
+  if (!aligned16(k_pool) || !aligned16(page_table) || !aligned16(summ)) return KVR_ERR_ALIGN;
+  const int cols = dims->n_kv_heads * 16;
+  const int ppc = cols >= kSumThreads ? 1 : kSumThreads / cols;
+  const dim3 grid((dims->n_pages + ppc - 1) / ppc, dims->batch);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (dims->page_size) {
+    case 16:
+      k_build_summaries<16><<<grid, kSumThreads, 0, st>>>(k_pool, page_table, summ,
+                                                          dims->n_kv_heads, dims->n_pages,
+                                                          dims->n_phys_pages, ppc);
+      break;
+    case 32:
+      k_build_summaries<32><<<grid, kSumThreads, 0, st>>>(k_pool, page_table, summ,
+                                                          dims->n_kv_heads, dims->n_pages,
+                                                          dims->n_phys_pages, ppc);
+      break;
+    default:
+      k_build_summaries<64><<<grid, kSumThreads, 0, st>>>(k_pool, page_table, summ,
+                                                          dims->n_kv_heads, dims->n_pages,
+                                                          dims->n_phys_pages, ppc);
+      break;
+  }
+  return check_launch("k_build_summaries");
+}
+
+int kvr_select_pages(const kvr_dims *dims, const uint16_t *q, const uint16_t *summ,
+                     const int32_t *page_table, int32_t top_k, int32_t *sel, int32_t *sel_phys,
+                     float *scores_opt, void *ws, size_t ws_bytes, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_topk(dims, top_k))) return rc;
+  if (!q || !summ || !page_table || !sel) return KVR_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(summ) || !aligned16(page_table) || !aligned16(sel) ||
+      (sel_phys && !aligned16(sel_phys)) || (scores_opt && !aligned16(scores_opt)))
+    return KVR_ERR_ALIGN;
+  if ((rc = check_ws(ws, ws_bytes, select_ws_bytes(dims)))) return rc;
+  return launch_select(dims, q, summ, page_table, top_k, carve_select(dims, (uint8_t *)ws), sel,
+                       sel_phys, scores_opt, no_spec(), static_cast<cudaStream_t>(stream));
+}
+
+int kvr_sparse_decode_attn(const kvr_dims *dims, const uint16_t *q, const uint16_t *k_pool,
+                           const uint16_t *v_pool, const int32_t *sel_phys, int32_t top_k,
+                           float scale, float *out, void *ws, size_t ws_bytes, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_topk(dims, top_k))) return rc;
+  if (!q || !k_pool || !v_pool || !sel_phys || !out) return KVR_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(sel_phys) ||
+      !aligned16(out))
+    return KVR_ERR_ALIGN;
+  if (std::isnan(scale)) return KVR_ERR_INVALID_ARG;
+  if ((rc = check_ws(ws, ws_bytes, attn_ws_bytes(dims, top_k)))) return rc;
+  return launch_attn(dims, q, k_pool, v_pool, dims->n_phys_pages, sel_phys, top_k, scale, nullptr,
+                     0, carve_attn(dims, top_k, (uint8_t *)ws), out,
+                     static_cast<cudaStream_t>(stream));
+}
+
+static int spec_select_impl(const kvr_dims *dims, kvr_spec_state *st, const uint16_t *q_t,
+                            const uint16_t *summ, const int32_t *page_table, int32_t top_k,
+                            float tau, uint8_t *corrected, float *cbar_opt, int32_t *sel_used,
+                            int32_t *sel_used_phys, const int32_t *page2slot, int n_slots,
+                            void *ws, cudaStream_t stream) {
+  SpecArgs s = no_spec();
+  s.enabled = 1;
+  s.step = st->step;
+  s.tau = tau;
+  s.q_prev = st->q_prev;
+  s.sel_prev = st->sel_prev;
+  s.corrected = corrected;
+  s.cbar = cbar_opt;
+  s.sel_used = sel_used;
+  s.sel_used_phys = sel_used_phys;
+  s.page2slot = page2slot;
+  s.n_slots = n_slots;
+  return launch_select(dims, q_t, summ, page_table, top_k, carve_select(dims, (uint8_t *)ws),
+                       nullptr, nullptr, nullptr, s, stream);
+}
+
+static int check_spec(const kvr_dims *dims, const kvr_spec_state *st, const uint16_t *q_t,
+                      const uint16_t *summ, uint8_t *corrected, float *cbar_opt,
+                      int32_t *sel_used, float tau) {
+  if (!st || !st->q_prev || !st->sel_prev || st->step < 0) return KVR_ERR_INVALID_ARG;
+  if (!q_t || !summ || !corrected || !sel_used) return KVR_ERR_INVALID_ARG;
+  if (std::isnan(tau)) return KVR_ERR_INVALID_ARG;
+  if (!aligned16(st->q_prev) || !aligned16(st->sel_prev) || !aligned16(q_t) || !aligned16(summ) ||
+      !aligned16(sel_used) || (cbar_opt && !aligned16(cbar_opt)))
+    return KVR_ERR_ALIGN;
+  (void)dims;
+  return KVR_OK;
+}
+
+int kvr_speculative_select(const kvr_dims *dims, kvr_spec_state *st, const uint16_t *q_t,
+                           const uint16_t *summ, const int32_t *page_table, int32_t top_k,
+                           float tau, uint8_t *corrected, float *cbar_opt, int32_t *sel_used,
+                           int32_t *sel_used_phys, void *ws, size_t ws_bytes, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_topk(dims, top_k))) return rc;
+  if ((rc = check_spec(dims, st, q_t, summ, corrected, cbar_opt, sel_used, tau))) return rc;
+  if (!page_table) return KVR_ERR_INVALID_ARG;
+  if (!aligned16(page_table) || (sel_used_phys && !aligned16(sel_used_phys))) return KVR_ERR_ALIGN;
+  if ((rc = check_ws(ws, ws_bytes, select_ws_bytes(dims)))) return rc;
+  rc = spec_select_impl(dims, st, q_t, summ, page_table, top_k, tau, corrected, cbar_opt, sel_used,
+                        sel_used_phys, nullptr, 0, ws, static_cast<cudaStream_t>(stream));
+  if (rc == KVR_OK) st->step += 1;
+  return rc;
+}
+
+int kvr_speculative_step(const kvr_dims *dims, kvr_spec_state *st, const uint16_t *q_t,
+                         const uint16_t *summ, const int32_t *page_table, const uint16_t *k_pool,
+                         const uint16_t *v_pool, int32_t top_k, float tau, float scale,
+                         float *out, uint8_t *corrected, float *cbar_opt, int32_t *sel_used,
+                         int32_t *sel_used_phys, void *ws, size_t ws_bytes, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_topk(dims, top_k))) return rc;
+  if ((rc = check_spec(dims, st, q_t, summ, corrected, cbar_opt, sel_used, tau))) return rc;
+  if (!page_table || !k_pool || !v_pool || !out || !sel_used_phys) return KVR_ERR_INVALID_ARG;
+  if (!aligned16(page_table) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
+      !aligned16(sel_used_phys))
+    return KVR_ERR_ALIGN;
+  if (std::isnan(scale)) return KVR_ERR_INVALID_ARG;
+  if ((rc = check_ws(ws, ws_bytes, select_ws_bytes(dims) + attn_ws_bytes(dims, top_k)))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = spec_select_impl(dims, st, q_t, summ, page_table, top_k, tau, corrected, cbar_opt, sel_used,
+                        sel_used_phys, nullptr, 0, ws, s);
+  if (rc) return rc;
+  st->step += 1;
+  return launch_attn(dims, q_t, k_pool, v_pool, dims->n_phys_pages, sel_used_phys, top_k, scale,
+                     nullptr, 0, carve_attn(dims, top_k, (uint8_t *)ws + select_ws_bytes(dims)),
+                     out, s);
+}
+
+int kvr_working_set_reset(const kvr_dims *dims, const kvr_working_set *wset, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (!wset || !wset->page2slot || !wset->slot2page || wset->n_slots <= 0) return KVR_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t units = static_cast<size_t>(dims->batch) * dims->n_kv_heads;
+  cudaError_t e = cudaMemsetAsync(wset->page2slot, 0xff, units * dims->n_pages * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(wset->slot2page, 0xff, units * wset->n_slots * 4, s);
+  return e == cudaSuccess ? KVR_OK : cuda_fail(e, "working set reset");
+}
+
+int kvr_recall_pages(const kvr_dims *dims, const kvr_host_kv *host, const kvr_working_set *wset,
+                     const int32_t *sel_new, const int32_t *protect, const uint8_t *corrected,
+                     int32_t top_k, int32_t *sel_slot_out, uint32_t *n_copied_opt, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_topk(dims, top_k))) return rc;
+  if ((rc = check_wset(dims, wset, top_k))) return rc;
+  if (!host || !host->k_host || !host->v_host || !sel_new || !protect) return KVR_ERR_INVALID_ARG;
+  if (corrected && !sel_slot_out) return KVR_ERR_INVALID_ARG;
+  if (!aligned16(host->k_host) || !aligned16(host->v_host) || !aligned16(sel_new) ||
+      !aligned16(protect) || (sel_slot_out && !aligned16(sel_slot_out)))
+    return KVR_ERR_ALIGN;
+  return launch_recall(dims, host, wset, sel_new, protect, corrected, top_k, sel_slot_out,
+                       n_copied_opt, static_cast<cudaStream_t>(stream));
+}
+
+int kvr_speculative_step_recall(const kvr_dims *dims, kvr_spec_state *st, const uint16_t *q_t,
+                                const uint16_t *summ, const kvr_host_kv *host,
+                                const kvr_working_set *wset, int32_t top_k, float tau,
+                                float scale, float *out, uint8_t *corrected, float *cbar_opt,
+                                int32_t *sel_used, int32_t *sel_used_slot,
+                                uint32_t *n_copied_opt, void *ws, size_t ws_bytes, void *stream,
+                                void *side_stream, void *ev_select, void *ev_recall) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_topk(dims, top_k))) return rc;
+  if ((rc = check_spec(dims, st, q_t, summ, corrected, cbar_opt, sel_used, tau))) return rc;
+  if ((rc = check_wset(dims, wset, top_k))) return rc;
+  if (!host || !host->k_host || !host->v_host || !out || !sel_used_slot || !ev_select ||
+      !ev_recall)
+    return KVR_ERR_INVALID_ARG;
+  if (!aligned16(host->k_host) || !aligned16(host->v_host) || !aligned16(out) ||
+      !aligned16(sel_used_slot))
+    return KVR_ERR_ALIGN;
+  if (std::isnan(scale)) return KVR_ERR_INVALID_ARG;
+  if ((rc = check_ws(ws, ws_bytes, select_ws_bytes(dims) + attn_ws_bytes(dims, top_k)))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStream_t side = static_cast<cudaStream_t>(side_stream);
+  cudaEvent_t es = static_cast<cudaEvent_t>(ev_select), er = static_cast<cudaEvent_t>(ev_recall);
+
+  // 1. selection; reused heads get their (resident) slots from page2slot
+  rc = spec_select_impl(dims, st, q_t, summ, nullptr, top_k, tau,
+                        corrected, cbar_opt, sel_used, sel_used_slot, wset->page2slot,
+                        wset->n_slots, ws, s);
+  if (rc) return rc;
+  st->step += 1;
+  cudaError_t e = cudaEventRecord(es, s);
+  if (e != cudaSuccess) return cuda_fail(e, "record select event");
+  // 2. side stream: recall the new selection (now in sel_prev), protecting sel_used
+  e = cudaStreamWaitEvent(side, es, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "side stream wait");
+  rc = launch_recall(dims, host, wset, st->sel_prev, sel_used, corrected, top_k, sel_used_slot,
+                     n_copied_opt, side);
+  if (rc) return rc;
+  e = cudaEventRecord(er, side);
+  if (e != cudaSuccess) return cuda_fail(e, "record recall event");
+  // 3. attention: reused heads now, corrected heads once their pages are in
+  const int64_t n_phys = static_cast<int64_t>(dims->batch) * wset->n_slots;
+  const AttnWs aw = carve_attn(dims, top_k, (uint8_t *)ws + select_ws_bytes(dims));
+  rc = launch_attn(dims, q_t, wset->k_slots, wset->v_slots, n_phys, sel_used_slot, top_k, scale,
+                   corrected, 1, aw, out, s);
+  if (rc) return rc;
+  e = cudaStreamWaitEvent(s, er, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "main stream wait");
+  return launch_attn(dims, q_t, wset->k_slots, wset->v_slots, n_phys, sel_used_slot, top_k, scale,
+                     corrected, 2, aw, out, s);
+}
+
+int kvr_get_status(void *stream, uint32_t *status_out) {
+  if (!status_out) return KVR_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "status sync");
+  uint32_t v = 0;
+  e = cudaMemcpyFromSymbolAsync(&v, g_status, sizeof v, 0, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  const uint32_t zero = 0;
+  e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "status clear");
+  *status_out = v;
+  return KVR_OK;
+}
+
+const char *kvr_error_string(int code) {
+  switch (code) {
+    case KVR_OK: return "ok";
+    case KVR_ERR_INVALID_ARG: return "invalid argument (null pointer, bad size or enum)";
+    case KVR_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case KVR_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case KVR_ERR_WORKSPACE: return "workspace missing or too small";
+    case KVR_ERR_CUDA: return g_err_text[0] ? g_err_text : "CUDA error";
+    case KVR_ERR_TIMEOUT: return "host-side wait timed out";
+    default: return "unknown error code";
+  }
+}
+
+uint64_t kvr_kv_bytes(int64_t n_layers, int64_t n_kv_heads, int64_t head_dim, int64_t n_tokens,
+                      int64_t bytes_per_elem) {
+  if (n_layers < 0 || n_kv_heads < 0 || head_dim < 0 || n_tokens < 0 || bytes_per_elem < 0) return 0;
+  unsigned __int128 v = 2;
+  for (int64_t f : {n_layers, n_kv_heads, head_dim, n_tokens, bytes_per_elem}) {
+    v *= static_cast<unsigned __int128>(f);
+    if (v > static_cast<unsigned __int128>(UINT64_MAX)) return 0;
+  }
+  return static_cast<uint64_t>(v);
+}
+
+}  // extern "C"

@@ -1,0 +1,209 @@
+"""ctypes binding of libkvr (the C ABI declared in include/kvr.h).
+
+Argument marshalling only: every function here forwards to the entry point of
+the same name in ``libkvr.so``; all work runs in the library's CUDA kernels.
+Tensors are passed as torch tensors (device or pinned host memory, as the
+header states) or raw integer addresses; ``stream`` defaults to torch's
+current CUDA stream.  A non-zero return code raises :class:`KvrError`.
+
+There is no fallback: if ``libkvr.so`` has not been built, importing this
+module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libkvr.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "kvr.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m kv_cache_page_build_b300.build`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+
+def _header_constants():
+    out = {}
+    with open(HEADER) as f:
+        for m in re.finditer(r"#define\s+(KVR_\w+)\s+\(?(-?(?:0x)?[0-9a-fA-F]+)u?\)?", f.read()):
+            out[m.group(1)] = int(m.group(2), 0)
+    return out
+
+
+globals().update(_header_constants())
+
+
+class kvr_dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("batch", "n_q_heads", "n_kv_heads", "head_dim", "page_size", "n_pages", "n_phys_pages")]
+
+
+class kvr_spec_state(ctypes.Structure):
+    _fields_ = [("q_prev", ctypes.c_void_p), ("sel_prev", ctypes.c_void_p), ("step", ctypes.c_int32)]
+
+
+class kvr_host_kv(ctypes.Structure):
+    _fields_ = [("k_host", ctypes.c_void_p), ("v_host", ctypes.c_void_p)]
+
+
+class kvr_working_set(ctypes.Structure):
+    _fields_ = [("k_slots", ctypes.c_void_p), ("v_slots", ctypes.c_void_p),
+                ("page2slot", ctypes.c_void_p), ("slot2page", ctypes.c_void_p),
+                ("n_slots", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_S = ctypes.c_size_t
+_F = ctypes.c_float
+_D = ctypes.POINTER(kvr_dims)
+
+_SIGS = {
+    "kvr_workspace_size": (_S, [_D, _I, _I]),
+    "kvr_build_summaries": (_I, [_D, _P, _P, _P, _P]),
+    "kvr_select_pages": (_I, [_D, _P, _P, _P, _I, _P, _P, _P, _P, _S, _P]),
+    "kvr_sparse_decode_attn": (_I, [_D, _P, _P, _P, _P, _I, _F, _P, _P, _S, _P]),
+    "kvr_speculative_select": (_I, [_D, ctypes.POINTER(kvr_spec_state), _P, _P, _P, _I, _F,
+                                    _P, _P, _P, _P, _P, _S, _P]),
+    "kvr_speculative_step": (_I, [_D, ctypes.POINTER(kvr_spec_state), _P, _P, _P, _P, _P, _I, _F,
+                                  _F, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "kvr_working_set_reset": (_I, [_D, ctypes.POINTER(kvr_working_set), _P]),
+    "kvr_recall_pages": (_I, [_D, ctypes.POINTER(kvr_host_kv), ctypes.POINTER(kvr_working_set),
+                              _P, _P, _P, _I, _P, _P, _P]),
+    "kvr_speculative_step_recall": (_I, [_D, ctypes.POINTER(kvr_spec_state), _P, _P,
+                                         ctypes.POINTER(kvr_host_kv), ctypes.POINTER(kvr_working_set),
+                                         _I, _F, _F, _P, _P, _P, _P, _P, _P, _P, _S, _P, _P, _P, _P]),
+    "kvr_get_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
+    "kvr_error_string": (ctypes.c_char_p, [_I]),
+    "kvr_kv_bytes": (ctypes.c_uint64, [ctypes.c_int64] * 5),
+}
+
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class KvrError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {_lib.kvr_error_string(code).decode()} ({code})")
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return getattr(s, "cuda_stream", s)
+
+
+def _check(rc, where):
+    if rc != 0:
+        raise KvrError(rc, where)
+    return rc
+
+
+def dims(batch, n_q_heads, n_kv_heads, head_dim, page_size, n_pages, n_phys_pages) -> kvr_dims:
+    return kvr_dims(batch, n_q_heads, n_kv_heads, head_dim, page_size, n_pages, n_phys_pages)
+
+
+def _d(d):
+    return ctypes.byref(d if isinstance(d, kvr_dims) else kvr_dims(**d))
+
+
+def kvr_workspace_size(d, top_k, op) -> int:
+    return int(_lib.kvr_workspace_size(_d(d), int(top_k), int(op)))
+
+
+def kvr_build_summaries(d, k_pool, page_table, summ, stream=None):
+    return _check(_lib.kvr_build_summaries(_d(d), _ptr(k_pool), _ptr(page_table), _ptr(summ),
+                                           _stream(stream)), "kvr_build_summaries")
+
+
+def kvr_select_pages(d, q, summ, page_table, top_k, sel, sel_phys, scores_opt, ws, ws_bytes, stream=None):
+    return _check(_lib.kvr_select_pages(_d(d), _ptr(q), _ptr(summ), _ptr(page_table), int(top_k),
+                                        _ptr(sel), _ptr(sel_phys), _ptr(scores_opt), _ptr(ws),
+                                        int(ws_bytes), _stream(stream)), "kvr_select_pages")
+
+
+def kvr_sparse_decode_attn(d, q, k_pool, v_pool, sel_phys, top_k, scale, out, ws, ws_bytes, stream=None):
+    return _check(_lib.kvr_sparse_decode_attn(_d(d), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(sel_phys),
+                                              int(top_k), float(scale), _ptr(out), _ptr(ws), int(ws_bytes),
+                                              _stream(stream)), "kvr_sparse_decode_attn")
+
+
+def kvr_speculative_select(d, st, q_t, summ, page_table, top_k, tau, corrected, cbar_opt, sel_used,
+                           sel_used_phys, ws, ws_bytes, stream=None):
+    return _check(_lib.kvr_speculative_select(_d(d), ctypes.byref(st), _ptr(q_t), _ptr(summ),
+                                              _ptr(page_table), int(top_k), float(tau), _ptr(corrected),
+                                              _ptr(cbar_opt), _ptr(sel_used), _ptr(sel_used_phys), _ptr(ws),
+                                              int(ws_bytes), _stream(stream)), "kvr_speculative_select")
+
+
+def kvr_speculative_step(d, st, q_t, summ, page_table, k_pool, v_pool, top_k, tau, scale, out,
+                         corrected, cbar_opt, sel_used, sel_used_phys, ws, ws_bytes, stream=None):
+    return _check(_lib.kvr_speculative_step(_d(d), ctypes.byref(st), _ptr(q_t), _ptr(summ), _ptr(page_table),
+                                            _ptr(k_pool), _ptr(v_pool), int(top_k), float(tau), float(scale),
+                                            _ptr(out), _ptr(corrected), _ptr(cbar_opt), _ptr(sel_used),
+                                            _ptr(sel_used_phys), _ptr(ws), int(ws_bytes), _stream(stream)),
+                  "kvr_speculative_step")
+
+
+def kvr_working_set_reset(d, wset, stream=None):
+    return _check(_lib.kvr_working_set_reset(_d(d), ctypes.byref(wset), _stream(stream)),
+                  "kvr_working_set_reset")
+
+
+def kvr_recall_pages(d, host, wset, sel_new, protect, corrected, top_k, sel_slot_out, n_copied_opt,
+                     stream=None):
+    return _check(_lib.kvr_recall_pages(_d(d), ctypes.byref(host), ctypes.byref(wset), _ptr(sel_new),
+                                        _ptr(protect), _ptr(corrected), int(top_k), _ptr(sel_slot_out),
+                                        _ptr(n_copied_opt), _stream(stream)), "kvr_recall_pages")
+
+
+def kvr_speculative_step_recall(d, st, q_t, summ, host, wset, top_k, tau, scale, out, corrected,
+                                cbar_opt, sel_used, sel_used_slot, n_copied_opt, ws, ws_bytes,
+                                stream, side_stream, ev_select, ev_recall):
+    return _check(_lib.kvr_speculative_step_recall(
+        _d(d), ctypes.byref(st), _ptr(q_t), _ptr(summ), ctypes.byref(host), ctypes.byref(wset),
+        int(top_k), float(tau), float(scale), _ptr(out), _ptr(corrected), _ptr(cbar_opt), _ptr(sel_used),
+        _ptr(sel_used_slot), _ptr(n_copied_opt), _ptr(ws), int(ws_bytes), _stream(stream),
+        _stream(side_stream), _event(ev_select), _event(ev_recall)), "kvr_speculative_step_recall")
+
+
+def _event(e):
+    if e is None or isinstance(e, int):
+        return e
+    return e.cuda_event
+
+
+def kvr_get_status(stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _check(_lib.kvr_get_status(_stream(stream), ctypes.byref(v)), "kvr_get_status")
+    return int(v.value)
+
+
+def kvr_error_string(code: int) -> str:
+    return _lib.kvr_error_string(int(code)).decode()
+
+
+def kvr_kv_bytes(n_layers, n_kv_heads, head_dim, n_tokens, bytes_per_elem) -> int:
+    return int(_lib.kvr_kv_bytes(n_layers, n_kv_heads, head_dim, n_tokens, bytes_per_elem))
+
+
+def raw():
+    """The loaded ctypes library (for tests that call entry points directly)."""
+    return _lib

@@ -1,0 +1,151 @@
+"""The C ABI without a GPU: the library loads, exports every entry point the
+header declares, validates arguments before touching CUDA, and its sizing
+helpers follow their definitions."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+from kv_cache_page_build_b300 import build, kvr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "kvr.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvr_\w+)\s*\(", text)))
+
+
+def test_library_is_current_and_exports_every_declared_symbol():
+    assert build.up_to_date(), "libkvr.so is older than its sources"
+    names = declared_functions()
+    assert len(names) >= 12
+    lib = kvr.raw()
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in kvr._SIGS, f"binding lacks {n}"
+
+
+def test_error_strings():
+    for code in (kvr.KVR_OK, kvr.KVR_ERR_INVALID_ARG, kvr.KVR_ERR_UNSUPPORTED_SHAPE, kvr.KVR_ERR_ALIGN,
+                 kvr.KVR_ERR_WORKSPACE, kvr.KVR_ERR_CUDA, kvr.KVR_ERR_TIMEOUT):
+        assert kvr.kvr_error_string(code)
+    assert "unknown" in kvr.kvr_error_string(12345)
+
+
+def test_kv_bytes_matches_printed_llama65b_figure_and_overflow():
+    g = json.load(open(os.path.join(GOLDEN, "kv_cache_size_llama65b.json")))
+    n = kvr.kvr_kv_bytes(g["n_layers"], g["n_kv_heads"], g["head_dim"], g["n_tokens"], g["bytes_per_elem"])
+    assert abs(n / 1e9 - g["stated_gb"]) <= g["stated_rounding_gb"]
+    assert kvr.kvr_kv_bytes(1, 1, 1, 1, 1) == 2
+    assert kvr.kvr_kv_bytes(1 << 40, 1 << 40, 1, 1, 1) == 0
+    assert kvr.kvr_kv_bytes(-1, 1, 1, 1, 1) == 0
+
+
+def D(**kw):
+    base = dict(batch=8, n_q_heads=32, n_kv_heads=8, head_dim=128, page_size=32, n_pages=1024,
+                n_phys_pages=8192)
+    base.update(kw)
+    return kvr.kvr_dims(**base)
+
+
+def test_workspace_size_rules():
+    d = D()
+    sel = kvr.kvr_workspace_size(d, 64, kvr.KVR_OP_SELECT)
+    att = kvr.kvr_workspace_size(d, 64, kvr.KVR_OP_ATTN)
+    assert sel >= 8 * 8 * 1024 * 4 + 8 * 8 * 4
+    assert att >= 8 * 8 * (64 // 4) * 4 * 130 * 4      # partial (m, l, o) per split and head
+    assert kvr.kvr_workspace_size(d, 64, kvr.KVR_OP_STEP) == sel + att
+    assert kvr.kvr_workspace_size(d, 2000, kvr.KVR_OP_SELECT) == 0   # k > N
+    assert kvr.kvr_workspace_size(d, 64, 99) == 0
+    assert kvr.kvr_workspace_size(D(head_dim=64), 64, kvr.KVR_OP_SELECT) == 0
+
+
+BAD_SHAPES = [
+    (dict(head_dim=64), kvr.KVR_ERR_UNSUPPORTED_SHAPE),
+    (dict(n_q_heads=30), kvr.KVR_ERR_UNSUPPORTED_SHAPE),      # Hq % H != 0
+    (dict(n_q_heads=24), kvr.KVR_ERR_UNSUPPORTED_SHAPE),      # G = 3
+    (dict(page_size=8), kvr.KVR_ERR_UNSUPPORTED_SHAPE),
+    (dict(n_pages=20000), kvr.KVR_ERR_UNSUPPORTED_SHAPE),
+    (dict(batch=0), kvr.KVR_ERR_INVALID_ARG),
+    (dict(n_phys_pages=-1), kvr.KVR_ERR_INVALID_ARG),
+]
+
+FAKE = 1 << 20          # a 16-byte aligned address that is never dereferenced
+
+
+@pytest.mark.parametrize("kw,code", BAD_SHAPES)
+def test_bad_shapes_rejected_before_launch(kw, code):
+    lib = kvr.raw()
+    d = D(**kw)
+    assert lib.kvr_build_summaries(ctypes.byref(d), FAKE, FAKE, FAKE, None) == code
+    assert lib.kvr_select_pages(ctypes.byref(d), FAKE, FAKE, FAKE, 8, FAKE, FAKE, None, FAKE, 1 << 30, None) == code
+    assert lib.kvr_sparse_decode_attn(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, 8, 0.0, FAKE, FAKE, 1 << 30,
+                                      None) == code
+
+
+def test_bad_arguments_rejected_before_launch():
+    lib = kvr.raw()
+    d = D()
+    big = 1 << 40
+    # top_k out of range
+    assert lib.kvr_select_pages(ctypes.byref(d), FAKE, FAKE, FAKE, 0, FAKE, FAKE, None, FAKE, big, None) \
+        == kvr.KVR_ERR_INVALID_ARG
+    assert lib.kvr_select_pages(ctypes.byref(d), FAKE, FAKE, FAKE, 1025, FAKE, FAKE, None, FAKE, big, None) \
+        == kvr.KVR_ERR_UNSUPPORTED_SHAPE
+    # null and misaligned pointers
+    assert lib.kvr_select_pages(ctypes.byref(d), None, FAKE, FAKE, 8, FAKE, FAKE, None, FAKE, big, None) \
+        == kvr.KVR_ERR_INVALID_ARG
+    assert lib.kvr_select_pages(ctypes.byref(d), FAKE + 2, FAKE, FAKE, 8, FAKE, FAKE, None, FAKE, big, None) \
+        == kvr.KVR_ERR_ALIGN
+    assert lib.kvr_build_summaries(ctypes.byref(d), FAKE, FAKE + 4, FAKE, None) == kvr.KVR_ERR_ALIGN
+    assert lib.kvr_build_summaries(None, FAKE, FAKE, FAKE, None) == kvr.KVR_ERR_INVALID_ARG
+    # workspace missing or too small
+    need = kvr.kvr_workspace_size(d, 64, kvr.KVR_OP_SELECT)
+    assert lib.kvr_select_pages(ctypes.byref(d), FAKE, FAKE, FAKE, 64, FAKE, FAKE, None, None, need, None) \
+        == kvr.KVR_ERR_WORKSPACE
+    assert lib.kvr_select_pages(ctypes.byref(d), FAKE, FAKE, FAKE, 64, FAKE, FAKE, None, FAKE, need - 1, None) \
+        == kvr.KVR_ERR_WORKSPACE
+    need = kvr.kvr_workspace_size(d, 64, kvr.KVR_OP_ATTN)
+    assert lib.kvr_sparse_decode_attn(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, 64, 0.0, FAKE, FAKE, need - 1,
+                                      None) == kvr.KVR_ERR_WORKSPACE
+    assert lib.kvr_sparse_decode_attn(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, 64, float("nan"), FAKE, FAKE,
+                                      need, None) == kvr.KVR_ERR_INVALID_ARG
+
+
+def test_speculative_and_recall_arguments_rejected_before_launch():
+    lib = kvr.raw()
+    d = D()
+    big = 1 << 40
+    st = kvr.kvr_spec_state(FAKE, FAKE, 0)
+    # missing state buffers, negative step
+    bad = kvr.kvr_spec_state(None, FAKE, 0)
+    assert lib.kvr_speculative_select(ctypes.byref(d), ctypes.byref(bad), FAKE, FAKE, FAKE, 64, 0.8, FAKE, None,
+                                      FAKE, FAKE, FAKE, big, None) == kvr.KVR_ERR_INVALID_ARG
+    neg = kvr.kvr_spec_state(FAKE, FAKE, -1)
+    assert lib.kvr_speculative_select(ctypes.byref(d), ctypes.byref(neg), FAKE, FAKE, FAKE, 64, 0.8, FAKE, None,
+                                      FAKE, FAKE, FAKE, big, None) == kvr.KVR_ERR_INVALID_ARG
+    assert lib.kvr_speculative_select(ctypes.byref(d), ctypes.byref(st), FAKE, FAKE, FAKE, 64, float("nan"),
+                                      FAKE, None, FAKE, FAKE, FAKE, big, None) == kvr.KVR_ERR_INVALID_ARG
+    # the full step needs sel_used_phys and a step-sized workspace
+    assert lib.kvr_speculative_step(ctypes.byref(d), ctypes.byref(st), FAKE, FAKE, FAKE, FAKE, FAKE, 64, 0.8, 0.0,
+                                    FAKE, FAKE, None, FAKE, None, FAKE, big, None) == kvr.KVR_ERR_INVALID_ARG
+    sel_only = kvr.kvr_workspace_size(d, 64, kvr.KVR_OP_SELECT)
+    assert lib.kvr_speculative_step(ctypes.byref(d), ctypes.byref(st), FAKE, FAKE, FAKE, FAKE, FAKE, 64, 0.8, 0.0,
+                                    FAKE, FAKE, None, FAKE, FAKE, FAKE, sel_only, None) == kvr.KVR_ERR_WORKSPACE
+    assert st.step == 0
+    # working set too small for double buffering
+    host = kvr.kvr_host_kv(FAKE, FAKE)
+    ws = kvr.kvr_working_set(FAKE, FAKE, FAKE, FAKE, 127)
+    assert lib.kvr_recall_pages(ctypes.byref(d), ctypes.byref(host), ctypes.byref(ws), FAKE, FAKE, None, 64,
+                                None, None, None) == kvr.KVR_ERR_UNSUPPORTED_SHAPE
+    ws.n_slots = 128
+    assert lib.kvr_recall_pages(ctypes.byref(d), ctypes.byref(host), ctypes.byref(ws), FAKE, FAKE, FAKE, 64,
+                                None, None, None) == kvr.KVR_ERR_INVALID_ARG   # corrected without output
+    ws.k_slots = FAKE + 8
+    assert lib.kvr_recall_pages(ctypes.byref(d), ctypes.byref(host), ctypes.byref(ws), FAKE, FAKE, None, 64,
+                                None, None, None) == kvr.KVR_ERR_ALIGN

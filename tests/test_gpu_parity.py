@@ -1,0 +1,198 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle on the
+seeded workloads: summaries value-exact, selections bit-exact, attention
+within 2e-3 max-abs and 1e-3 relative L2."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kv_cache_page_build_b300 import kvr, synth
+from tests import gpuhelp as gh
+
+pytestmark = pytest.mark.gpu
+
+_CACHE = {}
+
+
+def accepted_case(cid):
+    """Workload cid's cache and query, redrawn until every top-k boundary has
+    a score margin of at least 1e-3 (so fp32 and fp64 selections agree)."""
+    if cid not in _CACHE:
+        wl = synth.WORKLOADS[cid]
+        case = synth.make_case(wl, accept=oracle.accept_single_step(wl.top_k))
+        _CACHE[cid] = (case, gh.DevCase(case), oracle.summaries(case.k_pool, case.page_table))
+    return _CACHE[cid]
+
+
+def small_case(**kw):
+    base = dict(batch=2, n_q_heads=8, n_kv_heads=2, head_dim=128, page_size=32, n_pages=150, top_k=21)
+    base.update(kw)
+    wl = synth.custom(**base)
+    case = synth.make_case(wl, accept=oracle.accept_single_step(wl.top_k))
+    return case, gh.DevCase(case)
+
+
+@pytest.fixture(autouse=True)
+def _status_clean():
+    kvr.kvr_get_status()
+    yield
+    assert kvr.kvr_get_status() == 0
+
+
+# ---------------------------------------------------------------- summaries
+
+@pytest.mark.parametrize("cid", [1, 2, 3])
+def test_summaries_value_exact(cid):
+    case, dc, (kmin, kmax) = accepted_case(cid)
+    s = gh.f64(dc.summaries())                       # [B][H][N][2][D]
+    np.testing.assert_array_equal(s[:, :, :, 0], kmin)
+    np.testing.assert_array_equal(s[:, :, :, 1], kmax)
+
+
+# ---------------------------------------------------------------- selection
+
+@pytest.mark.parametrize("cid", [1, 2, 3])
+def test_selection_bit_exact_and_scores_within_bound(cid):
+    case, dc, summ = accepted_case(cid)
+    wl = case.wl
+    sel, sel_phys, scores = gh.select(dc)
+    s_ref = oracle.scores(case.q, *summ)
+    want = oracle.topk(s_ref, wl.top_k)
+    np.testing.assert_array_equal(sel.cpu().numpy(), want)
+    np.testing.assert_array_equal(sel_phys.cpu().numpy(), np.take_along_axis(
+        case.page_table[:, None, :].repeat(wl.n_kv_heads, 1), want, axis=2))
+    tol = gh.score_tolerance(case.q, *summ, wl.group)
+    err = np.abs(scores.cpu().numpy().astype(np.float64) - s_ref)
+    assert np.all(err <= tol), f"worst score error {err.max():.3g} vs bound {tol[err == err.max()][0]:.3g}"
+
+
+def test_tie_goes_to_lower_page_id():
+    """Two pages with bitwise-identical keys straddle the top-k boundary: the
+    lower page id is selected, by the oracle and by the GPU."""
+    wl = synth.custom(batch=1, n_q_heads=4, n_kv_heads=1, head_dim=128, page_size=16, n_pages=200, top_k=17)
+    case = synth.make_case(wl)
+    s = oracle.scores(case.q, *oracle.summaries(case.k_pool, case.page_table))[0, 0]
+    order = np.argsort(-s, kind="stable")
+    # a boundary with clear margins on both sides of the tied pair
+    k = next(k for k in range(8, 60) if s[order[k - 2]] - s[order[k - 1]] >= 1e-3
+             and s[order[k - 1]] - s[order[k]] >= 1e-3)
+    kth = order[k - 1]
+    low = [p for p in order[k + 5:] if p < kth]
+    high = [p for p in order[k + 5:] if p > kth]
+    targets = ([low[-1]] if low else []) + ([high[-1]] if high else [])
+    assert targets
+    for target in targets:
+        c2 = synth.Case(**{**case.__dict__, "k_pool": case.k_pool.copy()})
+        c2.k_pool[c2.page_table[0, target]] = c2.k_pool[c2.page_table[0, kth]]
+        summ = oracle.summaries(c2.k_pool, c2.page_table)
+        want = oracle.topk(oracle.scores(c2.q, *summ), k)[0, 0]
+        lo, hi = min(kth, target), max(kth, target)
+        assert lo in want and hi not in want
+        dc = gh.DevCase(c2)
+        sel, _, scores = gh.select(dc, top_k=k)
+        np.testing.assert_array_equal(sel.cpu().numpy()[0, 0], want)
+        sc = scores.cpu().numpy()[0, 0]
+        assert sc[kth] == sc[target]
+
+
+# ---------------------------------------------------------------- attention
+
+@pytest.mark.parametrize("cid", [1, 2, 3])
+def test_attention_on_oracle_selection(cid):
+    case, dc, summ = accepted_case(cid)
+    wl = case.wl
+    sel = oracle.topk(oracle.scores(case.q, *summ), wl.top_k)
+    ref = oracle.attention(case.q, case.k_pool, case.v_pool, case.page_table, sel)
+    phys = np.take_along_axis(case.page_table[:, None, :].repeat(wl.n_kv_heads, 1), sel, axis=2)
+    out = gh.attention(dc, torch.from_numpy(np.ascontiguousarray(phys)).cuda())
+    gh.assert_attn_close(out.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("cid", [1, 2, 3])
+def test_decode_step_end_to_end(cid):
+    """Selection and attention chained on the device, against the oracle step."""
+    case, dc, summ = accepted_case(cid)
+    sel_ref, _, out_ref = oracle.decode_step(case.q, case.k_pool, case.v_pool, case.page_table,
+                                             case.wl.n_kv_heads, case.wl.top_k, summ=summ)
+    sel, sel_phys, _ = gh.select(dc)
+    out = gh.attention(dc, sel_phys)
+    np.testing.assert_array_equal(sel.cpu().numpy(), sel_ref)
+    gh.assert_attn_close(out.cpu().numpy(), out_ref)
+
+
+SHAPES = [
+    dict(),                                                   # ragged chunk (150 pages) and split (21 pages)
+    dict(page_size=16, n_pages=97, top_k=33),
+    dict(page_size=64, n_pages=70, top_k=5),
+    dict(n_q_heads=2, n_kv_heads=2, top_k=9),                  # G = 1
+    dict(n_q_heads=8, n_kv_heads=4, top_k=12),                 # G = 2
+    dict(n_q_heads=16, n_kv_heads=2, top_k=30, n_pages=64),    # G = 8
+    dict(top_k=150),                                           # k = N: dense attention
+    dict(top_k=1, batch=3),
+    dict(n_pages=1, top_k=1, page_size=16),
+    dict(channel_scale=True, n_pages=300, top_k=40),
+]
+
+
+@pytest.mark.parametrize("kw", SHAPES, ids=[str(i) for i in range(len(SHAPES))])
+def test_small_shapes_and_edges(kw):
+    case, dc = small_case(**kw)
+    wl = case.wl
+    summ = oracle.summaries(case.k_pool, case.page_table)
+    sel_ref, _, out_ref = oracle.decode_step(case.q, case.k_pool, case.v_pool, case.page_table,
+                                             wl.n_kv_heads, wl.top_k, summ=summ)
+    s = gh.f64(dc.summaries())
+    np.testing.assert_array_equal(s[:, :, :, 0], summ[0])
+    np.testing.assert_array_equal(s[:, :, :, 1], summ[1])
+    sel, sel_phys, _ = gh.select(dc)
+    np.testing.assert_array_equal(sel.cpu().numpy(), sel_ref)
+    out = gh.attention(dc, sel_phys)
+    gh.assert_attn_close(out.cpu().numpy(), out_ref)
+
+
+def test_explicit_scale():
+    case, dc = small_case()
+    wl = case.wl
+    sel_ref, _, _ = oracle.decode_step(case.q, case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads, wl.top_k)
+    ref = oracle.attention(case.q, case.k_pool, case.v_pool, case.page_table, sel_ref, scale=0.05)
+    _, sel_phys, _ = gh.select(dc)
+    gh.assert_attn_close(gh.attention(dc, sel_phys, scale=0.05).cpu().numpy(), ref)
+
+
+def test_repeatable_and_workspace_left_zeroed():
+    """Five runs on poisoned outputs give bitwise-identical results (so the
+    ticket counters were reset), and the counters end at zero."""
+    case, dc, _ = accepted_case(2)
+    ws_s = gh.workspace(dc.dims, case.wl.top_k, kvr.KVR_OP_SELECT)
+    ws_a = gh.workspace(dc.dims, case.wl.top_k, kvr.KVR_OP_ATTN)
+    first = None
+    for _ in range(5):
+        sel, sel_phys, sc = gh.select(dc, ws=ws_s)
+        out = gh.attention(dc, sel_phys, ws=ws_a)
+        cur = (sel.cpu().numpy(), sc.cpu().numpy(), out.cpu().numpy())
+        if first is None:
+            first = cur
+        for a, b in zip(first, cur):
+            np.testing.assert_array_equal(a, b)
+    units = case.wl.batch * case.wl.n_kv_heads
+    tail = (units * 4 + 255) // 256 * 256          # the counters are the last region of each workspace
+    assert int(ws_s[-tail:].count_nonzero()) == 0
+    assert int(ws_a[-tail:].count_nonzero()) == 0
+
+
+def test_out_of_range_page_is_skipped_and_reported():
+    case, dc = small_case()
+    wl = case.wl
+    sel_ref, _, _ = oracle.decode_step(case.q, case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads, wl.top_k)
+    _, sel_phys, _ = gh.select(dc)
+    bad = sel_phys.clone()
+    bad[0, 0, 3] = dc.dims.n_phys_pages + 5
+    out = gh.attention(dc, bad)
+    assert kvr.kvr_get_status() & kvr.KVR_ST_BAD_INDEX
+    # the row attends over the remaining pages only
+    fewer = np.delete(sel_ref[:1], 3, axis=2)       # unit (0, 0) without its 4th page
+    ref = oracle.attention(case.q[:1], case.k_pool, case.v_pool, case.page_table[:1], fewer)
+    gh.assert_attn_close(out.cpu().numpy()[0, :wl.group], ref[0, :wl.group])
+    # the other units are unaffected
+    ref_all = oracle.attention(case.q, case.k_pool, case.v_pool, case.page_table, sel_ref)
+    gh.assert_attn_close(out.cpu().numpy()[:, wl.group:], ref_all[:, wl.group:])

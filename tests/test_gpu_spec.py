@@ -1,0 +1,181 @@
+"""Speculative decode (reuse + correction) and streamed recall from a host
+cache, through the C ABI, against the oracle's speculative trace."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kv_cache_page_build_b300 import kvr, synth
+from tests import gpuhelp as gh
+from tests.test_gpu_parity import accepted_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _status_clean():
+    kvr.kvr_get_status()
+    yield
+    assert kvr.kvr_get_status() == 0
+
+
+_TRACES = {}
+
+
+def accepted_trace(cid):
+    """Workload cid's query trace with both margins (top-k boundary, |C - tau|)
+    of at least 1e-3 at every step, and the oracle's speculative run of it."""
+    if cid not in _TRACES:
+        wl = synth.WORKLOADS[cid]
+        case, dc, summ = accepted_case(wl.cache_of)
+        tr = synth.make_trace(wl, case, accept=oracle.accept_trace_step(summ, wl.n_kv_heads, wl.top_k, wl.tau))
+        ref = oracle.speculative_trace(tr.q, case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads,
+                                       wl.top_k, wl.tau, summ=summ)
+        _TRACES[cid] = (wl, case, dc, tr, ref)
+    return _TRACES[cid]
+
+
+class SpecRun:
+    """Device state and outputs of a speculative run."""
+
+    def __init__(self, wl, dc):
+        B, Hq, H, D, k = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.top_k
+        self.q_prev = torch.zeros((B, Hq, D), dtype=torch.int16, device="cuda")
+        self.sel_prev = torch.zeros((B, H, k), dtype=torch.int32, device="cuda")
+        self.st = kvr.kvr_spec_state(self.q_prev.data_ptr(), self.sel_prev.data_ptr(), 0)
+        self.out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
+        self.corrected = torch.empty((B, H), dtype=torch.uint8, device="cuda")
+        self.cbar = torch.empty((B, H), dtype=torch.float32, device="cuda")
+        self.sel_used = torch.empty((B, H, k), dtype=torch.int32, device="cuda")
+        self.sel_used_phys = torch.empty((B, H, k), dtype=torch.int32, device="cuda")
+        self.ws = gh.workspace(dc.dims, k, kvr.KVR_OP_STEP)
+        self.wl, self.dc = wl, dc
+
+    def step(self, q_t):
+        wl, dc = self.wl, self.dc
+        self.out.fill_(float("nan"))
+        self.sel_used.fill_(-7)
+        kvr.kvr_speculative_step(dc.dims, self.st, q_t, dc.summaries(), dc.page_table, dc.k_pool, dc.v_pool,
+                                 wl.top_k, wl.tau, 0.0, self.out, self.corrected, self.cbar, self.sel_used,
+                                 self.sel_used_phys, self.ws, self.ws.numel())
+
+
+def test_speculative_trace_matches_oracle():
+    wl, case, dc, tr, ref = accepted_trace(4)
+    qs = gh.t16(tr.q)
+    run = SpecRun(wl, dc)
+    for t in range(wl.steps):
+        run.step(qs[t])
+        assert run.st.step == t + 1
+        corr = run.corrected.cpu().numpy().astype(bool)
+        np.testing.assert_array_equal(corr, ref["corrected"][t], err_msg=f"step {t}")
+        np.testing.assert_array_equal(run.sel_used.cpu().numpy(), ref["sel_used"][t], err_msg=f"step {t}")
+        np.testing.assert_array_equal(run.sel_prev.cpu().numpy(), ref["sel_new"][t], err_msg=f"step {t}")
+        np.testing.assert_array_equal(run.sel_used_phys.cpu().numpy(), np.take_along_axis(
+            case.page_table[:, None, :].repeat(wl.n_kv_heads, 1), ref["sel_used"][t], axis=2))
+        if t > 0:
+            assert np.max(np.abs(run.cbar.cpu().numpy() - ref["cbar"][t])) < 1e-5
+        else:
+            assert np.all(np.isnan(run.cbar.cpu().numpy()))
+        gh.assert_attn_close(run.out.cpu().numpy(), ref["out"][t])
+    # the trace exercises both branches of the decision
+    assert ref["corrected"][1:].any() and not ref["corrected"][1:].all()
+    for t in tr.jumps:
+        assert ref["corrected"][t].all()
+
+
+def test_speculative_state_checkpoint_resume():
+    """Saving (q_prev, sel_prev, step) at step 31 and resuming from it
+    reproduces steps 32..63 bit for bit."""
+    wl, case, dc, tr, ref = accepted_trace(4)
+    qs = gh.t16(tr.q)
+    run = SpecRun(wl, dc)
+    saved, outs = None, []
+    for t in range(wl.steps):
+        if t == 32:
+            saved = (run.q_prev.clone(), run.sel_prev.clone(), run.st.step)
+        run.step(qs[t])
+        if t >= 32:
+            outs.append((run.out.clone(), run.sel_used.clone(), run.corrected.clone()))
+    again = SpecRun(wl, dc)
+    again.q_prev.copy_(saved[0])
+    again.sel_prev.copy_(saved[1])
+    again.st.step = saved[2]
+    for i, t in enumerate(range(32, wl.steps)):
+        again.step(qs[t])
+        for a, b in zip(outs[i], (again.out, again.sel_used, again.corrected)):
+            assert torch.equal(a, b), f"step {t}"
+
+
+def test_speculative_select_alone_matches_step():
+    wl, case, dc, tr, ref = accepted_trace(4)
+    qs = gh.t16(tr.q)
+    run = SpecRun(wl, dc)
+    ws = gh.workspace(dc.dims, wl.top_k, kvr.KVR_OP_SELECT)
+    for t in range(6):
+        kvr.kvr_speculative_select(dc.dims, run.st, qs[t], dc.summaries(), dc.page_table, wl.top_k, wl.tau,
+                                   run.corrected, None, run.sel_used, run.sel_used_phys, ws, ws.numel())
+        np.testing.assert_array_equal(run.sel_used.cpu().numpy(), ref["sel_used"][t])
+        np.testing.assert_array_equal(run.corrected.cpu().numpy().astype(bool), ref["corrected"][t])
+
+
+# ---------------------------------------------------------------- host-resident cache
+
+def test_recall_trace_matches_oracle_and_hbm_path():
+    wl, case, dc, tr, ref = accepted_trace(5)
+    B, Hq, H, D, P, N, k = (wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.page_size, wl.n_pages,
+                            wl.top_k)
+    S = 2 * k
+    kh, vh = synth.host_hnd(case)
+    k_host = torch.from_numpy(kh.view(np.int16)).pin_memory()
+    v_host = torch.from_numpy(vh.view(np.int16)).pin_memory()
+    del kh, vh
+    k_slots = torch.zeros((B, S, P, H, D), dtype=torch.int16, device="cuda")
+    v_slots = torch.zeros_like(k_slots)
+    p2s = torch.empty((B, H, N), dtype=torch.int32, device="cuda")
+    s2p = torch.empty((B, H, S), dtype=torch.int32, device="cuda")
+    host = kvr.kvr_host_kv(k_host.data_ptr(), v_host.data_ptr())
+    wset = kvr.kvr_working_set(k_slots.data_ptr(), v_slots.data_ptr(), p2s.data_ptr(), s2p.data_ptr(), S)
+    kvr.kvr_working_set_reset(dc.dims, wset)
+    run = SpecRun(wl, dc)
+    sel_used_slot = torch.empty((B, H, k), dtype=torch.int32, device="cuda")
+    n_copied = torch.zeros(1, dtype=torch.int32, device="cuda")
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    ev_s, ev_r = torch.cuda.Event(), torch.cuda.Event()
+    ev_s.record()                                  # torch creates the CUDA event on first record
+    ev_r.record()
+    qs = gh.t16(tr.q)
+    ws_a = gh.workspace(dc.dims, k, kvr.KVR_OP_ATTN)
+    bidx = torch.arange(B, device="cuda")[:, None, None]
+    gidx = torch.arange(H, device="cuda")[None, :, None]
+    for t in range(wl.steps):
+        run.out.fill_(float("nan"))
+        kvr.kvr_speculative_step_recall(dc.dims, run.st, qs[t], dc.summaries(), host, wset, k, wl.tau, 0.0,
+                                        run.out, run.corrected, run.cbar, run.sel_used, sel_used_slot, n_copied,
+                                        run.ws, run.ws.numel(), main, side, ev_s, ev_r)
+        torch.cuda.synchronize()
+        if t == 0:
+            assert int(n_copied.item()) == B * H * k        # cold start: the whole first selection
+        np.testing.assert_array_equal(run.corrected.cpu().numpy().astype(bool), ref["corrected"][t])
+        np.testing.assert_array_equal(run.sel_used.cpu().numpy(), ref["sel_used"][t])
+        gh.assert_attn_close(run.out.cpu().numpy(), ref["out"][t])
+        # the same selection read from the HBM-resident pool gives the same bits
+        phys = torch.gather(dc.page_table[:, None, :].expand(B, H, N), 2, run.sel_used.long())
+        hbm = gh.attention(dc, phys.contiguous(), q=qs[t], ws=ws_a)
+        assert torch.equal(hbm, run.out), f"step {t}"
+        # every resident slot holds exactly its page, and maps agree both ways
+        s2p_now = s2p.long()
+        resident = s2p_now >= 0
+        pages = s2p_now.clamp(min=0)
+        assert torch.equal(torch.gather(p2s.long(), 2, pages)[resident],
+                           torch.arange(S, device="cuda").expand(B, H, S)[resident])
+        phys_res = dc.page_table.long()[bidx.squeeze(-1), pages.reshape(B, -1)].reshape(B, H, S)
+        want_k = dc.k_pool[phys_res, :, gidx, :]                       # [B][H][S][P][D]
+        got_k = k_slots.permute(0, 3, 1, 2, 4)                         # [B][H][S][P][D]
+        assert torch.equal(got_k[resident], want_k[resident])
+        want_v = dc.v_pool[phys_res, :, gidx, :]
+        assert torch.equal(v_slots.permute(0, 3, 1, 2, 4)[resident], want_v[resident])
+        # the pages used by this step are resident where sel_used_slot says
+        slot_of_used = sel_used_slot.long() - bidx * S
+        assert torch.equal(torch.gather(s2p_now, 2, slot_of_used), run.sel_used.long())
