@@ -63,6 +63,7 @@ extern "C" {
 #define KVR_ERR_WORKSPACE (-4)         /* workspace missing or too small */
 #define KVR_ERR_CUDA (-5)              /* a CUDA call or launch failed */
 #define KVR_ERR_TIMEOUT (-6)           /* a host-side wait ran past its deadline */
+#define KVR_ERR_SCRATCH_LIMIT (-7)     /* needs more than KVR_NOALLOC_SCRATCH_BYTES */
 
 /* status-word bits set by kernels */
 #define KVR_ST_BAD_INDEX 0x1u     /* a page id outside its pool was skipped */
@@ -253,6 +254,35 @@ const char *kvr_error_string(int code);
  * negative argument. */
 uint64_t kvr_kv_bytes(int64_t n_layers, int64_t n_kv_heads, int64_t head_dim,
                       int64_t n_tokens, int64_t bytes_per_elem);
+
+/* Allocation-free page selection.  The pages have no counterpart to this
+ * entry point: it exists for callers that cannot allocate device memory,
+ * such as an inference-engine plugin whose enqueue step may only use the
+ * buffers it was handed, a serving loop that forbids allocation after
+ * warm-up to keep latency flat, or a foreign-language caller with no access
+ * to the process's device allocator.  It computes exactly what
+ * kvr_select_pages computes (same kernel, same results), but its scratch
+ * (the fp32 score rows and ticket counters) lives in a fixed array of
+ * KVR_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library keeps until the process exits.  The caller still passes all
+ * inputs and outputs (q, summ, page_table, sel, sel_phys, scores_opt as in
+ * kvr_select_pages).
+ *   - Limit: B * H * N * 4 bytes of scores plus the counters must fit in
+ *     KVR_NOALLOC_SCRATCH_BYTES (about one million page scores); larger
+ *     problems return KVR_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current) and caches it; make that first call before
+ *     any stream capture.
+ *   - Every call clears the counters it needs on `stream`, then launches.
+ *     All calls share the one array: calls that overlap on the GPU (on
+ *     different streams, or from several threads) race and must be
+ *     serialised by the caller.
+ * It never calls cudaMalloc, cudaFree or any allocating routine. */
+#define KVR_NOALLOC_SCRATCH_BYTES 4194304u /* 4 MiB */
+int kvr_select_pages_noalloc(const kvr_dims *dims, const uint16_t *q,
+                             const uint16_t *summ, const int32_t *page_table,
+                             int32_t top_k, int32_t *sel, int32_t *sel_phys,
+                             float *scores_opt, void *stream);
 
 #ifdef __cplusplus
 }

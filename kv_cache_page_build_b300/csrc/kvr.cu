@@ -566,6 +566,8 @@ const char *kvr_error_string(int code) {
     case KVR_ERR_WORKSPACE: return "workspace missing or too small";
     case KVR_ERR_CUDA: return g_err_text[0] ? g_err_text : "CUDA error";
     case KVR_ERR_TIMEOUT: return "host-side wait timed out";
+    case KVR_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than the fixed array of the allocation-free entry point";
     default: return "unknown error code";
   }
 }
@@ -582,3 +584,62 @@ uint64_t kvr_kv_bytes(int64_t n_layers, int64_t n_kv_heads, int64_t head_dim, in
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free selection
+//
+// kvr_select_pages_noalloc: the selection kernel with its scratch (score rows
+// and ticket counters) in this fixed device array instead of a caller
+// workspace, for callers that may not allocate device memory.  Host code
+// must not pass the array's name to a kernel (on the host it only stands in
+// for the symbol); the device address is looked up once per device below.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[KVR_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up on
+// the first call per device, then cached).
+int noalloc_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return KVR_ERR_UNSUPPORTED_SHAPE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "scratch symbol address");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return KVR_OK;
+}
+
+}  // namespace
+
+extern "C" int kvr_select_pages_noalloc(const kvr_dims *dims, const uint16_t *q,
+                                        const uint16_t *summ, const int32_t *page_table,
+                                        int32_t top_k, int32_t *sel, int32_t *sel_phys,
+                                        float *scores_opt, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_topk(dims, top_k))) return rc;
+  if (!q || !summ || !page_table || !sel) return KVR_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(summ) || !aligned16(page_table) || !aligned16(sel) ||
+      (sel_phys && !aligned16(sel_phys)) || (scores_opt && !aligned16(scores_opt)))
+    return KVR_ERR_ALIGN;
+  const size_t need = select_ws_bytes(dims);
+  if (need > KVR_NOALLOC_SCRATCH_BYTES) return KVR_ERR_SCRATCH_LIMIT;
+  void *scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const SelectWs w = carve_select(dims, static_cast<uint8_t *>(scratch));
+  // the ticket counters must start at zero (a previous call may have been cut short)
+  const size_t units = static_cast<size_t>(dims->batch) * dims->n_kv_heads;
+  const cudaError_t e = cudaMemsetAsync(w.count, 0, units * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return cuda_fail(e, "clear scratch counters");
+  return launch_select(dims, q, summ, page_table, top_k, w, sel, sel_phys, scores_opt, no_spec(),
+                       st);
+}

@@ -77,6 +77,7 @@ _SIGS = {
                                          ctypes.POINTER(kvr_host_kv), ctypes.POINTER(kvr_working_set),
                                          _I, _F, _F, _P, _P, _P, _P, _P, _P, _P, _S, _P, _P, _P, _P]),
     "kvr_get_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
+    "kvr_select_pages_noalloc": (_I, [_D, _P, _P, _P, _I, _P, _P, _P, _P]),
     "kvr_error_string": (ctypes.c_char_p, [_I]),
     "kvr_kv_bytes": (ctypes.c_uint64, [ctypes.c_int64] * 5),
 }
@@ -188,6 +189,14 @@ def _event(e):
     if e is None or isinstance(e, int):
         return e
     return e.cuda_event
+
+
+def kvr_select_pages_noalloc(d, q, summ, page_table, top_k, sel, sel_phys, scores_opt, stream=None):
+    """kvr_select_pages without a caller workspace (scratch is a fixed array in
+    the library; see include/kvr.h for the size limit and the sharing rule)."""
+    return _check(_lib.kvr_select_pages_noalloc(_d(d), _ptr(q), _ptr(summ), _ptr(page_table), int(top_k),
+                                                _ptr(sel), _ptr(sel_phys), _ptr(scores_opt), _stream(stream)),
+                  "kvr_select_pages_noalloc")
 
 
 def kvr_get_status(stream=None) -> int:
