@@ -6,6 +6,7 @@
 // compute is in the kernels of the included .cuh files.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -85,7 +86,7 @@ struct SelectWs {
 };
 struct AttnWs {
   float *part_o;
-  float *part_ml;
+  float2 *part_ml;
   uint32_t *count;
 };
 
@@ -94,12 +95,19 @@ size_t select_ws_bytes(const kvr_dims *d) {
   return align_up(units * d->n_pages * sizeof(float)) + align_up(units * sizeof(uint32_t));
 }
 
+// Partial slots of the attention merge: a CTA's segment of unit u goes to
+// slot cta + u, so kAttnMaxCtas + units slots cover every grid size.
+size_t attn_slots(const kvr_dims *d) {
+  return static_cast<size_t>(kAttnMaxCtas) + static_cast<size_t>(d->batch) * d->n_kv_heads;
+}
+
 size_t attn_ws_bytes(const kvr_dims *d, int top_k) {
+  (void)top_k;
   const size_t units = static_cast<size_t>(d->batch) * d->n_kv_heads;
   const size_t G = d->n_q_heads / d->n_kv_heads;
-  const size_t splits = attn_splits(top_k, d->page_size);
-  return align_up(units * splits * G * kD * sizeof(float)) +
-         align_up(units * splits * G * 2 * sizeof(float)) + align_up(units * sizeof(uint32_t));
+  const size_t slots = attn_slots(d);
+  return align_up(slots * G * kD * sizeof(float)) + align_up(slots * G * sizeof(float2)) +
+         align_up(units * sizeof(uint32_t));
 }
 
 SelectWs carve_select(const kvr_dims *d, uint8_t *p) {
@@ -111,14 +119,14 @@ SelectWs carve_select(const kvr_dims *d, uint8_t *p) {
 }
 
 AttnWs carve_attn(const kvr_dims *d, int top_k, uint8_t *p) {
-  const size_t units = static_cast<size_t>(d->batch) * d->n_kv_heads;
+  (void)top_k;
   const size_t G = d->n_q_heads / d->n_kv_heads;
-  const size_t splits = attn_splits(top_k, d->page_size);
+  const size_t slots = attn_slots(d);
   AttnWs w;
   w.part_o = reinterpret_cast<float *>(p);
-  p += align_up(units * splits * G * kD * sizeof(float));
-  w.part_ml = reinterpret_cast<float *>(p);
-  p += align_up(units * splits * G * 2 * sizeof(float));
+  p += align_up(slots * G * kD * sizeof(float));
+  w.part_ml = reinterpret_cast<float2 *>(p);
+  p += align_up(slots * G * sizeof(float2));
   w.count = reinterpret_cast<uint32_t *>(p);
   return w;
 }
@@ -168,18 +176,29 @@ int make_pool_map(CUtensorMap *map, const void *pool, const kvr_dims *d, int64_t
 
 // ---------------------------------------------------------------- launches
 
+int sm_count(int *out);
+
 template <int G>
 int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
                     const int32_t *ptab, int k, SelectWs w, int32_t *sel, int32_t *sel_phys,
                     float *scores, const SpecArgs &spec, cudaStream_t st) {
-  const int n_chunks = (d->n_pages + kSelChunk - 1) / kSelChunk;
-  const size_t smem = std::max<size_t>(kSelStageBytes, static_cast<size_t>(d->n_pages) * 4);
+  const size_t smem = kSelSmem;
   auto kern = k_score_select<G>;
   static int max_set[kMaxDevices] = {};
   if (int rc = ensure_smem(reinterpret_cast<const void *>(kern), smem, max_set)) return rc;
-  const dim3 grid(n_chunks, d->n_kv_heads, d->batch);
-  kern<<<grid, kSelThreads, smem, st>>>(q, summ, ptab, d->n_kv_heads, d->n_pages, k, n_chunks,
-                                        w.scores, w.count, sel, sel_phys, scores, spec);
+  // splits per (b, g) row: about two resident CTAs per SM over all rows, at
+  // least one 32-page stage per CTA
+  int sms = 0;
+  if (int rc = sm_count(&sms)) return rc;
+  const long long units = static_cast<long long>(d->batch) * d->n_kv_heads;
+  const long long per_sm = G <= 4 ? 2 : 1;
+  long long n_split = sms * per_sm / units;
+  n_split = std::max<long long>(1, std::min<long long>(
+                                       n_split, (d->n_pages + kSelStagePages - 1) / kSelStagePages));
+  const dim3 grid(static_cast<unsigned>(n_split), d->n_kv_heads, d->batch);
+  kern<<<grid, kSelThreads, smem, st>>>(q, summ, ptab, d->n_kv_heads, d->n_pages, k,
+                                        static_cast<int>(n_split), w.scores, w.count, sel,
+                                        sel_phys, scores, spec);
   return check_launch("k_score_select");
 }
 
@@ -194,20 +213,50 @@ int launch_select(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
   }
 }
 
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count(int *out) {
+  static int cached[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return KVR_ERR_UNSUPPORTED_SHAPE;
+  if (cached[dev] == 0) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "multiprocessor count");
+    cached[dev] = n;
+  }
+  *out = cached[dev];
+  return KVR_OK;
+}
+
+// Persistent grid of the attention kernel: one CTA per SM, at least
+// kAttnMinPagesPerCta pages per CTA, at most kAttnMaxCtas CTAs.
+int attn_grid(long long W, int *n_ctas) {
+  int sms = 0;
+  if (int rc = sm_count(&sms)) return rc;
+  long long n = std::min<long long>(sms, (W + kAttnMinPagesPerCta - 1) / kAttnMinPagesPerCta);
+  n = std::max<long long>(1, std::min<long long>(n, kAttnMaxCtas));
+  if ((W + n - 1) / n >= (1LL << 31)) return KVR_ERR_UNSUPPORTED_SHAPE;
+  *n_ctas = static_cast<int>(n);
+  return KVR_OK;
+}
+
 template <int G, int P>
 int launch_attn_gp(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &tv,
                    const uint16_t *q, const int32_t *sel_phys, int k, int n_phys, float scale,
                    const uint8_t *filter, int filter_mode, AttnWs w, float *out, cudaStream_t st) {
-  const int n_splits = attn_splits(k, P);
-  const size_t smem = 2 * static_cast<size_t>(kAttnTileBytes) + kAttnTokens * G * sizeof(float);
+  const long long W = static_cast<long long>(d->batch) * d->n_kv_heads * k;
+  int n_ctas = 0;
+  if (int rc = attn_grid(W, &n_ctas)) return rc;
+  const size_t smem = AttnCfg<G, P>::kSmem;
   auto kern = k_sparse_decode<G, P>;
   static int max_set[kMaxDevices] = {};
   if (int rc = ensure_smem(reinterpret_cast<const void *>(kern), smem, max_set)) return rc;
   const float scale_log2 = scale * 1.4426950408889634f;
-  const dim3 grid(n_splits, d->n_kv_heads, d->batch);
-  kern<<<grid, kAttnThreads, smem, st>>>(tk, tv, q, sel_phys, d->n_kv_heads, k, n_phys, n_splits,
-                                         scale_log2, filter, filter_mode, w.part_o, w.part_ml,
-                                         w.count, out);
+  kern<<<n_ctas, AttnCfg<G, P>::kThreads, smem, st>>>(tk, tv, q, sel_phys, d->n_kv_heads, k, n_phys, W,
+                                           scale_log2, filter, filter_mode, w.part_o, w.part_ml,
+                                           w.count, out);
   return check_launch("k_sparse_decode");
 }
 

@@ -13,33 +13,44 @@
 // otherwise; with q+ = max(q, 0) and q- = min(q, 0) the term is
 // fma(q+, kmax, fma(q-, kmin, .)) where one of the two products is an exact
 // zero, so each channel adds exactly one exact bf16 x bf16 product to an fp32
-// accumulator.  Every page is reduced in the same fixed order (8 channels
-// per lane in order, G heads pairwise, then a 16-lane butterfly), so two
-// pages with equal summaries get bitwise-equal scores.
+// accumulator.  Every page is reduced in the same fixed order (channel pairs
+// into two interleaved accumulators with packed FFMA2, the pair summed, G
+// heads pairwise, then a 16-lane butterfly), so two pages with equal
+// summaries get bitwise-equal scores.
 //
-// Layout of work.  Grid (chunks, H, B).  A CTA scores 64 consecutive pages of
-// one (b, g): it pulls their 64 x 512-byte summaries into shared memory with
-// four 8 KiB bulk copies (one mbarrier each) and a half-warp scores one page
-// at a time (lane = 8 channels, 16-byte shared loads of the min and max
-// rows).  Scores go to an fp32 workspace row; the CTA that finishes the
-// (b, g) row last (atomic ticket, no waiting) selects the top k.
+// Layout of work.  Grid (splits, H, B): the N pages of a (b, g) row are cut
+// into `splits` contiguous ranges, about two CTAs per SM in total.  A CTA's
+// summaries are one contiguous byte range; its producer warp streams them
+// with 1D bulk copies (32 pages = 16 KiB per copy) into a ring of stages,
+// and the 8 consumer warps score every stage together (a half-warp per page,
+// lane = 8 channels of the min and max rows).  Scores go to an fp32
+// workspace row; the CTA that finishes the (b, g) row last (atomic ticket,
+// no waiting) selects the top k.
 //
-// Top-k.  Scores map to order-preserving 32-bit keys (-0 folded into +0).  A
-// most-significant-digit radix select (8-bit digits, shared-memory
-// histograms) finds the k-th largest key; pages above it are selected, and
-// among pages equal to it the lowest ids fill the remaining places (ties to
-// the lower page id).  An ordered compaction writes the ids ascending.
+// Top-k.  Scores map to order-preserving 32-bit keys (-0 folded into +0).
+// The k-th largest key lies in a key interval [L, R], first [min, max].  A
+// round cuts the interval into at most 2048 bins of 2^shift consecutive keys,
+// histograms the keys inside it, and keeps the bin that holds the k-th
+// largest (the keys of higher bins are selected).  Rounds repeat until the
+// kept bin holds exactly as many keys as are still needed, or one key value
+// only; among keys equal to that value the lowest page ids are taken (ties
+// to the lower page id).  An ordered compaction writes the ids ascending.
 #pragma once
 
 #include "common.cuh"
 
 namespace kvr {
 
-constexpr int kSelThreads = 256;
-constexpr int kSelChunk = 64;                   // pages per scoring CTA
-constexpr int kSummBytes = 2 * kD * 2;          // bytes of one page summary
-constexpr int kSelStageBytes = kSelChunk * kSummBytes;  // 32 KiB
-static_assert(kSelThreads == 256, "one histogram bin per thread");
+constexpr int kSelConsumers = 8;                        // consumer warps
+constexpr int kSelCT = 32 * kSelConsumers;              // consumer threads
+constexpr int kSelThreads = kSelCT + 32;                // + one producer warp
+constexpr int kSelStagePages = 32;                      // pages per bulk copy
+constexpr int kSummBytes = 2 * kD * 2;                  // bytes of one page summary
+constexpr int kSelStageBytes = kSelStagePages * kSummBytes;  // 16 KiB
+constexpr int kSelStages = 6;
+constexpr int kSelSmem = kSelStages * kSelStageBytes;   // 96 KiB: also holds N <= 16384 keys
+constexpr int kSelBins = 2048;
+static_assert(kSelSmem >= kMaxPages * 4, "the top-k keys reuse the stage ring");
 
 struct SpecArgs {
   int enabled;                 // 0: plain selection
@@ -60,161 +71,250 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Exclusive prefix sum over the kSelCT consumer threads (named barrier 1);
+// `scratch` holds kSelConsumers words.  Also returns the total.
+__device__ __forceinline__ uint32_t sel_exclusive_scan(uint32_t v, uint32_t *scratch,
+                                                       uint32_t &total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  named_bar_sync(1, kSelCT);
+  uint32_t base = 0u, tot = 0u;
+#pragma unroll
+  for (int w = 0; w < kSelConsumers; ++w) {
+    const uint32_t x = scratch[w];
+    base += w < warp ? x : 0u;
+    tot += x;
+  }
+  total = tot;
+  named_bar_sync(1, kSelCT);  // scratch free again
+  return base + incl - v;
+}
+
 template <int G>
-__global__ void __launch_bounds__(kSelThreads)
+__global__ void __launch_bounds__(kSelThreads, (G <= 4 ? 2 : 1))
     k_score_select(const uint16_t *__restrict__ q, const uint16_t *__restrict__ summ,
-                   const int32_t *__restrict__ page_table, int H, int N, int k, int n_chunks,
+                   const int32_t *__restrict__ page_table, int H, int N, int k, int n_split,
                    float *__restrict__ ws_scores, uint32_t *__restrict__ ws_count,
                    int32_t *__restrict__ sel_out, int32_t *__restrict__ sel_phys_out,
                    float *__restrict__ scores_out, SpecArgs spec) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[4];
-  __shared__ uint32_t s_hist[256];
-  __shared__ uint32_t s_scan[kSelThreads / 32];
-  __shared__ uint32_t s_prefix, s_mask, s_need, s_done, s_last, s_corr;
+  __shared__ __align__(8) uint64_t full[kSelStages], empty[kSelStages];
+  __shared__ uint32_t s_hist[kSelBins];
+  __shared__ uint32_t s_scan[kSelConsumers];
+  __shared__ uint32_t s_mm[2 * kSelConsumers];
+  __shared__ uint32_t s_bin, s_bin_above, s_bin_cnt, s_last, s_corr;
   __shared__ float s_cos[8];
+  __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = blockIdx.y, b = blockIdx.z;
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int Hq = H * G;
   const size_t unit = static_cast<size_t>(b) * H + g;
-  const int p0 = blockIdx.x * kSelChunk;
-  const int np = min(kSelChunk, N - p0);
+  const int p0 = static_cast<int>(static_cast<long long>(split) * N / n_split);
+  const int p1 = static_cast<int>(static_cast<long long>(split + 1) * N / n_split);
+  const int np = p1 - p0;
+  const int n_stages = (np + kSelStagePages - 1) / kSelStagePages;
 
-  // ---- stage the chunk's summaries (4 bulk copies of up to 16 pages)
   if (tid == 0) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+    for (int s = 0; s < kSelStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kSelConsumers);
+    }
+    s_abort = 0;
     fence_barrier_init();
-    const uint8_t *src = reinterpret_cast<const uint8_t *>(summ) + (unit * N + p0) * kSummBytes;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int cnt = min(16, np - 16 * i);
-      if (cnt > 0) {
-        const uint32_t bytes = static_cast<uint32_t>(cnt) * kSummBytes;
-        mbar_arrive_expect_tx(&bars[i], bytes);
-        bulk_copy_g2s(smem + i * 16 * kSummBytes, src + i * 16 * kSummBytes, bytes, &bars[i]);
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------ producer warp
+  if (warp == kSelConsumers) {
+    if (lane == 0) {
+      const uint8_t *src = reinterpret_cast<const uint8_t *>(summ) + (unit * N + p0) * kSummBytes;
+      int issued = 0;
+      bool abort = false;
+#pragma unroll 1
+      for (int j = 0; j < n_stages; ++j) {
+        const int s = j % kSelStages, use = j / kSelStages;
+        if (use > 0 && !mbar_wait(&empty[s], static_cast<uint32_t>((use - 1) & 1))) abort = true;
+        if (s_abort) abort = true;
+        if (abort) {
+          s_abort = 1;
+          break;
+        }
+        const uint32_t bytes =
+            static_cast<uint32_t>(min(kSelStagePages, np - j * kSelStagePages)) * kSummBytes;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_copy_g2s(smem + s * kSelStageBytes,
+                      src + static_cast<size_t>(j) * kSelStageBytes, bytes, &full[s]);
+        issued = j + 1;
+      }
+      if (abort) {  // never leave with copies in flight
+#pragma unroll 1
+        for (int j = max(0, issued - kSelStages); j < issued; ++j)
+          mbar_wait(&full[j % kSelStages], static_cast<uint32_t>((j / kSelStages) & 1));
       }
     }
+    return;
   }
 
-  // ---- this lane's query channels: 8 channels (8*sub .. 8*sub+7) of each head
-  const int hw = tid >> 4, sub = tid & 15;
-  float qp[G][8], qn[G][8];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const uint4 raw = *reinterpret_cast<const uint4 *>(
-        q + (static_cast<size_t>(b) * Hq + g * G + h) * kD + 8 * sub);
-    float x[8];
-    unpack8(raw, x);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      qp[h][c] = fmaxf(x[c], 0.0f);
-      qn[h][c] = fminf(x[c], 0.0f);
-    }
-  }
-  __syncthreads();  // barrier initialisation visible to all threads
-
-  // ---- score: half-warp hw takes page 16*i + hw of the chunk
-  bool timed_out = false;
-#pragma unroll 1
-  for (int i = 0; i < 4; ++i) {
-    if (16 * i >= np) break;  // uniform over the CTA
-    if (!mbar_wait(&bars[i], 0)) timed_out = true;
-    const int pl = 16 * i + hw;
-    const uint8_t *pg = smem + pl * kSummBytes;  // rows beyond np are never written out
-    float kmin[8], kmax[8];
-    unpack8(*reinterpret_cast<const uint4 *>(pg + 16 * sub), kmin);
-    unpack8(*reinterpret_cast<const uint4 *>(pg + kD * 2 + 16 * sub), kmax);
-    float acc[G];
+  // ------------------------------------------------------------ consumer warps: scores
+  const int ct = tid;
+  {
+    // this lane's query channels: 8 channels (8*sub .. 8*sub+7) of each head, as
+    // sign-split pairs
+    const int hw = ct >> 4, sub = ct & 15;
+    float2 qp[G][4], qn[G][4];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      float a = 0.0f;
+      const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
+          q + (static_cast<size_t>(b) * Hq + g * G + h) * kD + 8 * sub));
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        a = fmaf(qp[h][c], kmax[c], a);
-        a = fmaf(qn[h][c], kmin[c], a);
+      for (int j = 0; j < 4; ++j) {
+        const float2 x = bf2_to_f2(w[j]);
+        qp[h][j] = make_float2(fmaxf(x.x, 0.0f), fmaxf(x.y, 0.0f));
+        qn[h][j] = make_float2(fminf(x.x, 0.0f), fminf(x.y, 0.0f));
       }
-      acc[h] = a;
     }
+    float *srow = ws_scores + unit * N + p0;
+    float *orow = scores_out ? scores_out + unit * N + p0 : nullptr;
+#pragma unroll 1
+    for (int j = 0; j < n_stages; ++j) {
+      const int s = j % kSelStages;
+      bool have = false;
+      if (__shfl_sync(0xffffffffu, s_abort, 0) == 0) {  // warp-uniform
+        const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((j / kSelStages) & 1));
+        if (__all_sync(0xffffffffu, ok)) {
+          have = true;
+        } else if (lane == 0) {
+          s_abort = 1;
+        }
+      }
+      if (have) {
+        const uint8_t *stage = smem + s * kSelStageBytes;
 #pragma unroll
-    for (int w = 1; w < G; w <<= 1)
+        for (int r = 0; r < 2; ++r) {
+          const int pl = j * kSelStagePages + hw + 16 * r;  // page within this CTA's range
+          const uint8_t *pg = stage + (hw + 16 * r) * kSummBytes;  // rows past np never written out
+          const uint4 mn = *reinterpret_cast<const uint4 *>(pg + 16 * sub);
+          const uint4 mx = *reinterpret_cast<const uint4 *>(pg + kD * 2 + 16 * sub);
+          const uint32_t wn[4] = {mn.x, mn.y, mn.z, mn.w};
+          const uint32_t wx[4] = {mx.x, mx.y, mx.z, mx.w};
+          float2 acc2[G];
 #pragma unroll
-      for (int h = 0; h < G; h += 2 * w) acc[h] += acc[h + w];
-    float tot = acc[0];
+          for (int h = 0; h < G; ++h) acc2[h] = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int m = 8; m >= 1; m >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, m);
-    if (sub == 0 && pl < np) ws_scores[unit * N + p0 + pl] = tot * (1.0f / G);
-  }
-  if (timed_out) {  // never leave the CTA with copies in flight
-    for (int i = 0; i < 4; ++i)
-      if (16 * i < np) mbar_wait(&bars[i], 0);
+          for (int c = 0; c < 4; ++c) {
+            const float2 kmin = bf2_to_f2(wn[c]), kmax = bf2_to_f2(wx[c]);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              acc2[h] = __ffma2_rn(qp[h][c], kmax, acc2[h]);
+              acc2[h] = __ffma2_rn(qn[h][c], kmin, acc2[h]);
+            }
+          }
+          float acc[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) acc[h] = acc2[h].x + acc2[h].y;
+#pragma unroll
+          for (int w = 1; w < G; w <<= 1)
+#pragma unroll
+            for (int h = 0; h < G; h += 2 * w) acc[h] += acc[h + w];
+          float tot = acc[0];
+#pragma unroll
+          for (int m = 8; m >= 1; m >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, m);
+          if (sub == 0 && pl < np) {
+            const float sc = tot * (1.0f / G);
+            srow[pl] = sc;
+            if (orow) orow[pl] = sc;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
   }
 
   // ---- last CTA of this (b, g) row selects
   __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(&ws_count[unit], 1u) == static_cast<uint32_t>(n_chunks - 1));
-  __syncthreads();
+  named_bar_sync(1, kSelCT);
+  if (ct == 0) s_last = (atomicAdd(&ws_count[unit], 1u) == static_cast<uint32_t>(n_split - 1));
+  named_bar_sync(1, kSelCT);
   if (!s_last) return;
   __threadfence();
 
-  uint32_t *keys = reinterpret_cast<uint32_t *>(smem);  // the staging area is free now
-  for (int i = tid; i < N; i += kSelThreads) {
-    const float s = __ldcg(ws_scores + unit * N + i);
-    keys[i] = score_key(s);
-    if (scores_out) scores_out[unit * N + i] = s;
+  // keys of the whole row (the stage ring is idle now) and their range
+  uint32_t *keys = reinterpret_cast<uint32_t *>(smem);
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
+  for (int i = ct; i < N; i += kSelCT) {
+    const uint32_t key = score_key(__ldcg(ws_scores + unit * N + i));
+    keys[i] = key;
+    kmn = min(kmn, key);
+    kmx = max(kmx, key);
   }
-  if (tid == 0) ws_count[unit] = 0u;  // leave the workspace zeroed
-  __syncthreads();
-
-  // radix select of the k-th largest key: prefix/mask = digits fixed so far,
-  // need = how many of the keys matching the prefix still have to be taken
-  uint32_t prefix = 0u, mask = 0u, need = static_cast<uint32_t>(k);
+  if (ct == 0) ws_count[unit] = 0u;  // leave the workspace zeroed
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    kmn = min(kmn, __shfl_xor_sync(0xffffffffu, kmn, m));
+    kmx = max(kmx, __shfl_xor_sync(0xffffffffu, kmx, m));
+  }
+  if (lane == 0) {
+    s_mm[warp] = kmn;
+    s_mm[kSelConsumers + warp] = kmx;
+  }
+  named_bar_sync(1, kSelCT);
+  uint32_t L = 0xffffffffu, R = 0u;
+#pragma unroll
+  for (int w = 0; w < kSelConsumers; ++w) {
+    L = min(L, s_mm[w]);
+    R = max(R, s_mm[kSelConsumers + w]);
+  }
+  // invariant: `need` of the `cnt` keys in [L, R] are still to be taken;
+  // every key above R is taken
+  uint32_t need = static_cast<uint32_t>(k), cnt = static_cast<uint32_t>(N);
 #pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    s_hist[tid] = 0u;  // kSelThreads == 256 bins
-    __syncthreads();
-    for (int i = tid; i < N; i += kSelThreads) {
+  while (cnt != need && L != R) {
+    const uint32_t span = R - L;
+    const int shift = span < kSelBins ? 0 : (32 - __clz(span)) - 11;
+    for (int i = ct; i < kSelBins; i += kSelCT) s_hist[i] = 0u;
+    named_bar_sync(1, kSelCT);
+    for (int i = ct; i < N; i += kSelCT) {
       const uint32_t key = keys[i];
-      if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1u);
+      if (key >= L && key <= R) atomicAdd(&s_hist[(key - L) >> shift], 1u);
     }
-    __syncthreads();
-    if (warp == 0) {
-      uint32_t c[8], sum = 0u;
+    named_bar_sync(1, kSelCT);
+    // thread ct owns bins [8 ct, 8 ct + 8); find the bin holding the need-th largest
+    uint32_t c[kSelBins / kSelCT], mine = 0u;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        c[i] = s_hist[255 - 8 * lane - i];  // lane 0 holds the highest digits
-        sum += c[i];
-      }
-      uint32_t incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const uint32_t excl = incl - sum;
-      if (excl < need && need <= incl) {
-        uint32_t above = excl;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (above + c[i] >= need) {
-            const uint32_t digit = static_cast<uint32_t>(255 - 8 * lane - i);
-            s_prefix = prefix | (digit << shift);
-            s_mask = mask | (255u << shift);
-            s_need = need - above;
-            s_done = (c[i] == need - above) ? 1u : 0u;
-            break;
-          }
-          above += c[i];
-        }
-      }
+    for (int e = 0; e < kSelBins / kSelCT; ++e) {
+      c[e] = s_hist[(kSelBins / kSelCT) * ct + e];
+      mine += c[e];
     }
-    __syncthreads();
-    prefix = s_prefix;
-    mask = s_mask;
-    need = s_need;
-    if (s_done) break;  // every key with this prefix is taken
+    uint32_t total;
+    const uint32_t below = sel_exclusive_scan(mine, s_scan, total);
+    uint32_t above_here = total - below - mine;  // keys of the interval in higher bins
+#pragma unroll
+    for (int e = kSelBins / kSelCT - 1; e >= 0; --e) {
+      if (above_here < need && need <= above_here + c[e]) {
+        s_bin = static_cast<uint32_t>((kSelBins / kSelCT) * ct + e);
+        s_bin_above = above_here;
+        s_bin_cnt = c[e];
+      }
+      above_here += c[e];
+    }
+    named_bar_sync(1, kSelCT);
+    const uint32_t nl = L + (s_bin << shift);
+    const unsigned long long nr = static_cast<unsigned long long>(nl) + ((1ull << shift) - 1ull);
+    need -= s_bin_above;
+    cnt = s_bin_cnt;
+    R = static_cast<uint32_t>(min(static_cast<unsigned long long>(R), nr));
+    L = nl;
+    named_bar_sync(1, kSelCT);  // s_bin* and s_hist free for the next round
   }
 
   // ---- speculative mode: group similarity and the correction decision
@@ -242,8 +342,8 @@ __global__ void __launch_bounds__(kSelThreads)
       }
       if (lane == 0) s_cos[warp] = (nx > 0.f && ny > 0.f) ? dot / (sqrtf(nx) * sqrtf(ny)) : 0.f;
     }
-    __syncthreads();
-    if (tid == 0) {
+    named_bar_sync(1, kSelCT);
+    if (ct == 0) {
       float cb = __int_as_float(0x7fc00000);  // NaN: no previous query at step 0
       bool corr = true;
       if (spec.step > 0) {
@@ -256,15 +356,15 @@ __global__ void __launch_bounds__(kSelThreads)
       spec.corrected[unit] = corr ? 1 : 0;
       if (spec.cbar) spec.cbar[unit] = cb;
     }
-    __syncthreads();
+    named_bar_sync(1, kSelCT);
     corrected = s_corr != 0u;
     // q_prev <- q_t for this group's heads (only this CTA reads them)
-    for (int i = tid; i < G * kD / 8; i += kSelThreads) {
+    for (int i = ct; i < G * kD / 8; i += kSelCT) {
       const size_t off = (static_cast<size_t>(b) * Hq + g * G) * kD + 8 * i;
       *reinterpret_cast<uint4 *>(spec.q_prev + off) = *reinterpret_cast<const uint4 *>(q + off);
     }
     if (!corrected) {  // reuse: sel_used <- previous selection (before it is replaced)
-      for (int i = tid; i < k; i += kSelThreads) {
+      for (int i = ct; i < k; i += kSelCT) {
         const int p = spec.sel_prev[unit * k + i];
         spec.sel_used[unit * k + i] = p;
         if (spec.sel_used_phys) {
@@ -279,28 +379,30 @@ __global__ void __launch_bounds__(kSelThreads)
         }
       }
     }
-    __syncthreads();
+    named_bar_sync(1, kSelCT);
   }
 
-  // ---- ordered compaction of the selection (ascending page ids)
-  const int per = (N + kSelThreads - 1) / kSelThreads;
-  const int beg = min(N, tid * per), end = min(N, beg + per);
+  // ---- ordered compaction of the selection (ascending page ids): every key
+  // above R, then the first `need` keys of [L, R] by page id (all of them
+  // when cnt == need)
+  const int per = (N + kSelCT - 1) / kSelCT;
+  const int beg = min(N, ct * per), end = min(N, beg + per);
   uint32_t n_gt = 0u, n_eq = 0u;
   for (int i = beg; i < end; ++i) {
-    const uint32_t m = keys[i] & mask;
-    n_gt += (m > prefix);
-    n_eq += (m == prefix);
+    const uint32_t key = keys[i];
+    n_gt += (key > R);
+    n_eq += (key >= L && key <= R);
   }
   uint32_t total;
-  const uint32_t eq_base = block_exclusive_scan<kSelThreads>(n_eq, s_scan, total);
+  const uint32_t eq_base = sel_exclusive_scan(n_eq, s_scan, total);
   uint32_t n_take = n_gt;
   for (uint32_t e = 0; e < n_eq; ++e) n_take += (eq_base + e < need);
-  uint32_t out = block_exclusive_scan<kSelThreads>(n_take, s_scan, total);
+  uint32_t out = sel_exclusive_scan(n_take, s_scan, total);
   uint32_t eq_seen = 0u;
   for (int i = beg; i < end; ++i) {
-    const uint32_t m = keys[i] & mask;
-    bool take = m > prefix;
-    if (m == prefix) take = (eq_base + eq_seen++) < need;
+    const uint32_t key = keys[i];
+    bool take = key > R;
+    if (key >= L && key <= R) take = (eq_base + eq_seen++) < need;
     if (!take) continue;
     if (out >= static_cast<uint32_t>(k)) break;  // never write past this unit's k entries
     const size_t o = unit * k + out++;
