@@ -37,7 +37,6 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode steps/s and selected-KV GB/s (fraction of B300 HBM peak) per layer"
 WORKLOADS = {"llama3.1-8b-32k": (2, 4), "qwen3-4b-128k": (3, 5)}  # (cache workload, trace workload)
-TRACE_LEN = 64
 
 
 def peaks():
@@ -151,7 +150,7 @@ def cpu_baseline(wl_name: str, seconds: float = 12.0):
     wl = case.wl
     n, t0 = 0, time.perf_counter()
     while True:
-        oracle.decode_step(tr.q[n % TRACE_LEN], case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads,
+        oracle.decode_step(tr.q[n % tr.q.shape[0]], case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads,
                            wl.top_k, summ=summ)
         n += 1
         el = time.perf_counter() - t0
@@ -208,7 +207,8 @@ def run_gpu(args, world, rank, local):
     k_pools = [to_dev(case.k_pool.view(np.int16)) for _ in range(COPIES)]
     v_pools = [to_dev(case.v_pool.view(np.int16)) for _ in range(COPIES)]
     page_table = to_dev(case.page_table)
-    qs = to_dev(tr.q.view(np.int16))                               # [64][B][Hq][D]
+    qs = to_dev(tr.q.view(np.int16))                               # [T][B][Hq][D]
+    TRACE_LEN = qs.shape[0]
     summs = [torch.empty((B, H, N, 2, D), dtype=torch.int16, device=dev) for _ in range(COPIES)]
     del case
 

@@ -74,6 +74,10 @@ int ensure_smem(const void *kern, size_t bytes, int *max_set) {
   if (max_set[dev] >= static_cast<int>(bytes)) return KVR_OK;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
   if (e != cudaSuccess) return cuda_fail(e, "dynamic shared memory attribute");
+  // prefer the largest shared-memory carveout, so several such CTAs fit per SM
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return cuda_fail(e, "shared memory carveout attribute");
   max_set[dev] = static_cast<int>(bytes);
   return KVR_OK;
 }
@@ -95,10 +99,10 @@ size_t select_ws_bytes(const kvr_dims *d) {
   return align_up(units * d->n_pages * sizeof(float)) + align_up(units * sizeof(uint32_t));
 }
 
-// Partial slots of the attention merge: a CTA's segment of unit u goes to
-// slot cta + u, so kAttnMaxCtas + units slots cover every grid size.
+// Partial slots of the attention merge: worker v's segment of unit u goes to
+// slot v + u, so kAttnMaxWorkers + units slots cover every grid size.
 size_t attn_slots(const kvr_dims *d) {
-  return static_cast<size_t>(kAttnMaxCtas) + static_cast<size_t>(d->batch) * d->n_kv_heads;
+  return static_cast<size_t>(kAttnMaxWorkers) + static_cast<size_t>(d->batch) * d->n_kv_heads;
 }
 
 size_t attn_ws_bytes(const kvr_dims *d, int top_k) {
@@ -147,8 +151,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// The pool [n_phys][P][H][D] bf16 viewed as [tokens][H][D]; one box is one
-// head's P consecutive token rows of a page (D x 1 x P elements).
+// The pool [n_phys][P][H][D] bf16 viewed as [tokens][H][D]; one box is 64
+// channels of one head over min(P, 32) consecutive token rows, written to
+// shared memory with 128-byte swizzling (the attention kernel's chunk halves).
 int make_pool_map(CUtensorMap *map, const void *pool, const kvr_dims *d, int64_t n_phys) {
   auto fn = encode_fn();
   if (!fn) {
@@ -159,12 +164,11 @@ int make_pool_map(CUtensorMap *map, const void *pool, const kvr_dims *d, int64_t
                               static_cast<cuuint64_t>(n_phys * d->page_size)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
                                  static_cast<cuuint64_t>(d->n_kv_heads) * kD * 2};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), 1u,
-                             static_cast<cuuint32_t>(d->page_size)};
+  const cuuint32_t box[3] = {64u, 1u, static_cast<cuuint32_t>(std::min(d->page_size, 32))};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   const CUresult r =
       fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box,
-         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     std::snprintf(g_err_text, sizeof g_err_text, "cuTensorMapEncodeTiled failed (%d)",
@@ -230,12 +234,13 @@ int sm_count(int *out) {
   return KVR_OK;
 }
 
-// Persistent grid of the attention kernel: one CTA per SM, at least
-// kAttnMinPagesPerCta pages per CTA, at most kAttnMaxCtas CTAs.
-int attn_grid(long long W, int *n_ctas) {
+// Grid of the attention kernel: `per_sm` resident CTAs per SM, at least
+// kAttnMinChunksPerWorker chunks per consumer warp, at most kAttnMaxCtas CTAs.
+int attn_grid(long long W, int per_sm, int *n_ctas) {
   int sms = 0;
   if (int rc = sm_count(&sms)) return rc;
-  long long n = std::min<long long>(sms, (W + kAttnMinPagesPerCta - 1) / kAttnMinPagesPerCta);
+  const long long per_cta = static_cast<long long>(kAttnMinChunksPerWorker) * kAttnNC;
+  long long n = std::min<long long>(static_cast<long long>(sms) * per_sm, (W + per_cta - 1) / per_cta);
   n = std::max<long long>(1, std::min<long long>(n, kAttnMaxCtas));
   if ((W + n - 1) / n >= (1LL << 31)) return KVR_ERR_UNSUPPORTED_SHAPE;
   *n_ctas = static_cast<int>(n);
@@ -246,18 +251,38 @@ template <int G, int P>
 int launch_attn_gp(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &tv,
                    const uint16_t *q, const int32_t *sel_phys, int k, int n_phys, float scale,
                    const uint8_t *filter, int filter_mode, AttnWs w, float *out, cudaStream_t st) {
-  const long long W = static_cast<long long>(d->batch) * d->n_kv_heads * k;
+  using Cfg = AttnCfg<G, P>;
+  const long long units = static_cast<long long>(d->batch) * d->n_kv_heads;
+  const long long kc = static_cast<long long>(k) * Cfg::CPP;
+  const long long W = units * kc;
   int n_ctas = 0;
-  if (int rc = attn_grid(W, &n_ctas)) return rc;
-  const size_t smem = AttnCfg<G, P>::kSmem;
+  if (int rc = attn_grid(W, kAttnCPS, &n_ctas)) return rc;
+  const size_t smem = Cfg::kSmem;
   auto kern = k_sparse_decode<G, P>;
   static int max_set[kMaxDevices] = {};
   if (int rc = ensure_smem(reinterpret_cast<const void *>(kern), smem, max_set)) return rc;
   const float scale_log2 = scale * 1.4426950408889634f;
-  kern<<<n_ctas, AttnCfg<G, P>::kThreads, smem, st>>>(tk, tv, q, sel_phys, d->n_kv_heads, k, n_phys, W,
+  kern<<<n_ctas, kAttnThreads, smem, st>>>(tk, tv, q, sel_phys, d->n_kv_heads, k, n_phys, W,
                                            scale_log2, filter, filter_mode, w.part_o, w.part_ml,
-                                           w.count, out);
-  return check_launch("k_sparse_decode");
+                                           out);
+  if (int rc = check_launch("k_sparse_decode")) return rc;
+  // merge of the split units: a programmatic dependent launch, so its launch
+  // overlaps the streaming kernel's tail
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units * G));
+  cfg.blockDim = dim3(kD);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_attn_merge<G>, static_cast<const float *>(w.part_o),
+                                           static_cast<const float2 *>(w.part_ml), d->n_kv_heads, kc,
+                                           W, n_ctas * kAttnNC, filter, filter_mode, out);
+  if (e != cudaSuccess) return cuda_fail(e, "k_attn_merge");
+  return KVR_OK;
 }
 
 template <int G>
