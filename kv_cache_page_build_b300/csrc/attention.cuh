@@ -86,13 +86,6 @@ __device__ __forceinline__ bool attn_unit_active(const uint8_t *filter, int filt
   return (filter[u] != 0) == (filter_mode == 2);
 }
 
-// Shared address of the 16-byte chunk `cc` (0..15) of row `row` in a stage
-// area of two 64-channel halves written by TMA with 128-byte swizzling.
-template <int HALF>
-__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int cc) {
-  return base + (cc >> 3) * HALF + row * 128 + (((cc & 7) ^ (row & 7)) << 4);
-}
-
 // One chunk of C tokens for head row gq of a consumer warp: QK on the tensor
 // cores, online-softmax update of (m_run, l_run) and O^T += V^T P^T.
 template <int G, int P>
@@ -386,12 +379,14 @@ __global__ void __launch_bounds__(kD)
     k_attn_merge(const float *__restrict__ part_o, const float2 *__restrict__ part_ml, int H,
                  long long kc, long long W, int n_workers, const uint8_t *__restrict__ filter,
                  int filter_mode, float *__restrict__ out) {
+  // every CTA waits, so this kernel never completes before k_sparse_decode
+  // (later work on the stream may rewrite what k_sparse_decode reads)
+  pdl_wait();
   const long long u = blockIdx.x / G;
   const int h = blockIdx.x % G, ch = threadIdx.x;
   const int c_first = attn_cta_of(u * kc, W, n_workers);
   const int n_segs = attn_cta_of((u + 1) * kc - 1, W, n_workers) - c_first + 1;
   if (n_segs == 1 || !attn_unit_active(filter, filter_mode, u)) return;  // written by the main kernel
-  pdl_wait();
   const size_t slot0 = static_cast<size_t>(c_first) + static_cast<size_t>(u);
   float M = -INFINITY, L = 0.f, A = 0.f;
 #pragma unroll 1

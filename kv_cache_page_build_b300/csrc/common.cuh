@@ -191,6 +191,24 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
       : "memory");
 }
 
+// Tiled 2D tensor copy global -> shared (coordinates innermost first).
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Shared address of the 16-byte chunk `cc` of row `row` in a tile stored as
+// 64-element (128-byte) column blocks of HALF bytes each, written by TMA with
+// 128-byte swizzling (chunk index XOR row mod 8 inside each 1024-byte atom).
+template <int HALF>
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int cc) {
+  return base + (cc >> 3) * HALF + row * 128 + (((cc & 7) ^ (row & 7)) << 4);
+}
+
 // Tiled 3D tensor copy global -> shared (coordinates innermost first).
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int c0, int c1, int c2) {

@@ -178,6 +178,30 @@ int make_pool_map(CUtensorMap *map, const void *pool, const kvr_dims *d, int64_t
   return KVR_OK;
 }
 
+// The page summaries [B][H][N][2][D] bf16 viewed as [pages][256]; one box is
+// 64 channels of `rows` pages, written to shared memory with 128-byte swizzling.
+int make_summ_map(CUtensorMap *map, const void *summ, long long F, int rows) {
+  auto fn = encode_fn();
+  if (!fn) {
+    std::snprintf(g_err_text, sizeof g_err_text, "cuTensorMapEncodeTiled unavailable");
+    return KVR_ERR_CUDA;
+  }
+  const cuuint64_t dims[2] = {2 * static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(F)};
+  const cuuint64_t strides[1] = {4 * static_cast<cuuint64_t>(kD)};
+  const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r =
+      fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(summ), dims, strides, box,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_err_text, sizeof g_err_text, "cuTensorMapEncodeTiled failed (%d)",
+                  static_cast<int>(r));
+    return KVR_ERR_CUDA;
+  }
+  return KVR_OK;
+}
+
 // ---------------------------------------------------------------- launches
 
 int sm_count(int *out);
@@ -186,24 +210,42 @@ template <int G>
 int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
                     const int32_t *ptab, int k, SelectWs w, int32_t *sel, int32_t *sel_phys,
                     float *scores, const SpecArgs &spec, cudaStream_t st) {
-  const size_t smem = kSelSmem;
-  auto kern = k_score_select<G>;
+  // 1. page scores: kScCPS CTAs per SM, each warp a worker over a contiguous
+  //    range of the flat page list
+  auto kern = k_page_scores<G>;
   static int max_set[kMaxDevices] = {};
-  if (int rc = ensure_smem(reinterpret_cast<const void *>(kern), smem, max_set)) return rc;
-  // splits per (b, g) row: about two resident CTAs per SM over all rows, at
-  // least one 32-page stage per CTA
+  if (int rc = ensure_smem(reinterpret_cast<const void *>(kern), kScSmem, max_set)) return rc;
   int sms = 0;
   if (int rc = sm_count(&sms)) return rc;
-  const long long units = static_cast<long long>(d->batch) * d->n_kv_heads;
-  const long long per_sm = G <= 4 ? 2 : 1;
-  long long n_split = sms * per_sm / units;
-  n_split = std::max<long long>(1, std::min<long long>(
-                                       n_split, (d->n_pages + kSelStagePages - 1) / kSelStagePages));
-  const dim3 grid(static_cast<unsigned>(n_split), d->n_kv_heads, d->batch);
-  kern<<<grid, kSelThreads, smem, st>>>(q, summ, ptab, d->n_kv_heads, d->n_pages, k,
-                                        static_cast<int>(n_split), w.scores, w.count, sel,
-                                        sel_phys, scores, spec);
-  return check_launch("k_score_select");
+  const long long F = static_cast<long long>(d->batch) * d->n_kv_heads * d->n_pages;
+  const long long per_cta = static_cast<long long>(kScMinPagesPerWorker) * kScNC;
+  long long n_ctas = std::min<long long>(static_cast<long long>(sms) * kScCPS, (F + per_cta - 1) / per_cta);
+  n_ctas = std::max<long long>(1, std::min<long long>(n_ctas, kScMaxCtas));
+  CUtensorMap tsm, tsm8;
+  if (int rc = make_summ_map(&tsm, summ, F, kScPages)) return rc;
+  if (int rc = make_summ_map(&tsm8, summ, F, 8)) return rc;
+  kern<<<static_cast<unsigned>(n_ctas), kScThreads, kScSmem, st>>>(tsm, tsm8, q, d->n_kv_heads,
+                                                                   d->n_pages, F, w.scores, scores);
+  if (int rc = check_launch("k_page_scores")) return rc;
+  // 2. top-k per unit: a programmatic dependent launch
+  const size_t smem = static_cast<size_t>(d->n_pages) * 4;
+  auto topk = k_topk<G>;
+  static int max_set_tk[kMaxDevices] = {};
+  if (int rc = ensure_smem(reinterpret_cast<const void *>(topk), smem, max_set_tk)) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(d->n_kv_heads, d->batch);
+  cfg.blockDim = dim3(kTkThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, topk, q, ptab, d->n_kv_heads, d->n_pages, k,
+                                           static_cast<const float *>(w.scores), sel, sel_phys, spec);
+  if (e != cudaSuccess) return cuda_fail(e, "k_topk");
+  return KVR_OK;
 }
 
 int launch_select(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,

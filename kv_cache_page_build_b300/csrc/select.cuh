@@ -12,20 +12,24 @@
 // Because kmin <= kmax, max(q kmin, q kmax) is q kmax for q >= 0 and q kmin
 // otherwise; with q+ = max(q, 0) and q- = min(q, 0) the term is
 // fma(q+, kmax, fma(q-, kmin, .)) where one of the two products is an exact
-// zero, so each channel adds exactly one exact bf16 x bf16 product to an fp32
-// accumulator.  Every page is reduced in the same fixed order (channel pairs
-// into two interleaved accumulators with packed FFMA2, the pair summed, G
-// heads pairwise, then a 16-lane butterfly), so two pages with equal
-// summaries get bitwise-equal scores.
+// zero, so each channel adds exactly one exact bf16 x bf16 product.  Per unit
+// this is a contraction [q- | q+] (G x 256) . [kmin ; kmax] (256 x pages):
+// it runs on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 out) with the
+// G heads on the 16-row side, then the G head scores of a page are summed by
+// a fixed xor butterfly.  Two pages with equal summaries go through identical
+// operations, so they get bitwise-equal scores.
 //
-// Layout of work.  Grid (splits, H, B): the N pages of a (b, g) row are cut
-// into `splits` contiguous ranges, about two CTAs per SM in total.  A CTA's
-// summaries are one contiguous byte range; its producer warp streams them
-// with 1D bulk copies (32 pages = 16 KiB per copy) into a ring of stages,
-// and the 8 consumer warps score every stage together (a half-warp per page,
-// lane = 8 channels of the min and max rows).  Scores go to an fp32
-// workspace row; the CTA that finishes the (b, g) row last (atomic ticket,
-// no waiting) selects the top k.
+// Two kernels.
+//   k_page_scores streams the summaries.  The rows of all (b, g) units form
+//   one flat list of 512-byte page summaries, viewed by TMA as [pages][256];
+//   every consumer warp of the grid is an independent worker over a
+//   contiguous range of it.  Its producer lane loads the range 32 pages
+//   (16 KiB: four 64-channel boxes, 128-byte swizzled) at a time, never
+//   across a unit boundary (a shorter stage takes 8-page boxes), into the
+//   worker's R private stages; the worker scores a stage with 64 MMAs fed by
+//   ldmatrix.
+//   k_topk, one CTA per unit, launched right after as a programmatic
+//   dependent launch, reads the unit's N scores and selects.
 //
 // Top-k.  Scores map to order-preserving 32-bit keys (-0 folded into +0).
 // The k-th largest key lies in a key interval [L, R], first [min, max].  A
@@ -41,16 +45,20 @@
 
 namespace kvr {
 
-constexpr int kSelConsumers = 8;                        // consumer warps
-constexpr int kSelCT = 32 * kSelConsumers;              // consumer threads
-constexpr int kSelThreads = kSelCT + 32;                // + one producer warp
-constexpr int kSelStagePages = 32;                      // pages per bulk copy
-constexpr int kSummBytes = 2 * kD * 2;                  // bytes of one page summary
-constexpr int kSelStageBytes = kSelStagePages * kSummBytes;  // 16 KiB
-constexpr int kSelStages = 6;
-constexpr int kSelSmem = kSelStages * kSelStageBytes;   // 96 KiB: also holds N <= 16384 keys
+constexpr int kSummBytes = 2 * kD * 2;                     // bytes of one page summary
+constexpr int kScNC = 3;                                   // workers (consumer warps) per CTA
+constexpr int kScThreads = 32 * (kScNC + 1);               // + one producer warp
+constexpr int kScPages = 32;                               // pages per stage
+constexpr int kScStageBytes = kScPages * kSummBytes;       // 16 KiB
+constexpr int kScR = 2;                                    // stages per worker
+constexpr int kScS = kScNC * kScR;
+constexpr int kScCPS = 2;                                  // CTAs per SM
+constexpr int kScSmem = kScS * kScStageBytes + 1024;       // 96 KiB + alignment of the ring
+constexpr int kScMaxCtas = 512;
+constexpr int kScMinPagesPerWorker = 32;
+constexpr int kTkThreads = 256;
 constexpr int kSelBins = 2048;
-static_assert(kSelSmem >= kMaxPages * 4, "the top-k keys reuse the stage ring");
+static_assert(kTkThreads == 256 && kSelBins % kTkThreads == 0, "top-k bin ownership");
 
 struct SpecArgs {
   int enabled;                 // 0: plain selection
@@ -71,193 +79,231 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive prefix sum over the kSelCT consumer threads (named barrier 1);
-// `scratch` holds kSelConsumers words.  Also returns the total.
-__device__ __forceinline__ uint32_t sel_exclusive_scan(uint32_t v, uint32_t *scratch,
-                                                       uint32_t &total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) scratch[warp] = incl;
-  named_bar_sync(1, kSelCT);
-  uint32_t base = 0u, tot = 0u;
-#pragma unroll
-  for (int w = 0; w < kSelConsumers; ++w) {
-    const uint32_t x = scratch[w];
-    base += w < warp ? x : 0u;
-    tot += x;
-  }
-  total = tot;
-  named_bar_sync(1, kSelCT);  // scratch free again
-  return base + incl - v;
+// Next stage of a worker: from flat page f (page pos of its unit), at most 32
+// pages, never past the unit's end or the range end e.
+__device__ __forceinline__ int sc_chunk(long long f, int pos, int N, long long e) {
+  return static_cast<int>(min(static_cast<long long>(min(kScPages, N - pos)), e - f));
 }
 
 template <int G>
-__global__ void __launch_bounds__(kSelThreads, (G <= 4 ? 2 : 1))
-    k_score_select(const uint16_t *__restrict__ q, const uint16_t *__restrict__ summ,
-                   const int32_t *__restrict__ page_table, int H, int N, int k, int n_split,
-                   float *__restrict__ ws_scores, uint32_t *__restrict__ ws_count,
-                   int32_t *__restrict__ sel_out, int32_t *__restrict__ sel_phys_out,
-                   float *__restrict__ scores_out, SpecArgs spec) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full[kSelStages], empty[kSelStages];
-  __shared__ uint32_t s_hist[kSelBins];
-  __shared__ uint32_t s_scan[kSelConsumers];
-  __shared__ uint32_t s_mm[2 * kSelConsumers];
-  __shared__ uint32_t s_bin, s_bin_above, s_bin_cnt, s_last, s_corr;
-  __shared__ float s_cos[8];
+__global__ void __launch_bounds__(kScThreads, kScCPS)
+    k_page_scores(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_s8,
+                  const uint16_t *__restrict__ q, int H, int N, long long F,
+                  float *__restrict__ ws_scores, float *__restrict__ scores_out) {
+  constexpr int HALF = kScPages * 128;  // one 64-channel box of a stage
+  extern __shared__ uint8_t smem_raw[];
+  // the swizzle pattern repeats every 1024 bytes: align the ring to it
+  uint8_t *smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+  const uint32_t ring = smem_addr(smem);
+  __shared__ __align__(8) uint64_t full[kScS], empty[kScS];
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int n_workers = gridDim.x * kScNC;
   const int Hq = H * G;
-  const size_t unit = static_cast<size_t>(b) * H + g;
-  const int p0 = static_cast<int>(static_cast<long long>(split) * N / n_split);
-  const int p1 = static_cast<int>(static_cast<long long>(split + 1) * N / n_split);
-  const int np = p1 - p0;
-  const int n_stages = (np + kSelStagePages - 1) / kSelStagePages;
 
   if (tid == 0) {
+    prefetch_tensormap(&tmap_s);
+    prefetch_tensormap(&tmap_s8);
 #pragma unroll
-    for (int s = 0; s < kSelStages; ++s) {
+    for (int s = 0; s < kScS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kSelConsumers);
+      mbar_init(&empty[s], 1);
     }
     s_abort = 0;
     fence_barrier_init();
   }
   __syncthreads();
+  if (tid == 0) pdl_launch_dependents();  // the top-k kernel may be scheduled now
 
   // ------------------------------------------------------------ producer warp
-  if (warp == kSelConsumers) {
-    if (lane == 0) {
-      const uint8_t *src = reinterpret_cast<const uint8_t *>(summ) + (unit * N + p0) * kSummBytes;
-      int issued = 0;
-      bool abort = false;
+  if (warp == kScNC) {
+    const bool feeder = lane < kScNC;
+    const long long v = static_cast<long long>(blockIdx.x) * kScNC + lane;
+    const long long e = feeder ? (v + 1) * F / n_workers : 0;
+    long long f = feeder ? v * F / n_workers : 0;
+    int pos = static_cast<int>(f % N), use = 0;
+    bool abort = false;
+    uint64_t t_prog = global_timer_ns();
 #pragma unroll 1
-      for (int j = 0; j < n_stages; ++j) {
-        const int s = j % kSelStages, use = j / kSelStages;
-        if (use > 0 && !mbar_wait(&empty[s], static_cast<uint32_t>((use - 1) & 1))) abort = true;
-        if (s_abort) abort = true;
-        if (abort) {
+    while (true) {
+      const bool mine = f < e && !abort;
+      if (!__any_sync(0xffffffffu, mine)) break;
+      if (mine) {
+        const int s = lane * kScR + use % kScR;
+        if (use < kScR || mbar_test_wait(&empty[s], static_cast<uint32_t>((use / kScR - 1) & 1))) {
+          const int cnt = sc_chunk(f, pos, N, e);
+          uint8_t *dst = smem + s * kScStageBytes;
+          if (cnt == kScPages) {  // four 32-page boxes
+            mbar_arrive_expect_tx(&full[s], kScStageBytes);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tma_load_2d(dst + j * HALF, &tmap_s, &full[s], 64 * j, static_cast<int>(f));
+          } else {  // 8-page boxes up to cnt (rows past the range are never scored out)
+            const int n8 = (cnt + 7) >> 3;
+            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(n8) * 8 * kSummBytes);
+            for (int r = 0; r < n8; ++r)
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                tma_load_2d(dst + j * HALF + r * 1024, &tmap_s8, &full[s], 64 * j,
+                            static_cast<int>(f) + 8 * r);
+          }
+          f += cnt;
+          pos += cnt;
+          if (pos == N) pos = 0;
+          ++use;
+          t_prog = global_timer_ns();
+        } else if (global_timer_ns() - t_prog > kWaitNs) {
+          set_status(KVR_ST_WAIT_TIMEOUT);
           s_abort = 1;
-          break;
         }
-        const uint32_t bytes =
-            static_cast<uint32_t>(min(kSelStagePages, np - j * kSelStagePages)) * kSummBytes;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_copy_g2s(smem + s * kSelStageBytes,
-                      src + static_cast<size_t>(j) * kSelStageBytes, bytes, &full[s]);
-        issued = j + 1;
-      }
-      if (abort) {  // never leave with copies in flight
-#pragma unroll 1
-        for (int j = max(0, issued - kSelStages); j < issued; ++j)
-          mbar_wait(&full[j % kSelStages], static_cast<uint32_t>((j / kSelStages) & 1));
+        if (s_abort) abort = true;
       }
     }
+    if (feeder && abort)  // never leave with copies in flight
+      for (int j = max(0, use - kScR); j < use; ++j)
+        mbar_wait(&full[lane * kScR + j % kScR], static_cast<uint32_t>((j / kScR) & 1));
     return;
   }
 
-  // ------------------------------------------------------------ consumer warps: scores
-  const int ct = tid;
-  {
-    // this lane's query channels: 8 channels (8*sub .. 8*sub+7) of each head, as
-    // sign-split pairs
-    const int hw = ct >> 4, sub = ct & 15;
-    float2 qp[G][4], qn[G][4];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
-          q + (static_cast<size_t>(b) * Hq + g * G + h) * kD + 8 * sub));
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 x = bf2_to_f2(w[j]);
-        qp[h][j] = make_float2(fmaxf(x.x, 0.0f), fmaxf(x.y, 0.0f));
-        qn[h][j] = make_float2(fminf(x.x, 0.0f), fminf(x.y, 0.0f));
-      }
-    }
-    float *srow = ws_scores + unit * N + p0;
-    float *orow = scores_out ? scores_out + unit * N + p0 : nullptr;
+  // ------------------------------------------------------------ workers
+  const long long v = static_cast<long long>(blockIdx.x) * kScNC + warp;
+  const long long e = (v + 1) * F / n_workers;
+  long long f = v * F / n_workers;
+  long long u = f / N;
+  int pos = static_cast<int>(f % N);
+  const int gq = lane >> 2, tq = lane & 3, mi = lane >> 3, mr = lane & 7;
+  // [q- | q+] of head gq as A fragments: k-step kk < 8 meets kmin channels
+  // 16kk.., kk >= 8 meets kmax channels 16(kk - 8)..; words hold bf16 pairs
+  uint32_t qa[16][2];
+  long long q_unit = -1;
 #pragma unroll 1
-    for (int j = 0; j < n_stages; ++j) {
-      const int s = j % kSelStages;
-      bool have = false;
-      if (__shfl_sync(0xffffffffu, s_abort, 0) == 0) {  // warp-uniform
-        const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((j / kSelStages) & 1));
-        if (__all_sync(0xffffffffu, ok)) {
-          have = true;
-        } else if (lane == 0) {
-          s_abort = 1;
+  for (int use = 0; f < e; ++use) {
+    const int cnt = sc_chunk(f, pos, N, e);
+    if (q_unit != u) {
+      const int b = static_cast<int>(u / H), g = static_cast<int>(u % H);
+      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+          q + (static_cast<size_t>(b) * Hq + g * G + min(gq, G - 1)) * kD);
+      const bool on = gq < G;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          const uint32_t w = on ? __ldg(qrow + 8 * kk + 4 * hlf + tq) : 0u;
+          // per bf16 half: all ones where the sign bit is set
+          const uint32_t neg = ((w >> 15) & 0x00010001u) * 0xffffu;
+          qa[kk][hlf] = w & neg;        // q- with kmin
+          qa[8 + kk][hlf] = w & ~neg;   // q+ with kmax
         }
       }
-      if (have) {
-        const uint8_t *stage = smem + s * kSelStageBytes;
+      q_unit = u;
+    }
+    const int s = warp * kScR + use % kScR;
+    bool have = false;
+    if (__shfl_sync(0xffffffffu, s_abort, 0) == 0) {  // warp-uniform
+      const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((use / kScR) & 1));
+      if (__all_sync(0xffffffffu, ok)) {
+        have = true;
+      } else if (lane == 0) {
+        s_abort = 1;
+      }
+    }
+    if (have) {
+      const uint32_t sb = ring + s * kScStageBytes;
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int pl = j * kSelStagePages + hw + 16 * r;  // page within this CTA's range
-          const uint8_t *pg = stage + (hw + 16 * r) * kSummBytes;  // rows past np never written out
-          const uint4 mn = *reinterpret_cast<const uint4 *>(pg + 16 * sub);
-          const uint4 mx = *reinterpret_cast<const uint4 *>(pg + kD * 2 + 16 * sub);
-          const uint32_t wn[4] = {mn.x, mn.y, mn.z, mn.w};
-          const uint32_t wx[4] = {mx.x, mx.y, mx.z, mx.w};
-          float2 acc2[G];
+      for (int nb = 0; nb < kScPages / 8; ++nb) {
+        if (8 * nb >= cnt) break;  // rows not loaded for a short stage
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int h = 0; h < G; ++h) acc2[h] = make_float2(0.f, 0.f);
+        for (int kq = 0; kq < 8; ++kq) {  // 16-byte chunks 4kq .. 4kq+3 = k-steps 2kq, 2kq+1
+          uint32_t bf[4];
+          ldsm_x4(swz<HALF>(sb, 8 * nb + mr, 4 * kq + mi), bf);
+          mma_bf16_16816(c, qa[2 * kq][0], 0u, qa[2 * kq][1], 0u, bf[0], bf[1]);
+          mma_bf16_16816(c, qa[2 * kq + 1][0], 0u, qa[2 * kq + 1][1], 0u, bf[2], bf[3]);
+        }
+        // sum the 8 row groups (heads G.. are zero rows): pages 8nb + 2tq (+1)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float2 kmin = bf2_to_f2(wn[c]), kmax = bf2_to_f2(wx[c]);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              acc2[h] = __ffma2_rn(qp[h][c], kmax, acc2[h]);
-              acc2[h] = __ffma2_rn(qn[h][c], kmin, acc2[h]);
-            }
-          }
-          float acc[G];
-#pragma unroll
-          for (int h = 0; h < G; ++h) acc[h] = acc2[h].x + acc2[h].y;
-#pragma unroll
-          for (int w = 1; w < G; w <<= 1)
-#pragma unroll
-            for (int h = 0; h < G; h += 2 * w) acc[h] += acc[h + w];
-          float tot = acc[0];
-#pragma unroll
-          for (int m = 8; m >= 1; m >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, m);
-          if (sub == 0 && pl < np) {
-            const float sc = tot * (1.0f / G);
-            srow[pl] = sc;
-            if (orow) orow[pl] = sc;
-          }
+        for (int e2 = 0; e2 < 2; ++e2) {
+          float t = c[e2];
+          t += __shfl_xor_sync(0xffffffffu, t, 4);
+          t += __shfl_xor_sync(0xffffffffu, t, 8);
+          t += __shfl_xor_sync(0xffffffffu, t, 16);
+          c[e2] = t * (1.0f / G);
+        }
+        const int p = 8 * nb + 2 * tq;
+        if (gq == 0 && p < cnt) {
+          ws_scores[f + p] = c[0];
+          if (scores_out) scores_out[f + p] = c[0];
+        }
+        if (gq == 0 && p + 1 < cnt) {
+          ws_scores[f + p + 1] = c[1];
+          if (scores_out) scores_out[f + p + 1] = c[1];
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    f += cnt;
+    pos += cnt;
+    if (pos == N) {
+      pos = 0;
+      ++u;
     }
   }
+}
 
-  // ---- last CTA of this (b, g) row selects
-  __threadfence();
-  named_bar_sync(1, kSelCT);
-  if (ct == 0) s_last = (atomicAdd(&ws_count[unit], 1u) == static_cast<uint32_t>(n_split - 1));
-  named_bar_sync(1, kSelCT);
-  if (!s_last) return;
-  __threadfence();
+// Selection of one (b, g) unit from its N scores (kTkThreads threads; the
+// keys live in dynamic shared memory, N * 4 bytes).
+template <int G>
+__global__ void __launch_bounds__(kTkThreads)
+    k_topk(const uint16_t *__restrict__ q, const int32_t *__restrict__ page_table, int H, int N,
+           int k, const float *__restrict__ ws_scores, int32_t *__restrict__ sel_out,
+           int32_t *__restrict__ sel_phys_out, SpecArgs spec) {
+  extern __shared__ __align__(16) uint32_t keys[];
+  __shared__ uint32_t s_hist[kSelBins];
+  __shared__ uint32_t s_scan[kTkThreads / 32];
+  __shared__ uint32_t s_mm[2 * (kTkThreads / 32)];
+  __shared__ uint32_t s_bin, s_bin_above, s_bin_cnt, s_corr;
+  __shared__ float s_cos[8];
 
-  // keys of the whole row (the stage ring is idle now) and their range
-  uint32_t *keys = reinterpret_cast<uint32_t *>(smem);
-  uint32_t kmn = 0xffffffffu, kmx = 0u;
-  for (int i = ct; i < N; i += kSelCT) {
-    const uint32_t key = score_key(__ldcg(ws_scores + unit * N + i));
-    keys[i] = key;
-    kmn = min(kmn, key);
-    kmx = max(kmx, key);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = blockIdx.x, b = blockIdx.y;
+  const int Hq = H * G;
+  const size_t unit = static_cast<size_t>(b) * H + g;
+
+  // the speculative mode's query slices: loaded now, used after the top-k
+  uint2 qa = make_uint2(0u, 0u), qb = make_uint2(0u, 0u);
+  const bool cos_lane = spec.enabled && spec.step > 0 && warp < G;
+  if (cos_lane) {
+    const size_t base = (static_cast<size_t>(b) * Hq + g * G + warp) * kD + 4 * lane;
+    qa = *reinterpret_cast<const uint2 *>(q + base);
+    qb = *reinterpret_cast<const uint2 *>(spec.q_prev + base);
   }
-  if (ct == 0) ws_count[unit] = 0u;  // leave the workspace zeroed
+
+  pdl_wait();  // the scores of k_page_scores are complete and visible
+
+  // keys of the row and their range; all loads of a thread in flight at once
+  const float *row = ws_scores + unit * N;
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
+#pragma unroll 1
+  for (int i0 = 0; i0 < N; i0 += 8 * kTkThreads) {
+    float sv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j * kTkThreads + tid;
+      sv[j] = i < N ? __ldg(row + i) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j * kTkThreads + tid;
+      if (i < N) {
+        const uint32_t key = score_key(sv[j]);
+        keys[i] = key;
+        kmn = min(kmn, key);
+        kmx = max(kmx, key);
+      }
+    }
+  }
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) {
     kmn = min(kmn, __shfl_xor_sync(0xffffffffu, kmn, m));
@@ -265,14 +311,14 @@ __global__ void __launch_bounds__(kSelThreads, (G <= 4 ? 2 : 1))
   }
   if (lane == 0) {
     s_mm[warp] = kmn;
-    s_mm[kSelConsumers + warp] = kmx;
+    s_mm[kTkThreads / 32 + warp] = kmx;
   }
-  named_bar_sync(1, kSelCT);
+  __syncthreads();
   uint32_t L = 0xffffffffu, R = 0u;
 #pragma unroll
-  for (int w = 0; w < kSelConsumers; ++w) {
+  for (int w = 0; w < kTkThreads / 32; ++w) {
     L = min(L, s_mm[w]);
-    R = max(R, s_mm[kSelConsumers + w]);
+    R = max(R, s_mm[kTkThreads / 32 + w]);
   }
   // invariant: `need` of the `cnt` keys in [L, R] are still to be taken;
   // every key above R is taken
@@ -281,52 +327,49 @@ __global__ void __launch_bounds__(kSelThreads, (G <= 4 ? 2 : 1))
   while (cnt != need && L != R) {
     const uint32_t span = R - L;
     const int shift = span < kSelBins ? 0 : (32 - __clz(span)) - 11;
-    for (int i = ct; i < kSelBins; i += kSelCT) s_hist[i] = 0u;
-    named_bar_sync(1, kSelCT);
-    for (int i = ct; i < N; i += kSelCT) {
+    for (int i = tid; i < kSelBins; i += kTkThreads) s_hist[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < N; i += kTkThreads) {
       const uint32_t key = keys[i];
       if (key >= L && key <= R) atomicAdd(&s_hist[(key - L) >> shift], 1u);
     }
-    named_bar_sync(1, kSelCT);
-    // thread ct owns bins [8 ct, 8 ct + 8); find the bin holding the need-th largest
-    uint32_t c[kSelBins / kSelCT], mine = 0u;
+    __syncthreads();
+    // thread tid owns bins [8 tid, 8 tid + 8); find the bin holding the need-th largest
+    uint32_t c[kSelBins / kTkThreads], mine = 0u;
 #pragma unroll
-    for (int e = 0; e < kSelBins / kSelCT; ++e) {
-      c[e] = s_hist[(kSelBins / kSelCT) * ct + e];
+    for (int e = 0; e < kSelBins / kTkThreads; ++e) {
+      c[e] = s_hist[(kSelBins / kTkThreads) * tid + e];
       mine += c[e];
     }
     uint32_t total;
-    const uint32_t below = sel_exclusive_scan(mine, s_scan, total);
+    const uint32_t below = block_exclusive_scan<kTkThreads>(mine, s_scan, total);
     uint32_t above_here = total - below - mine;  // keys of the interval in higher bins
 #pragma unroll
-    for (int e = kSelBins / kSelCT - 1; e >= 0; --e) {
+    for (int e = kSelBins / kTkThreads - 1; e >= 0; --e) {
       if (above_here < need && need <= above_here + c[e]) {
-        s_bin = static_cast<uint32_t>((kSelBins / kSelCT) * ct + e);
+        s_bin = static_cast<uint32_t>((kSelBins / kTkThreads) * tid + e);
         s_bin_above = above_here;
         s_bin_cnt = c[e];
       }
       above_here += c[e];
     }
-    named_bar_sync(1, kSelCT);
+    __syncthreads();
     const uint32_t nl = L + (s_bin << shift);
     const unsigned long long nr = static_cast<unsigned long long>(nl) + ((1ull << shift) - 1ull);
     need -= s_bin_above;
     cnt = s_bin_cnt;
     R = static_cast<uint32_t>(min(static_cast<unsigned long long>(R), nr));
     L = nl;
-    named_bar_sync(1, kSelCT);  // s_bin* and s_hist free for the next round
+    __syncthreads();  // s_bin* and s_hist free for the next round
   }
 
   // ---- speculative mode: group similarity and the correction decision
   const int32_t *ptab = page_table ? page_table + static_cast<size_t>(b) * N : nullptr;
   bool corrected = true;
   if (spec.enabled) {
-    if (spec.step > 0 && warp < G) {
-      const size_t base = (static_cast<size_t>(b) * Hq + g * G + warp) * kD + 4 * lane;
-      const uint2 a = *reinterpret_cast<const uint2 *>(q + base);
-      const uint2 c = *reinterpret_cast<const uint2 *>(spec.q_prev + base);
-      const float x[4] = {bf_lo(a.x), bf_hi(a.x), bf_lo(a.y), bf_hi(a.y)};
-      const float y[4] = {bf_lo(c.x), bf_hi(c.x), bf_lo(c.y), bf_hi(c.y)};
+    if (cos_lane) {
+      const float x[4] = {bf_lo(qa.x), bf_hi(qa.x), bf_lo(qa.y), bf_hi(qa.y)};
+      const float y[4] = {bf_lo(qb.x), bf_hi(qb.x), bf_lo(qb.y), bf_hi(qb.y)};
       float dot = 0.f, nx = 0.f, ny = 0.f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -342,8 +385,8 @@ __global__ void __launch_bounds__(kSelThreads, (G <= 4 ? 2 : 1))
       }
       if (lane == 0) s_cos[warp] = (nx > 0.f && ny > 0.f) ? dot / (sqrtf(nx) * sqrtf(ny)) : 0.f;
     }
-    named_bar_sync(1, kSelCT);
-    if (ct == 0) {
+    __syncthreads();
+    if (tid == 0) {
       float cb = __int_as_float(0x7fc00000);  // NaN: no previous query at step 0
       bool corr = true;
       if (spec.step > 0) {
@@ -356,15 +399,15 @@ __global__ void __launch_bounds__(kSelThreads, (G <= 4 ? 2 : 1))
       spec.corrected[unit] = corr ? 1 : 0;
       if (spec.cbar) spec.cbar[unit] = cb;
     }
-    named_bar_sync(1, kSelCT);
+    __syncthreads();
     corrected = s_corr != 0u;
     // q_prev <- q_t for this group's heads (only this CTA reads them)
-    for (int i = ct; i < G * kD / 8; i += kSelCT) {
+    for (int i = tid; i < G * kD / 8; i += kTkThreads) {
       const size_t off = (static_cast<size_t>(b) * Hq + g * G) * kD + 8 * i;
       *reinterpret_cast<uint4 *>(spec.q_prev + off) = *reinterpret_cast<const uint4 *>(q + off);
     }
     if (!corrected) {  // reuse: sel_used <- previous selection (before it is replaced)
-      for (int i = ct; i < k; i += kSelCT) {
+      for (int i = tid; i < k; i += kTkThreads) {
         const int p = spec.sel_prev[unit * k + i];
         spec.sel_used[unit * k + i] = p;
         if (spec.sel_used_phys) {
@@ -379,14 +422,14 @@ __global__ void __launch_bounds__(kSelThreads, (G <= 4 ? 2 : 1))
         }
       }
     }
-    named_bar_sync(1, kSelCT);
+    __syncthreads();
   }
 
   // ---- ordered compaction of the selection (ascending page ids): every key
   // above R, then the first `need` keys of [L, R] by page id (all of them
   // when cnt == need)
-  const int per = (N + kSelCT - 1) / kSelCT;
-  const int beg = min(N, ct * per), end = min(N, beg + per);
+  const int per = (N + kTkThreads - 1) / kTkThreads;
+  const int beg = min(N, tid * per), end = min(N, beg + per);
   uint32_t n_gt = 0u, n_eq = 0u;
   for (int i = beg; i < end; ++i) {
     const uint32_t key = keys[i];
@@ -394,10 +437,10 @@ __global__ void __launch_bounds__(kSelThreads, (G <= 4 ? 2 : 1))
     n_eq += (key >= L && key <= R);
   }
   uint32_t total;
-  const uint32_t eq_base = sel_exclusive_scan(n_eq, s_scan, total);
+  const uint32_t eq_base = block_exclusive_scan<kTkThreads>(n_eq, s_scan, total);
   uint32_t n_take = n_gt;
   for (uint32_t e = 0; e < n_eq; ++e) n_take += (eq_base + e < need);
-  uint32_t out = sel_exclusive_scan(n_take, s_scan, total);
+  uint32_t out = block_exclusive_scan<kTkThreads>(n_take, s_scan, total);
   uint32_t eq_seen = 0u;
   for (int i = beg; i < end; ++i) {
     const uint32_t key = keys[i];
