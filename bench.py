@@ -255,12 +255,20 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     assert kvr.kvr_get_status() == 0
 
-    # capture L steps (starting at a trace position multiple of 64) into a graph
+    # capture L steps (starting at a trace position multiple of the trace
+    # length) into a graph; the timed graph holds nothing but the steps
     L = min(TRACE_LEN, args.steps)
-    ev_mid = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(L)]
-    ev_end = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(L)]
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
+        for i in range(L):
+            step(i)
+    # a second graph with events around each call, for the per-kernel split
+    # (event nodes between the calls break the kernels' programmatic
+    # dependent launches, so its per-call times are an upper bound)
+    ev_mid = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(L)]
+    ev_end = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(L)]
+    graph_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_ev):
         for i in range(L):
             step(i, ev_mid[i], ev_end[i])
     rem = args.steps % L
@@ -295,7 +303,10 @@ def run_gpu(args, world, rank, local):
     status = kvr.kvr_get_status()
     value, t_max = aggregate(args.steps, elapsed, world)
 
-    # per-launch device time of the two kernels, from the last replay
+    # per-launch device time of the two calls, from a replay of the graph with events
+    for _ in range(2):
+        graph_ev.replay()
+    torch.cuda.synchronize()
     attn_ms = [ev_mid[i].elapsed_time(ev_end[i]) for i in range(L)]
     sel_ms = [ev_end[i - 1].elapsed_time(ev_mid[i]) for i in range(1, L)]
     attn_avg = sum(attn_ms) / len(attn_ms) / 1e3
@@ -349,23 +360,25 @@ def run_gpu(args, world, rank, local):
             "parallelism": f"{world} independent replica(s)" if world > 1 else "1 GPU",
             "l2": f"{COPIES} rotating cache copies: {(COPIES - 1) * (attn_bytes + summ_bytes) / 2**20:.0f} MiB "
                   f"touched between reuses of one copy (L2 126 MB)",
-            "graph": f"steps replayed from a CUDA graph of {L} steps",
+            "graph": f"steps replayed from a CUDA graph of {L} steps (per-kernel times from a second graph "
+                     f"with events between the calls)",
         },
         "selected_kv_gbs": round(achieved, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "k_sparse_decode", "bytes_per_launch": attn_bytes,
+                     "kernel": "k_sparse_decode (+ k_attn_merge)", "bytes_per_launch": attn_bytes,
                      "launch_us": round(attn_avg * 1e6, 3)},
         "kernels": {
-            "k_sparse_decode": {"us": round(attn_avg * 1e6, 3), "bytes": attn_bytes,
-                                "gbs": round(achieved, 1)},
-            "k_score_select": {"us": round(sel_avg * 1e6, 3) if sel_avg else None, "bytes": summ_bytes,
-                               "gbs": round(summ_bytes / sel_avg / 1e9, 1) if sel_avg else None},
+            "attention (k_sparse_decode + k_attn_merge)": {"us": round(attn_avg * 1e6, 3), "bytes": attn_bytes,
+                                                           "gbs": round(achieved, 1)},
+            "selection (k_page_scores + k_topk)": {"us": round(sel_avg * 1e6, 3) if sel_avg else None,
+                                                   "bytes": summ_bytes,
+                                                   "gbs": round(summ_bytes / sel_avg / 1e9, 1) if sel_avg else None},
             "k_build_summaries": {"us": round(summ_ms * 1e3, 3), "bytes": k_bytes + summ_bytes,
                                   "gbs": round((k_bytes + summ_bytes) / (summ_ms / 1e3) / 1e9, 1),
                                   "note": "once per cache (prefill), not in the step"},
         },
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 4 * args.steps,  # k_page_scores, k_topk, k_sparse_decode, k_attn_merge
         "e2e": {"value": round(e2e_value, 2), "unit": "steps/s",
                 "h2d_bytes_per_step": B * Hq * D * 2, "d2h_bytes_per_step": B * Hq * D * 4,
                 "how": f"{n_e2e} eager kvr_speculative_step calls, q copied in from pinned host memory and "

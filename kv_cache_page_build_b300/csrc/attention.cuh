@@ -204,7 +204,11 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
     fence_barrier_init();
   }
   __syncthreads();
-  if (tid == 0) pdl_launch_dependents();  // the merge kernel may be scheduled now
+  // Launched as a programmatic dependent launch, this kernel's setup above
+  // overlaps the previous kernel; every global read and write comes after
+  // this wait.  Then the merge kernel may be scheduled.
+  pdl_wait();
+  if (tid == 0) pdl_launch_dependents();
 
   // ------------------------------------------------------------ producer warp
   if (warp == NC) {

@@ -224,26 +224,48 @@ int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
   CUtensorMap tsm, tsm8;
   if (int rc = make_summ_map(&tsm, summ, F, kScPages)) return rc;
   if (int rc = make_summ_map(&tsm8, summ, F, 8)) return rc;
-  kern<<<static_cast<unsigned>(n_ctas), kScThreads, kScSmem, st>>>(tsm, tsm8, q, d->n_kv_heads,
-                                                                   d->n_pages, F, w.scores, scores);
-  if (int rc = check_launch("k_page_scores")) return rc;
-  // 2. top-k per unit: a programmatic dependent launch
-  const size_t smem = static_cast<size_t>(d->n_pages) * 4;
-  auto topk = k_topk<G>;
-  static int max_set_tk[kMaxDevices] = {};
-  if (int rc = ensure_smem(reinterpret_cast<const void *>(topk), smem, max_set_tk)) return rc;
+  {  // a programmatic dependent launch: the setup overlaps the kernel before it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(n_ctas));
+    cfg.blockDim = dim3(kScThreads);
+    cfg.dynamicSmemBytes = kScSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tsm, tsm8, q, d->n_kv_heads, d->n_pages, F,
+                                             w.scores, scores);
+    if (e != cudaSuccess) return cuda_fail(e, "k_page_scores");
+  }
+  // 2. top-k per unit: a programmatic dependent launch; 4 keys per thread up
+  //    to 1024 pages, 16 beyond; 256 threads up to 4096 pages, 1024 beyond
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d->n_kv_heads, d->batch);
-  cfg.blockDim = dim3(kTkThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, topk, q, ptab, d->n_kv_heads, d->n_pages, k,
-                                           static_cast<const float *>(w.scores), sel, sel_phys, spec);
+  const float *ws_sc = static_cast<const float *>(w.scores);
+  cudaError_t e;
+  if (d->n_pages <= 256 * 4) {
+    cfg.blockDim = dim3(256);
+    e = cudaLaunchKernelEx(&cfg, k_topk<G, 256, 4>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
+                           sel, sel_phys, spec);
+  } else if (d->n_pages <= 256 * 16) {
+    cfg.blockDim = dim3(256);
+    e = cudaLaunchKernelEx(&cfg, k_topk<G, 256, 16>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
+                           sel, sel_phys, spec);
+  } else {
+    cfg.blockDim = dim3(1024);
+    static_assert(1024 * 16 >= kMaxPages, "the largest top-k launch covers every page count");
+    e = cudaLaunchKernelEx(&cfg, k_topk<G, 1024, 16>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
+                           sel, sel_phys, spec);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "k_topk");
   return KVR_OK;
 }
@@ -292,7 +314,8 @@ int attn_grid(long long W, int per_sm, int *n_ctas) {
 template <int G, int P>
 int launch_attn_gp(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &tv,
                    const uint16_t *q, const int32_t *sel_phys, int k, int n_phys, float scale,
-                   const uint8_t *filter, int filter_mode, AttnWs w, float *out, cudaStream_t st) {
+                   const uint8_t *filter, int filter_mode, AttnWs w, float *out, cudaStream_t st,
+                   bool pdl_ok) {
   using Cfg = AttnCfg<G, P>;
   const long long units = static_cast<long long>(d->batch) * d->n_kv_heads;
   const long long kc = static_cast<long long>(k) * Cfg::CPP;
@@ -304,10 +327,24 @@ int launch_attn_gp(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &
   static int max_set[kMaxDevices] = {};
   if (int rc = ensure_smem(reinterpret_cast<const void *>(kern), smem, max_set)) return rc;
   const float scale_log2 = scale * 1.4426950408889634f;
-  kern<<<n_ctas, kAttnThreads, smem, st>>>(tk, tv, q, sel_phys, d->n_kv_heads, k, n_phys, W,
-                                           scale_log2, filter, filter_mode, w.part_o, w.part_ml,
-                                           out);
-  if (int rc = check_launch("k_sparse_decode")) return rc;
+  // a programmatic dependent launch (unless the stream's last operation is
+  // an event wait): the setup overlaps the kernel before it on the stream
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(n_ctas));
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = pdl_ok ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tk, tv, q, sel_phys, d->n_kv_heads, k,
+                                             n_phys, W, scale_log2, filter, filter_mode, w.part_o,
+                                             w.part_ml, out);
+    if (e != cudaSuccess) return cuda_fail(e, "k_sparse_decode");
+  }
   // merge of the split units: a programmatic dependent launch, so its launch
   // overlaps the streaming kernel's tail
   cudaLaunchConfig_t cfg = {};
@@ -330,24 +367,27 @@ int launch_attn_gp(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &
 template <int G>
 int launch_attn_g(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &tv,
                   const uint16_t *q, const int32_t *sel_phys, int k, int n_phys, float scale,
-                  const uint8_t *filter, int filter_mode, AttnWs w, float *out, cudaStream_t st) {
+                  const uint8_t *filter, int filter_mode, AttnWs w, float *out, cudaStream_t st,
+                  bool pdl_ok) {
   switch (d->page_size) {
     case 16:
       return launch_attn_gp<G, 16>(d, tk, tv, q, sel_phys, k, n_phys, scale, filter, filter_mode,
-                                   w, out, st);
+                                   w, out, st, pdl_ok);
     case 32:
       return launch_attn_gp<G, 32>(d, tk, tv, q, sel_phys, k, n_phys, scale, filter, filter_mode,
-                                   w, out, st);
+                                   w, out, st, pdl_ok);
     default:
       return launch_attn_gp<G, 64>(d, tk, tv, q, sel_phys, k, n_phys, scale, filter, filter_mode,
-                                   w, out, st);
+                                   w, out, st, pdl_ok);
   }
 }
 
+// pdl_ok: launch as a programmatic dependent launch (false right after an
+// event wait on the stream, whose dependency must stay a full one)
 int launch_attn(const kvr_dims *d, const uint16_t *q, const uint16_t *k_pool,
                 const uint16_t *v_pool, int64_t n_phys, const int32_t *sel_phys, int k,
                 float scale, const uint8_t *filter, int filter_mode, AttnWs w, float *out,
-                cudaStream_t st) {
+                cudaStream_t st, bool pdl_ok = true) {
   CUtensorMap tk, tv;
   int rc = make_pool_map(&tk, k_pool, d, n_phys);
   if (rc) return rc;
@@ -356,10 +396,10 @@ int launch_attn(const kvr_dims *d, const uint16_t *q, const uint16_t *k_pool,
   if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(kD));
   const int np = static_cast<int>(n_phys);
   switch (d->n_q_heads / d->n_kv_heads) {
-    case 1: return launch_attn_g<1>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st);
-    case 2: return launch_attn_g<2>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st);
-    case 4: return launch_attn_g<4>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st);
-    default: return launch_attn_g<8>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st);
+    case 1: return launch_attn_g<1>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok);
+    case 2: return launch_attn_g<2>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok);
+    case 4: return launch_attn_g<4>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok);
+    default: return launch_attn_g<8>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok);
   }
 }
 
@@ -648,12 +688,12 @@ int kvr_speculative_step_recall(const kvr_dims *dims, kvr_spec_state *st, const 
   const int64_t n_phys = static_cast<int64_t>(dims->batch) * wset->n_slots;
   const AttnWs aw = carve_attn(dims, top_k, (uint8_t *)ws + select_ws_bytes(dims));
   rc = launch_attn(dims, q_t, wset->k_slots, wset->v_slots, n_phys, sel_used_slot, top_k, scale,
-                   corrected, 1, aw, out, s);
+                   corrected, 1, aw, out, s, false);
   if (rc) return rc;
   e = cudaStreamWaitEvent(s, er, 0);
   if (e != cudaSuccess) return cuda_fail(e, "main stream wait");
   return launch_attn(dims, q_t, wset->k_slots, wset->v_slots, n_phys, sel_used_slot, top_k, scale,
-                     corrected, 2, aw, out, s);
+                     corrected, 2, aw, out, s, false);
 }
 
 int kvr_get_status(void *stream, uint32_t *status_out) {

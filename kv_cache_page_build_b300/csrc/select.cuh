@@ -56,9 +56,7 @@ constexpr int kScCPS = 2;                                  // CTAs per SM
 constexpr int kScSmem = kScS * kScStageBytes + 1024;       // 96 KiB + alignment of the ring
 constexpr int kScMaxCtas = 512;
 constexpr int kScMinPagesPerWorker = 32;
-constexpr int kTkThreads = 256;
 constexpr int kSelBins = 2048;
-static_assert(kTkThreads == 256 && kSelBins % kTkThreads == 0, "top-k bin ownership");
 
 struct SpecArgs {
   int enabled;                 // 0: plain selection
@@ -114,7 +112,11 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
     fence_barrier_init();
   }
   __syncthreads();
-  if (tid == 0) pdl_launch_dependents();  // the top-k kernel may be scheduled now
+  // Launched as a programmatic dependent launch, this kernel's setup above
+  // overlaps the previous kernel; every global read and write comes after
+  // this wait.  Then the top-k kernel may be scheduled.
+  pdl_wait();
+  if (tid == 0) pdl_launch_dependents();
 
   // ------------------------------------------------------------ producer warp
   if (warp == kScNC) {
@@ -252,56 +254,61 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
   }
 }
 
-// Selection of one (b, g) unit from its N scores (kTkThreads threads; the
-// keys live in dynamic shared memory, N * 4 bytes).
-template <int G>
-__global__ void __launch_bounds__(kTkThreads)
+// Selection of one (b, g) unit from its N <= NT * KPT scores, one CTA of NT
+// threads.  Each thread keeps KPT keys in registers: key j of lane l in warp
+// w is page (w KPT + j) 32 + l, so every warp holds consecutive
+// blocks of 32 pages.  The histogram rounds issue all of a thread's shared
+// atomics back to back (histograms double-buffered, a round's bins cleared
+// by their owners once read; the bin search is a per-warp scan plus one
+// exchange of warp totals), and the ordered compaction works on ballots of
+// the 32-page blocks, so no pass walks keys through shared memory.
+template <int G, int NT, int KPT>
+__global__ void __launch_bounds__(NT, 1)
     k_topk(const uint16_t *__restrict__ q, const int32_t *__restrict__ page_table, int H, int N,
            int k, const float *__restrict__ ws_scores, int32_t *__restrict__ sel_out,
            int32_t *__restrict__ sel_phys_out, SpecArgs spec) {
-  extern __shared__ __align__(16) uint32_t keys[];
-  __shared__ uint32_t s_hist[kSelBins];
-  __shared__ uint32_t s_scan[kTkThreads / 32];
-  __shared__ uint32_t s_mm[2 * (kTkThreads / 32)];
-  __shared__ uint32_t s_bin, s_bin_above, s_bin_cnt, s_corr;
+  constexpr int NW = NT / 32, BPT = kSelBins / NT;  // warps, bins per thread
+  static_assert(NT % 32 == 0 && kSelBins % NT == 0, "bins are split evenly over the threads");
+  __shared__ uint32_t s_hist[2][kSelBins];
+  __shared__ uint32_t s_w1[NW], s_w2[NW];
+  __shared__ uint32_t s_bin, s_bin_above, s_bin_cnt;
   __shared__ float s_cos[8];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = blockIdx.x, b = blockIdx.y;
   const int Hq = H * G;
   const size_t unit = static_cast<size_t>(b) * H + g;
+  const int base = warp * KPT * 32 + lane;  // page of key j: base + 32 j
 
-  // the speculative mode's query slices: loaded now, used after the top-k
+  // Inputs of the speculative mode, loaded now and used after the top-k: the
+  // query slices and the previous selection.  Safe before the wait:
+  // k_page_scores, the kernel this one depends on, passed its own wait before
+  // letting this one start, and writes neither.
   uint2 qa = make_uint2(0u, 0u), qb = make_uint2(0u, 0u);
   const bool cos_lane = spec.enabled && spec.step > 0 && warp < G;
   if (cos_lane) {
-    const size_t base = (static_cast<size_t>(b) * Hq + g * G + warp) * kD + 4 * lane;
-    qa = *reinterpret_cast<const uint2 *>(q + base);
-    qb = *reinterpret_cast<const uint2 *>(spec.q_prev + base);
+    const size_t qo = (static_cast<size_t>(b) * Hq + g * G + warp) * kD + 4 * lane;
+    qa = *reinterpret_cast<const uint2 *>(q + qo);
+    qb = *reinterpret_cast<const uint2 *>(spec.q_prev + qo);
   }
+  const int sp0 = spec.enabled && tid < k ? spec.sel_prev[unit * k + tid] : -1;
+  for (int i = tid; i < 2 * kSelBins; i += NT) (&s_hist[0][0])[i] = 0u;
 
   pdl_wait();  // the scores of k_page_scores are complete and visible
 
-  // keys of the row and their range; all loads of a thread in flight at once
+  // the keys, all loads in flight at once, and their range
   const float *row = ws_scores + unit * N;
+  float sv[KPT];
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) sv[j] = base + 32 * j < N ? __ldg(row + base + 32 * j) : 0.f;
+  uint32_t key[KPT];
   uint32_t kmn = 0xffffffffu, kmx = 0u;
-#pragma unroll 1
-  for (int i0 = 0; i0 < N; i0 += 8 * kTkThreads) {
-    float sv[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = i0 + j * kTkThreads + tid;
-      sv[j] = i < N ? __ldg(row + i) : 0.f;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = i0 + j * kTkThreads + tid;
-      if (i < N) {
-        const uint32_t key = score_key(sv[j]);
-        keys[i] = key;
-        kmn = min(kmn, key);
-        kmx = max(kmx, key);
-      }
+  for (int j = 0; j < KPT; ++j) {
+    key[j] = score_key(sv[j]);
+    if (base + 32 * j < N) {
+      kmn = min(kmn, key[j]);
+      kmx = max(kmx, key[j]);
     }
   }
 #pragma unroll
@@ -310,44 +317,59 @@ __global__ void __launch_bounds__(kTkThreads)
     kmx = max(kmx, __shfl_xor_sync(0xffffffffu, kmx, m));
   }
   if (lane == 0) {
-    s_mm[warp] = kmn;
-    s_mm[kTkThreads / 32 + warp] = kmx;
+    s_w1[warp] = kmn;
+    s_w2[warp] = kmx;
   }
   __syncthreads();
   uint32_t L = 0xffffffffu, R = 0u;
 #pragma unroll
-  for (int w = 0; w < kTkThreads / 32; ++w) {
-    L = min(L, s_mm[w]);
-    R = max(R, s_mm[kTkThreads / 32 + w]);
+  for (int w = 0; w < NW; ++w) {
+    L = min(L, s_w1[w]);
+    R = max(R, s_w2[w]);
   }
   // invariant: `need` of the `cnt` keys in [L, R] are still to be taken;
   // every key above R is taken
   uint32_t need = static_cast<uint32_t>(k), cnt = static_cast<uint32_t>(N);
+  int buf = 0;
 #pragma unroll 1
   while (cnt != need && L != R) {
     const uint32_t span = R - L;
     const int shift = span < kSelBins ? 0 : (32 - __clz(span)) - 11;
-    for (int i = tid; i < kSelBins; i += kTkThreads) s_hist[i] = 0u;
-    __syncthreads();
-    for (int i = tid; i < N; i += kTkThreads) {
-      const uint32_t key = keys[i];
-      if (key >= L && key <= R) atomicAdd(&s_hist[(key - L) >> shift], 1u);
-    }
-    __syncthreads();
-    // thread tid owns bins [8 tid, 8 tid + 8); find the bin holding the need-th largest
-    uint32_t c[kSelBins / kTkThreads], mine = 0u;
+    uint32_t *hist = s_hist[buf];
 #pragma unroll
-    for (int e = 0; e < kSelBins / kTkThreads; ++e) {
-      c[e] = s_hist[(kSelBins / kTkThreads) * tid + e];
+    for (int j = 0; j < KPT; ++j)
+      if (base + 32 * j < N && key[j] >= L && key[j] <= R)
+        atomicAdd(&hist[(key[j] - L) >> shift], 1u);
+    __syncthreads();
+    // thread tid owns bins [BPT tid, BPT tid + BPT); clear them for the round
+    // after next once read
+    uint32_t c[BPT], mine = 0u;
+#pragma unroll
+    for (int e = 0; e < BPT; ++e) {
+      c[e] = hist[BPT * tid + e];
+      hist[BPT * tid + e] = 0u;
       mine += c[e];
     }
-    uint32_t total;
-    const uint32_t below = block_exclusive_scan<kTkThreads>(mine, s_scan, total);
-    uint32_t above_here = total - below - mine;  // keys of the interval in higher bins
+    uint32_t incl = mine;
 #pragma unroll
-    for (int e = kSelBins / kTkThreads - 1; e >= 0; --e) {
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_w1[warp] = incl;
+    __syncthreads();
+    uint32_t total = 0u, before = 0u;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const uint32_t x = s_w1[w];
+      total += x;
+      before += w < warp ? x : 0u;
+    }
+    uint32_t above_here = total - (before + incl);  // keys of the interval in higher bins
+#pragma unroll
+    for (int e = BPT - 1; e >= 0; --e) {
       if (above_here < need && need <= above_here + c[e]) {
-        s_bin = static_cast<uint32_t>((kSelBins / kTkThreads) * tid + e);
+        s_bin = static_cast<uint32_t>(BPT * tid + e);
         s_bin_above = above_here;
         s_bin_cnt = c[e];
       }
@@ -360,7 +382,7 @@ __global__ void __launch_bounds__(kTkThreads)
     cnt = s_bin_cnt;
     R = static_cast<uint32_t>(min(static_cast<unsigned long long>(R), nr));
     L = nl;
-    __syncthreads();  // s_bin* and s_hist free for the next round
+    buf ^= 1;
   }
 
   // ---- speculative mode: group similarity and the correction decision
@@ -386,29 +408,26 @@ __global__ void __launch_bounds__(kTkThreads)
       if (lane == 0) s_cos[warp] = (nx > 0.f && ny > 0.f) ? dot / (sqrtf(nx) * sqrtf(ny)) : 0.f;
     }
     __syncthreads();
+    // every thread takes the same decision from the same values
+    float cb = __int_as_float(0x7fc00000);  // NaN: no previous query at step 0
+    if (spec.step > 0) {
+      float sum = 0.f;
+      for (int h = 0; h < G; ++h) sum += s_cos[h];
+      cb = sum / G;
+      corrected = cb < spec.tau;
+    }
     if (tid == 0) {
-      float cb = __int_as_float(0x7fc00000);  // NaN: no previous query at step 0
-      bool corr = true;
-      if (spec.step > 0) {
-        float sum = 0.f;
-        for (int h = 0; h < G; ++h) sum += s_cos[h];
-        cb = sum / G;
-        corr = cb < spec.tau;
-      }
-      s_corr = corr ? 1u : 0u;
-      spec.corrected[unit] = corr ? 1 : 0;
+      spec.corrected[unit] = corrected ? 1 : 0;
       if (spec.cbar) spec.cbar[unit] = cb;
     }
-    __syncthreads();
-    corrected = s_corr != 0u;
     // q_prev <- q_t for this group's heads (only this CTA reads them)
-    for (int i = tid; i < G * kD / 8; i += kTkThreads) {
+    for (int i = tid; i < G * kD / 8; i += NT) {
       const size_t off = (static_cast<size_t>(b) * Hq + g * G) * kD + 8 * i;
       *reinterpret_cast<uint4 *>(spec.q_prev + off) = *reinterpret_cast<const uint4 *>(q + off);
     }
-    if (!corrected) {  // reuse: sel_used <- previous selection (before it is replaced)
-      for (int i = tid; i < k; i += kTkThreads) {
-        const int p = spec.sel_prev[unit * k + i];
+    if (!corrected) {  // reuse: sel_used <- previous selection (read before it is replaced)
+      for (int i = tid; i < k; i += NT) {
+        const int p = i == tid ? sp0 : spec.sel_prev[unit * k + i];
         spec.sel_used[unit * k + i] = p;
         if (spec.sel_used_phys) {
           int phys = -1;
@@ -422,42 +441,69 @@ __global__ void __launch_bounds__(kTkThreads)
         }
       }
     }
-    __syncthreads();
   }
 
-  // ---- ordered compaction of the selection (ascending page ids): every key
-  // above R, then the first `need` keys of [L, R] by page id (all of them
-  // when cnt == need)
-  const int per = (N + kTkThreads - 1) / kTkThreads;
-  const int beg = min(N, tid * per), end = min(N, beg + per);
-  uint32_t n_gt = 0u, n_eq = 0u;
-  for (int i = beg; i < end; ++i) {
-    const uint32_t key = keys[i];
-    n_gt += (key > R);
-    n_eq += (key >= L && key <= R);
+  // ---- ordered compaction (ascending page ids): every key above R, then the
+  // first `need` keys of [L, R] by page id (all of them when cnt == need).
+  // Per 32-page block: ballots of the two kinds; per warp: running counts;
+  // across warps: one exchange of the warp totals.
+  const uint32_t lt = (1u << lane) - 1u;  // lanes below this one
+  uint32_t w_gt = 0u, w_eq = 0u;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const bool valid = base + 32 * j < N;
+    w_gt += __popc(__ballot_sync(0xffffffffu, valid && key[j] > R));
+    w_eq += __popc(__ballot_sync(0xffffffffu, valid && key[j] >= L && key[j] <= R));
   }
-  uint32_t total;
-  const uint32_t eq_base = block_exclusive_scan<kTkThreads>(n_eq, s_scan, total);
-  uint32_t n_take = n_gt;
-  for (uint32_t e = 0; e < n_eq; ++e) n_take += (eq_base + e < need);
-  uint32_t out = block_exclusive_scan<kTkThreads>(n_take, s_scan, total);
-  uint32_t eq_seen = 0u;
-  for (int i = beg; i < end; ++i) {
-    const uint32_t key = keys[i];
-    bool take = key > R;
-    if (key >= L && key <= R) take = (eq_base + eq_seen++) < need;
-    if (!take) continue;
-    if (out >= static_cast<uint32_t>(k)) break;  // never write past this unit's k entries
-    const size_t o = unit * k + out++;
+  __syncthreads();  // s_w* free; every read of the previous selection is done
+  if (lane == 0) {
+    s_w1[warp] = w_gt;
+    s_w2[warp] = w_eq;
+  }
+  __syncthreads();
+  uint32_t gt_seen = 0u, eq_seen = 0u;  // keys of the two kinds in lower pages
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    gt_seen += w < warp ? s_w1[w] : 0u;
+    eq_seen += w < warp ? s_w2[w] : 0u;
+  }
+  int pos[KPT];
+  int nsel = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {  // the ballots again, now in page order
+    const bool valid = base + 32 * j < N;
+    const bool is_gt = valid && key[j] > R, is_eq = valid && key[j] >= L && key[j] <= R;
+    const uint32_t m_gt = __ballot_sync(0xffffffffu, is_gt);
+    const uint32_t m_eq = __ballot_sync(0xffffffffu, is_eq);
+    const uint32_t gb = gt_seen + __popc(m_gt & lt), eb = eq_seen + __popc(m_eq & lt);
+    const bool take = is_gt || (is_eq && eb < need);
+    const uint32_t out = gb + min(eb, need);  // selected keys in lower pages
+    pos[j] = take && out < static_cast<uint32_t>(k) ? static_cast<int>(out) : -1;
+    nsel += pos[j] >= 0;
+    gt_seen += __popc(m_gt);
+    eq_seen += __popc(m_eq);
+  }
+  // page-table entries of the selected pages: all loads before any store
+  int phys[KPT];
+  const bool want_phys = spec.enabled ? (corrected && spec.sel_used_phys && !spec.page2slot)
+                                      : sel_phys_out != nullptr;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) phys[j] = want_phys && pos[j] >= 0 ? __ldg(ptab + base + 32 * j) : -1;
+  if (nsel == 0) return;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    if (pos[j] < 0) continue;
+    const int i = base + 32 * j;
+    const size_t o = unit * k + pos[j];
     if (spec.enabled) {
       spec.sel_prev[o] = i;
       if (corrected) {
         spec.sel_used[o] = i;
-        if (spec.sel_used_phys && !spec.page2slot) spec.sel_used_phys[o] = ptab[i];
+        if (want_phys) spec.sel_used_phys[o] = phys[j];
       }
     } else {
       sel_out[o] = i;
-      if (sel_phys_out) sel_phys_out[o] = ptab[i];
+      if (want_phys) sel_phys_out[o] = phys[j];
     }
   }
 }

@@ -95,6 +95,22 @@ def test_tie_goes_to_lower_page_id():
         assert sc[kth] == sc[target]
 
 
+@pytest.mark.parametrize("n_pages", [300, 3000, 5000])
+def test_all_scores_equal_selects_lowest_ids(n_pages):
+    """Every page holds the same keys, so all scores tie and the selection is
+    pages 0 .. k-1 in order (the histogram search ends at once on L == R)."""
+    wl = synth.custom(batch=1, n_q_heads=8, n_kv_heads=2, head_dim=128, page_size=16, n_pages=n_pages, top_k=37)
+    case = synth.make_case(wl)
+    c2 = synth.Case(**{**case.__dict__, "k_pool": case.k_pool.copy()})
+    c2.k_pool[:] = c2.k_pool[c2.page_table[0, 0]]
+    summ = oracle.summaries(c2.k_pool, c2.page_table)
+    want = oracle.topk(oracle.scores(c2.q, *summ), wl.top_k)
+    np.testing.assert_array_equal(want, np.broadcast_to(np.arange(wl.top_k), want.shape))
+    sel, sel_phys, _ = gh.select(gh.DevCase(c2))
+    np.testing.assert_array_equal(sel.cpu().numpy(), want)
+    np.testing.assert_array_equal(sel_phys.cpu().numpy()[0], c2.page_table[0, want[0]])
+
+
 # ---------------------------------------------------------------- attention
 
 @pytest.mark.parametrize("cid", [1, 2, 3])
@@ -131,6 +147,9 @@ SHAPES = [
     dict(top_k=1, batch=3),
     dict(n_pages=1, top_k=1, page_size=16),
     dict(channel_scale=True, n_pages=300, top_k=40),
+    dict(n_pages=1500, top_k=100, batch=1, page_size=16),      # ragged, 16 keys per top-k thread
+    dict(n_pages=5000, top_k=130, batch=1, page_size=16, n_kv_heads=1),   # 1024-thread top-k
+    dict(n_pages=16384, top_k=256, batch=1, page_size=16, n_q_heads=4, n_kv_heads=1),  # most pages
 ]
 
 
