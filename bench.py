@@ -366,10 +366,10 @@ def run_gpu(args, world, rank, local):
         "selected_kv_gbs": round(achieved, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "k_sparse_decode (+ k_attn_merge)", "bytes_per_launch": attn_bytes,
+                     "kernel": "k_sparse_decode", "bytes_per_launch": attn_bytes,
                      "launch_us": round(attn_avg * 1e6, 3)},
         "kernels": {
-            "attention (k_sparse_decode + k_attn_merge)": {"us": round(attn_avg * 1e6, 3), "bytes": attn_bytes,
+            "attention (k_sparse_decode)": {"us": round(attn_avg * 1e6, 3), "bytes": attn_bytes,
                                                            "gbs": round(achieved, 1)},
             "selection (k_page_scores + k_topk)": {"us": round(sel_avg * 1e6, 3) if sel_avg else None,
                                                    "bytes": summ_bytes,
@@ -378,7 +378,7 @@ def run_gpu(args, world, rank, local):
                                   "gbs": round((k_bytes + summ_bytes) / (summ_ms / 1e3) / 1e9, 1),
                                   "note": "once per cache (prefill), not in the step"},
         },
-        "gpu_launches": 4 * args.steps,  # k_page_scores, k_topk, k_sparse_decode, k_attn_merge
+        "gpu_launches": 3 * args.steps,  # k_page_scores, k_topk, k_sparse_decode
         "e2e": {"value": round(e2e_value, 2), "unit": "steps/s",
                 "h2d_bytes_per_step": B * Hq * D * 2, "d2h_bytes_per_step": B * Hq * D * 4,
                 "how": f"{n_e2e} eager kvr_speculative_step calls, q copied in from pinned host memory and "

@@ -8,18 +8,19 @@
 // attend over the tokens of the unit's k selected pages:
 //   out[b][h] = sum_t softmax_t(scale * q_h . K_t) V_t .
 //
-// Work decomposition.  The selected pages of all units, cut into chunks of
-// C = min(P, 32) tokens, form one flat list (unit-major, the order of
-// sel_phys).  Every consumer warp of the grid is an independent "worker":
-// worker v of n owns the contiguous range [v W / n, (v + 1) W / n) of the
-// list, so all workers stream the same number of chunks.  Where a range
-// covers part of a unit, the worker writes a partial (m, l, o) for that
-// "segment" straight from its registers; k_attn_merge, launched right after,
-// merges each split unit's segments in segment order.  A unit whose chunks
-// all fall in one worker's range is normalised directly.
+// Work decomposition.  Unit u is handled by one cluster of Q CTAs (Q in
+// {1, 2, 4, 8}, chosen on the host so that the Q x units CTAs are resident
+// together when they fit).  The unit's k CPP chunks of C = min(P, 32) tokens
+// are cut into Q NC equal contiguous ranges, one per consumer warp (a
+// "worker") of the cluster.  A worker keeps its split's running (m, l, O) in
+// registers and leaves it in its CTA's shared memory at the end; after a
+// cluster barrier, CTA r merges channels [r D/Q, (r+1) D/Q) of the G heads
+// from all Q NC partials, read through distributed shared memory, with a
+// log-sum-exp rescale, and writes them to `out`.  A second cluster barrier
+// keeps every CTA resident until its partials have been read.  Nothing of
+// the split goes through global memory and no second kernel is needed.
 //
-// Inside a CTA (CPS per SM, all resident) the warps share nothing but the
-// shared-memory ring:
+// Inside a CTA (CPS per SM) the warps share the shared-memory ring:
 //   producer  warp NC; lane w feeds consumer warp w, which owns R stages of
 //        the ring: as soon as the warp releases a stage, the lane issues the
 //        warp's next chunk into it (four tiled TMA copies: the 64-channel
@@ -41,21 +42,21 @@
 // from the tensor cores' peak; they are used because they cut the issue
 // slots per chunk about five-fold against CUDA-core FMAs, which keeps the
 // consumers well ahead of the memory stream.
-// Every wait is bounded; after a timeout the CTA stops issuing copies and
-// drains the ones in flight.
+// Every wait on a copy is bounded; after a timeout the CTA stops issuing
+// copies, drains the ones in flight and still takes part in both cluster
+// barriers, which every thread of the cluster reaches after bounded work.
 #pragma once
 
 #include "common.cuh"
 
 namespace kvr {
 
-constexpr int kAttnNC = 3;                         // consumer warps per CTA
+constexpr int kAttnNC = 2;                         // consumer warps per CTA
 constexpr int kAttnThreads = 32 * (kAttnNC + 1);   // + one producer warp
-constexpr int kAttnMaxCtas = 512;                  // bound on the grid
-constexpr int kAttnMaxWorkers = kAttnMaxCtas * kAttnNC;
-constexpr int kAttnMinChunksPerWorker = 2;
 constexpr int kAttnIds = 128;                      // page ids of a worker range kept in shared memory
 constexpr int kAttnCPS = 2;                        // CTAs per SM
+constexpr int kAttnMaxQ = 8;                       // CTAs per cluster (the portable limit)
+constexpr int kAttnWarpRing = 48 * 1024;           // ring bytes of one consumer warp
 constexpr int kSmemPerSM = 228 * 1024;             // shared memory of one SM
 
 template <int G, int P>
@@ -66,19 +67,14 @@ struct AttnCfg {
   static constexpr int KP = C / 16;                // 16-token k-steps of the PV MMA
   static constexpr int kHalf = C * 128;            // 64 channels of C rows (swizzled)
   static constexpr int kStageBytes = 4 * kHalf;    // K lo, K hi, V lo, V hi
-  static constexpr int R = 32768 / kStageBytes;    // stages per consumer warp (32 KiB)
+  static constexpr int R = kAttnWarpRing / kStageBytes;  // stages per consumer warp
   static constexpr int S = kAttnNC * R;            // ring depth
-  static constexpr int kSmem = S * kStageBytes + 1024;  // + 1 KiB to align the ring
-  static_assert(kAttnCPS * (kSmem + 2048 + 4 * kAttnNC * kAttnIds) <= kSmemPerSM,
-                "CTAs per SM must fit");
+  static constexpr int kSmem = S * kStageBytes + 1024;   // + 1 KiB to align the ring
+  static constexpr int kStatic = kAttnNC * G * kD * 4 + kAttnMaxQ * kAttnNC * G * 8 +
+                                 kAttnNC * kAttnIds * 4 + S * 20 + 64;
+  static_assert(kAttnCPS * (kSmem + kStatic + 1024) <= kSmemPerSM, "CTAs per SM must fit");
   static_assert(CPP * C == P && NB * 8 == C && KP * 16 == C && R >= 2, "chunk tiling");
 };
-
-// Index of the worker (or CTA) whose range holds flat chunk w (ranges start
-// at c W / n).
-__device__ __forceinline__ int attn_cta_of(long long w, long long W, int n) {
-  return static_cast<int>(((w + 1) * n + W - 1) / W) - 1;
-}
 
 __device__ __forceinline__ bool attn_unit_active(const uint8_t *filter, int filter_mode,
                                                  long long u) {
@@ -86,56 +82,89 @@ __device__ __forceinline__ bool attn_unit_active(const uint8_t *filter, int filt
   return (filter[u] != 0) == (filter_mode == 2);
 }
 
-// One chunk of C tokens for head row gq of a consumer warp: QK on the tensor
-// cores, online-softmax update of (m_run, l_run) and O^T += V^T P^T.
+// One chunk of C tokens for a consumer warp.
+//   QK   S^T[t][h] = K_t . q_h with the tokens on the MMA's 16-row side and
+//        the heads as its 8 columns (columns G..7 zero): C/16 row blocks x 8
+//        channel k-steps; K fragments by ldmatrix, q as B fragments held in
+//        registers.  Lane (gq, tq) gets tokens 16 mt + gq (+8) of heads 2tq,
+//        2tq + 1.
+//   softmax  online, base 2 (logits prescaled by scale * log2 e); the lane's
+//        running (m, l) are those of its heads 2tq, 2tq + 1.
+//   PV   O^T[c][h] += V^T[c][t] P^T[t][h]: V fragments by transposing
+//        ldmatrix; P^T as B fragments by transposing the accumulator tiles
+//        in registers (movmatrix).  P is split into a bf16 high part and a
+//        bf16 residual, so the weights keep about 16 bits: for G <= 4 the
+//        residual rides in columns h + 4 of the same MMA (the output of head
+//        h is then column h plus column h + 4); for G = 8 it takes a second
+//        MMA.
 template <int G, int P>
-__device__ __forceinline__ void attn_chunk(uint32_t kb, const uint32_t (&qa)[8][2],
-                                           float scale_log2, float &m_run, float &l_run,
+__device__ __forceinline__ void attn_chunk(uint32_t kb, const uint32_t (&qb)[8][2],
+                                           float scale_log2, float (&m_run)[2], float (&l_run)[2],
                                            float (&o)[8][4], int lane) {
   using Cfg = AttnCfg<G, P>;
-  constexpr int HALF = Cfg::kHalf;
-  const int gq = lane >> 2, tq = lane & 3, mi = lane >> 3, mr = lane & 7;
+  constexpr int HALF = Cfg::kHalf, MT = Cfg::C / 16;
+  constexpr bool kPair = G <= 4;
+  const int tq = lane & 3, mi = lane >> 3, mr = lane & 7;
   const uint32_t vb = kb + 2 * HALF;
-  // ---- QK: sc[nb] = S[gq][8 nb + 2 tq (+1)]
-  float sc[Cfg::NB][4];
+  // ---- S^T, even and odd channel k-steps in separate accumulators
+  float st[MT][4], su[MT][4];
 #pragma unroll
-  for (int nb = 0; nb < Cfg::NB; ++nb) {
-    sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int kq = 0; kq < 4; ++kq) {  // channel chunks 4kq .. 4kq+3 = k-steps 2kq, 2kq+1
-      uint32_t bf[4];
-      ldsm_x4(swz<HALF>(kb, 8 * nb + mr, 4 * kq + mi), bf);
-      mma_bf16_16816(sc[nb], qa[2 * kq][0], 0u, qa[2 * kq][1], 0u, bf[0], bf[1]);
-      mma_bf16_16816(sc[nb], qa[2 * kq + 1][0], 0u, qa[2 * kq + 1][1], 0u, bf[2], bf[3]);
+    for (int e = 0; e < 4; ++e) st[mt][e] = su[mt][e] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      uint32_t a[4];
+      ldsm_x4(swz<HALF>(kb, 16 * mt + 8 * (mi & 1) + mr, 2 * kk + (mi >> 1)), a);
+      if (kk & 1)
+        mma_bf16_16816(su[mt], a[0], a[1], a[2], a[3], qb[kk][0], qb[kk][1]);
+      else
+        mma_bf16_16816(st[mt], a[0], a[1], a[2], a[3], qb[kk][0], qb[kk][1]);
+    }
+  // ---- online softmax for heads 2tq (e = 0, 2) and 2tq + 1 (e = 1, 3)
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) st[mt][e] = (st[mt][e] + su[mt][e]) * scale_log2;
+    mx0 = fmaxf(mx0, fmaxf(st[mt][0], st[mt][2]));
+    mx1 = fmaxf(mx1, fmaxf(st[mt][1], st[mt][3]));
+  }
+#pragma unroll
+  for (int m = 4; m <= 16; m <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, m));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, m));
+  }
+  const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+  const float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
+  const bool on0 = 2 * tq < G, on1 = 2 * tq + 1 < G;
+  float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    st[mt][0] = on0 ? exp2f(st[mt][0] - mn0) : 0.f;
+    st[mt][2] = on0 ? exp2f(st[mt][2] - mn0) : 0.f;
+    st[mt][1] = on1 ? exp2f(st[mt][1] - mn1) : 0.f;
+    st[mt][3] = on1 ? exp2f(st[mt][3] - mn1) : 0.f;
+    ls0 += st[mt][0] + st[mt][2];
+    ls1 += st[mt][1] + st[mt][3];
+  }
+  l_run[0] = fmaf(l_run[0], al0, ls0);
+  l_run[1] = fmaf(l_run[1], al1, ls1);
+  m_run[0] = mn0;
+  m_run[1] = mn1;
+  // rescale O; with the residual in columns h + 4, lanes tq >= 2 hold the
+  // residual columns of heads 2tq - 4, 2tq - 3 (the lane tq - 2's heads)
+  float a0 = al0, a1 = al1;
+  if (kPair) {
+    const float x0 = __shfl_xor_sync(0xffffffffu, al0, 2);
+    const float x1 = __shfl_xor_sync(0xffffffffu, al1, 2);
+    if (tq >= 2) {
+      a0 = x0;
+      a1 = x1;
     }
   }
-  // ---- online softmax for head gq (4 lanes per head, 2 tokens per block each)
-  float mx = -INFINITY;
-#pragma unroll
-  for (int nb = 0; nb < Cfg::NB; ++nb) {
-    sc[nb][0] *= scale_log2;
-    sc[nb][1] *= scale_log2;
-    mx = fmaxf(mx, fmaxf(sc[nb][0], sc[nb][1]));
-  }
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-  const float m_new = fmaxf(m_run, mx);
-  const float alpha = exp2f(m_run - m_new);
-  const bool row_on = gq < G;
-  float ls = 0.f;
-#pragma unroll
-  for (int nb = 0; nb < Cfg::NB; ++nb) {
-    const float p0 = row_on ? exp2f(sc[nb][0] - m_new) : 0.f;
-    const float p1 = row_on ? exp2f(sc[nb][1] - m_new) : 0.f;
-    sc[nb][0] = p0;
-    sc[nb][1] = p1;
-    ls += p0 + p1;
-  }
-  l_run = fmaf(l_run, alpha, ls);
-  m_run = m_new;
-  // rescale O: this lane's columns are heads 2tq and 2tq + 1
-  const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * tq);
-  const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * tq + 4);
 #pragma unroll
   for (int mb = 0; mb < 8; ++mb) {
     o[mb][0] *= a0;
@@ -143,42 +172,50 @@ __device__ __forceinline__ void attn_chunk(uint32_t kb, const uint32_t (&qa)[8][
     o[mb][2] *= a0;
     o[mb][3] *= a1;
   }
-  // ---- P^T as B fragments: high bf16 part and bf16 residual
-  uint32_t ph[Cfg::KP][2], pl[Cfg::KP][2];
+  // ---- P^T as B fragments: 8x8 tiles (tokens 16 mt + 8 r .., heads) transposed
+  uint32_t pb[MT][2], pl[MT][2];
 #pragma unroll
-  for (int kp = 0; kp < Cfg::KP; ++kp)
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float x0 = sc[2 * kp + e][0], x1 = sc[2 * kp + e][1];
+    for (int r = 0; r < 2; ++r) {
+      const float x0 = st[mt][2 * r], x1 = st[mt][2 * r + 1];
       const uint32_t hi = pack_bf16x2(x0, x1);
-      ph[kp][e] = hi;
-      pl[kp][e] = pack_bf16x2(x0 - __uint_as_float(hi << 16),
-                              x1 - __uint_as_float(hi & 0xffff0000u));
+      const uint32_t lo = pack_bf16x2(x0 - __uint_as_float(hi << 16),
+                                      x1 - __uint_as_float(hi & 0xffff0000u));
+      if (kPair) {
+        const uint32_t lo_s = __shfl_xor_sync(0xffffffffu, lo, 2);
+        pb[mt][r] = movmatrix_trans(tq < 2 ? hi : lo_s);
+        pl[mt][r] = 0u;
+      } else {
+        pb[mt][r] = movmatrix_trans(hi);
+        pl[mt][r] = movmatrix_trans(lo);
+      }
     }
   // ---- PV: O^T[16 mb ..][heads] += V^T[16 mb ..][16 kp ..] P^T
 #pragma unroll
   for (int mb = 0; mb < 8; ++mb) {
 #pragma unroll
-    for (int kp = 0; kp < Cfg::KP; ++kp) {
+    for (int kp = 0; kp < MT; ++kp) {
       uint32_t va[4];
       ldsm_x4_trans(swz<HALF>(vb, 16 * kp + 8 * (mi >> 1) + mr, 2 * mb + (mi & 1)), va);
-      mma_bf16_16816(o[mb], va[0], va[1], va[2], va[3], ph[kp][0], ph[kp][1]);
-      mma_bf16_16816(o[mb], va[0], va[1], va[2], va[3], pl[kp][0], pl[kp][1]);
+      mma_bf16_16816(o[mb], va[0], va[1], va[2], va[3], pb[kp][0], pb[kp][1]);
+      if (!kPair) mma_bf16_16816(o[mb], va[0], va[1], va[2], va[3], pl[kp][0], pl[kp][1]);
     }
   }
 }
 
-// filter_mode: 0 every unit; 1 only units with filter[unit] == 0; 2 only != 0
+// filter_mode: 0 every unit; 1 only units with filter[unit] == 0; 2 only != 0.
+// Grid: units x Q CTAs in clusters of Q (cluster c = unit c).
 template <int G, int P>
 __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
     k_sparse_decode(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const uint16_t *__restrict__ q,
-                    const int32_t *__restrict__ sel_phys, int H, int k, int n_phys, long long W,
+                    const int32_t *__restrict__ sel_phys, int H, int k, int n_phys, int Q,
                     float scale_log2, const uint8_t *__restrict__ filter, int filter_mode,
-                    float *__restrict__ part_o, float2 *__restrict__ part_ml,
                     float *__restrict__ out) {
   using Cfg = AttnCfg<G, P>;
   constexpr int NC = kAttnNC, CPP = Cfg::CPP, HALF = Cfg::kHalf, R = Cfg::R, S = Cfg::S;
+  constexpr int kIdRounds = kAttnIds / 32;
   extern __shared__ uint8_t smem_raw[];
   // the swizzle pattern repeats every 1024 bytes: align the ring to it
   uint8_t *smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
@@ -186,11 +223,25 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
   __shared__ __align__(8) uint64_t full[S], empty[S];
   __shared__ int s_ok[S];
   __shared__ int s_ids[NC][kAttnIds];  // page ids of the first kAttnIds chunks of each worker
+  // partials of the cluster's workers for this CTA's channel slice:
+  // [worker][head][channel of the slice] and (m, l) per worker and head
+  __shared__ __align__(16) float s_recv[NC * G * kD];
+  __shared__ __align__(8) float2 s_mlr[kAttnMaxQ * NC * G];
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n_workers = gridDim.x * NC;
-  const long long kc = static_cast<long long>(k) * CPP;  // chunks per unit
+  const int rank = cluster_ctarank();
+  const long long u = blockIdx.x / Q;
+  const int b = static_cast<int>(u / H), g = static_cast<int>(u % H);
+  const int nw = Q * NC;                                  // workers of the unit
+  const int per = kD / Q;                                 // channels merged by each CTA
+  const long long kc = static_cast<long long>(k) * CPP;   // chunks of the unit
+  // range of this CTA's worker w: chunks [a, a + n) of the unit
+  auto worker_range = [&](int w, long long &a, int &n) {
+    const long long v = static_cast<long long>(rank) * NC + w;
+    a = v * kc / nw;
+    n = static_cast<int>((v + 1) * kc / nw - a);
+  };
 
   if (tid == 0) {
     prefetch_tensormap(&tmap_k);
@@ -204,32 +255,43 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
     fence_barrier_init();
   }
   __syncthreads();
-  // Launched as a programmatic dependent launch, this kernel's setup above
-  // overlaps the previous kernel; every global read and write comes after
-  // this wait.  Then the merge kernel may be scheduled.
+  // Launched as a programmatic dependent launch, the setup above overlaps
+  // the previous kernel; every global read and write comes after this wait.
   pdl_wait();
   if (tid == 0) pdl_launch_dependents();
+  // the whole cluster holds one unit, so this exit is uniform over it
+  if (!attn_unit_active(filter, filter_mode, u)) return;
 
-  // ------------------------------------------------------------ producer warp
   if (warp == NC) {
-    // page ids of the workers' ranges, once, so that issuing never waits on a load
-#pragma unroll 1
-    for (int w = 0; w < NC; ++w) {
-      const long long v = static_cast<long long>(blockIdx.x) * NC + w;
-      const long long a = v * W / n_workers, n = (v + 1) * W / n_workers - a;
-      for (int j = lane; j < n && j < kAttnIds; j += 32) s_ids[w][j] = __ldg(sel_phys + (a + j) / CPP);
+    // ---------------------------------------------------------- producer warp
+    // page ids of the workers' ranges, once (all loads in flight together),
+    // so that issuing never waits on a load
+    {
+      int idv[NC][kIdRounds];
+#pragma unroll
+      for (int w = 0; w < NC; ++w) {
+        long long a;
+        int n;
+        worker_range(w, a, n);
+#pragma unroll
+        for (int r = 0; r < kIdRounds; ++r) {
+          const int j = lane + 32 * r;
+          idv[w][r] = j < n ? __ldg(sel_phys + u * k + (a + j) / CPP) : -1;
+        }
+      }
+#pragma unroll
+      for (int w = 0; w < NC; ++w)
+#pragma unroll
+        for (int r = 0; r < kIdRounds; ++r) s_ids[w][lane + 32 * r] = idv[w][r];
     }
     __syncwarp();
     // lane w (< NC) feeds consumer warp w: the worker's chunks go to its R
-    // stages in turn.  The lane walks them incrementally: unit u, chunk
-    // position pos in the unit, KV head g = u % H.
+    // stages in turn
     const bool feeder = lane < NC;
-    const long long v = static_cast<long long>(blockIdx.x) * NC + lane;
-    const long long a = v * W / n_workers;
-    const int n = feeder ? static_cast<int>((v + 1) * W / n_workers - a) : 0;
+    long long a = 0;
+    int n = 0;
+    if (feeder) worker_range(lane, a, n);
     int i = 0;
-    long long u = a / kc, pos = a % kc;
-    int g = static_cast<int>(u % H);
     bool abort = false;
     uint64_t t_prog = global_timer_ns();
 #pragma unroll 1
@@ -239,9 +301,9 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
       if (mine) {
         const int s = lane * R + i % R;
         if (i < R || mbar_test_wait(&empty[s], static_cast<uint32_t>((i / R - 1) & 1))) {
+          const long long pos = a + i;
           const int id = i < kAttnIds ? s_ids[lane][i] : __ldg(sel_phys + u * k + pos / CPP);
-          const bool act = attn_unit_active(filter, filter_mode, u);
-          const bool ok = act && id >= 0 && id < n_phys;
+          const bool ok = id >= 0 && id < n_phys;
           s_ok[s] = ok ? 1 : 0;
           if (ok) {
             uint8_t *dst = smem + s * Cfg::kStageBytes;
@@ -252,15 +314,10 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
             tma_load_3d(dst + 2 * HALF, &tmap_v, &full[s], 0, g, row);
             tma_load_3d(dst + 3 * HALF, &tmap_v, &full[s], 64, g, row);
           } else {
-            if (act) set_status(KVR_ST_BAD_INDEX);
+            set_status(KVR_ST_BAD_INDEX);
             mbar_arrive(&full[s]);
           }
           ++i;
-          if (++pos == kc) {
-            pos = 0;
-            ++u;
-            g = g + 1 == H ? 0 : g + 1;
-          }
           t_prog = global_timer_ns();
         } else if (global_timer_ns() - t_prog > kWaitNs) {
           set_status(KVR_ST_WAIT_TIMEOUT);
@@ -274,155 +331,110 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
     if (feeder && abort)
       for (int j = max(0, i - R); j < i; ++j)
         mbar_wait(&full[lane * R + j % R], static_cast<uint32_t>((j / R) & 1));
-    return;
-  }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- consumer warps
+    const int cw = warp;
+    const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group and column pair
+    const int Hq = H * G;
+    long long a;
+    int n;
+    worker_range(cw, a, n);
 
-  // ------------------------------------------------------------ consumer warps
-  const int cw = warp;
-  const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group and column pair
-  const int Hq = H * G;
-  const long long v = static_cast<long long>(blockIdx.x) * NC + cw;  // this worker
-  const long long a = v * W / n_workers;
-  const int n = static_cast<int>((v + 1) * W / n_workers - a);
-
-  uint32_t qa[8][2];            // q of head gq as A fragments (k-step kk: channels 16kk + 2tq, +8)
-  float m_run, l_run;           // per head gq; l_run is this lane's partial
-  float o[8][4];                // O^T[16 mb + gq (+8)][2 tq (+1)]
-  long long u = a / kc, pos = a % kc;
-
-  // Close the segment of unit `uu`: a partial for a split unit, the
-  // normalised output for a unit that lies in this range alone.
-  auto flush = [&](long long uu) {
-    if (!attn_unit_active(filter, filter_mode, uu)) return;  // uniform over the warp
-    float l = l_run;
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    const int c_first = attn_cta_of(uu * kc, W, n_workers);
-    const int n_segs = attn_cta_of((uu + 1) * kc - 1, W, n_workers) - c_first + 1;
-    if (n_segs == 1) {
-      const int b = static_cast<int>(uu / H), g = static_cast<int>(uu % H);
-      float *orow = out + (static_cast<size_t>(b) * Hq + g * G) * kD;
-      const float la = __shfl_sync(0xffffffffu, l, 8 * tq);      // head 2tq
-      const float lb = __shfl_sync(0xffffffffu, l, 8 * tq + 4);  // head 2tq + 1
-      if (tq == 0 && gq < G && l <= 0.f) set_status(KVR_ST_NO_TOKENS);
-#pragma unroll
-      for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int head = 2 * tq + (e & 1), ch = 16 * mb + gq + 8 * (e >> 1);
-          const float lh = (e & 1) ? lb : la;
-          if (head < G) orow[head * kD + ch] = lh > 0.f ? o[mb][e] / lh : 0.f;
-        }
-    } else {
-      const size_t slot = static_cast<size_t>(v) + static_cast<size_t>(uu);
-      float *po = part_o + slot * G * kD;
-      if (tq == 0 && gq < G) part_ml[slot * G + gq] = make_float2(m_run, l);
-#pragma unroll
-      for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int head = 2 * tq + (e & 1), ch = 16 * mb + gq + 8 * (e >> 1);
-          if (head < G) po[head * kD + ch] = o[mb][e];
-        }
-    }
-  };
-  auto start = [&](long long uu) {  // new segment: zero state, q of the unit
-    m_run = -INFINITY;
-    l_run = 0.f;
+    uint32_t qb[8][2];  // q of head gq as B fragments (k-step kk: channels 16kk + 2tq, +8)
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};  // heads 2tq, 2tq + 1
+    float o[8][4];  // O^T[16 mb + gq (+8)][2 tq (+1)]
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
-    const int b = static_cast<int>(uu / H), g = static_cast<int>(uu % H);
-    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-        q + (static_cast<size_t>(b) * Hq + g * G + min(gq, G - 1)) * kD);
-    const bool on = gq < G;
+    {
+      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+          q + (static_cast<size_t>(b) * Hq + g * G + min(gq, G - 1)) * kD);
+      const bool on = gq < G;
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      qa[kk][0] = on ? __ldg(qrow + 8 * kk + tq) : 0u;
-      qa[kk][1] = on ? __ldg(qrow + 8 * kk + 4 + tq) : 0u;
-    }
-  };
-
-  start(u);
-#pragma unroll 1
-  for (int i = 0; i < n; ++i) {
-    if (i > 0 && pos == 0) {  // the range enters the next unit
-      flush(u - 1);
-      start(u);
-    }
-    const int s = cw * R + i % R;  // this warp's stages in turn
-    bool have = false;
-    if (__shfl_sync(0xffffffffu, s_abort, 0) == 0) {  // warp-uniform
-      const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((i / R) & 1));
-      if (__all_sync(0xffffffffu, ok)) {
-        have = s_ok[s] != 0;
-      } else if (lane == 0) {
-        s_abort = 1;
+      for (int kk = 0; kk < 8; ++kk) {
+        qb[kk][0] = on ? __ldg(qrow + 8 * kk + tq) : 0u;
+        qb[kk][1] = on ? __ldg(qrow + 8 * kk + 4 + tq) : 0u;
       }
     }
-    if (have) attn_chunk<G, P>(ring + s * Cfg::kStageBytes, qa, scale_log2, m_run, l_run, o, lane);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    if (++pos == kc) {
-      pos = 0;
-      ++u;
-    }
-  }
-  if (n > 0) flush(pos == 0 ? u - 1 : u);
-}
-
-// Merge of the split units, launched right after k_sparse_decode on the same
-// stream as a programmatic dependent launch (its CTAs may be scheduled while
-// k_sparse_decode runs; pdl_wait holds them until it has completed and its
-// partials are visible).  One CTA per (unit, query head of the group), one
-// thread per channel: the thread folds the unit's segments in segment order,
-// kMG at a time with all of their loads in flight, rescaling online.
-constexpr int kMG = 16;
-
-template <int G>
-__global__ void __launch_bounds__(kD)
-    k_attn_merge(const float *__restrict__ part_o, const float2 *__restrict__ part_ml, int H,
-                 long long kc, long long W, int n_workers, const uint8_t *__restrict__ filter,
-                 int filter_mode, float *__restrict__ out) {
-  // every CTA waits, so this kernel never completes before k_sparse_decode
-  // (later work on the stream may rewrite what k_sparse_decode reads)
-  pdl_wait();
-  const long long u = blockIdx.x / G;
-  const int h = blockIdx.x % G, ch = threadIdx.x;
-  const int c_first = attn_cta_of(u * kc, W, n_workers);
-  const int n_segs = attn_cta_of((u + 1) * kc - 1, W, n_workers) - c_first + 1;
-  if (n_segs == 1 || !attn_unit_active(filter, filter_mode, u)) return;  // written by the main kernel
-  const size_t slot0 = static_cast<size_t>(c_first) + static_cast<size_t>(u);
-  float M = -INFINITY, L = 0.f, A = 0.f;
 #pragma unroll 1
-  for (int j0 = 0; j0 < n_segs; j0 += kMG) {
-    float2 ml[kMG];
-    float ov[kMG];
-#pragma unroll
-    for (int j = 0; j < kMG; ++j) {
-      const size_t sl = slot0 + min(j0 + j, n_segs - 1);
-      ml[j] = __ldg(part_ml + sl * G + h);
-      ov[j] = __ldg(part_o + (sl * G + h) * kD + ch);
+    for (int i = 0; i < n; ++i) {
+      const int s = cw * R + i % R;  // this warp's stages in turn
+      bool have = false;
+      if (__shfl_sync(0xffffffffu, s_abort, 0) == 0) {  // warp-uniform
+        const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((i / R) & 1));
+        if (__all_sync(0xffffffffu, ok)) {
+          have = s_ok[s] != 0;
+        } else if (lane == 0) {
+          s_abort = 1;
+        }
+      }
+      if (have) attn_chunk<G, P>(ring + s * Cfg::kStageBytes, qb, scale_log2, m_run, l_run, o, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
-    // no early exits below: every load above is consumed in straight-line
-    // code, so the compiler keeps them all in flight together
-    float bm = M;
+    // ---- this worker's partial, pushed to the CTAs that merge it: channel
+    // c goes to CTA c / per, (m, l) to every CTA
+    const int j = rank * NC + cw;  // worker index in the cluster
+    float l0 = l_run[0], l1 = l_run[1];
 #pragma unroll
-    for (int j = 0; j < kMG; ++j) bm = fmaxf(bm, j0 + j < n_segs ? ml[j].x : -INFINITY);
-    const float rs = M == -INFINITY ? 0.f : exp2f(M - bm);
-    L *= rs;
-    A *= rs;
-#pragma unroll
-    for (int j = 0; j < kMG; ++j) {
-      const bool on = j0 + j < n_segs && ml[j].x != -INFINITY;
-      const float sc = on ? exp2f(ml[j].x - bm) : 0.f;
-      L = fmaf(sc, ml[j].y, L);
-      A = fmaf(sc, ov[j], A);
+    for (int m = 4; m <= 16; m <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, m);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, m);
     }
-    M = bm;
+    if (G <= 4) {  // add the residual columns h + 4 into columns h
+#pragma unroll
+      for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mb][e] += __shfl_xor_sync(0xffffffffu, o[mb][e], 2);
+    }
+    const uint32_t ml0 = smem_addr(s_mlr), rc0 = smem_addr(s_recv);
+    if (gq == 0) {
+#pragma unroll 1
+      for (int qr = 0; qr < Q; ++qr) {
+        if (2 * tq < G)
+          st_cluster_f32x2(cluster_map(ml0 + (j * G + 2 * tq) * 8, qr), make_float2(m_run[0], l0));
+        if (2 * tq + 1 < G)
+          st_cluster_f32x2(cluster_map(ml0 + (j * G + 2 * tq + 1) * 8, qr), make_float2(m_run[1], l1));
+      }
+    }
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      const int owner = (16 * mb) / per;  // per >= 16: a 16-channel block has one owner
+      const uint32_t base = cluster_map(rc0, owner);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int h = 2 * tq + (e & 1), cl = 16 * mb + gq + 8 * (e >> 1) - owner * per;
+        if (h < G) st_cluster_f32(base + ((j * G + h) * per + cl) * 4, o[mb][e]);
+      }
+    }
+    __syncwarp();
   }
-  const int b = static_cast<int>(u / H), g = static_cast<int>(u % H);
-  if (L <= 0.f && ch == 0) set_status(KVR_ST_NO_TOKENS);
-  out[((static_cast<size_t>(b) * H + g) * G + h) * kD + ch] = L > 0.f ? A / L : 0.f;
+
+  // ------------------------------------------------------------ merge
+  // every partial of the cluster has been pushed and is visible; after this
+  // barrier no CTA touches another's shared memory, so each may exit freely
+  cluster_sync();
+  {
+    const int Hq = H * G;
+    float *orow = out + (static_cast<size_t>(b) * Hq + g * G) * kD + rank * per;
+#pragma unroll 1
+    for (int e = tid; e < G * per; e += kAttnThreads) {
+      const int h = e / per, cl = e - h * per;
+      float M = -INFINITY;
+#pragma unroll 4
+      for (int j = 0; j < nw; ++j) M = fmaxf(M, s_mlr[j * G + h].x);
+      float L = 0.f, A = 0.f;
+#pragma unroll 4
+      for (int j = 0; j < nw; ++j) {
+        const float2 ml = s_mlr[j * G + h];
+        const float sc = ml.x != -INFINITY ? exp2f(ml.x - M) : 0.f;
+        L = fmaf(sc, ml.y, L);
+        A = fmaf(sc, s_recv[(j * G + h) * per + cl], A);
+      }
+      if (L <= 0.f && rank == 0 && cl == 0) set_status(KVR_ST_NO_TOKENS);
+      orow[h * kD + cl] = L > 0.f ? A / L : 0.f;
+    }
+  }
 }
 
 }  // namespace kvr

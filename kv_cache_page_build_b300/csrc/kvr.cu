@@ -89,9 +89,7 @@ struct SelectWs {
   uint32_t *count;
 };
 struct AttnWs {
-  float *part_o;
-  float2 *part_ml;
-  uint32_t *count;
+  uint32_t *reserved;  // the attention keeps its split partials on chip
 };
 
 size_t select_ws_bytes(const kvr_dims *d) {
@@ -99,19 +97,10 @@ size_t select_ws_bytes(const kvr_dims *d) {
   return align_up(units * d->n_pages * sizeof(float)) + align_up(units * sizeof(uint32_t));
 }
 
-// Partial slots of the attention merge: worker v's segment of unit u goes to
-// slot v + u, so kAttnMaxWorkers + units slots cover every grid size.
-size_t attn_slots(const kvr_dims *d) {
-  return static_cast<size_t>(kAttnMaxWorkers) + static_cast<size_t>(d->batch) * d->n_kv_heads;
-}
-
 size_t attn_ws_bytes(const kvr_dims *d, int top_k) {
   (void)top_k;
   const size_t units = static_cast<size_t>(d->batch) * d->n_kv_heads;
-  const size_t G = d->n_q_heads / d->n_kv_heads;
-  const size_t slots = attn_slots(d);
-  return align_up(slots * G * kD * sizeof(float)) + align_up(slots * G * sizeof(float2)) +
-         align_up(units * sizeof(uint32_t));
+  return align_up(units * sizeof(uint32_t));
 }
 
 SelectWs carve_select(const kvr_dims *d, uint8_t *p) {
@@ -123,15 +112,10 @@ SelectWs carve_select(const kvr_dims *d, uint8_t *p) {
 }
 
 AttnWs carve_attn(const kvr_dims *d, int top_k, uint8_t *p) {
+  (void)d;
   (void)top_k;
-  const size_t G = d->n_q_heads / d->n_kv_heads;
-  const size_t slots = attn_slots(d);
   AttnWs w;
-  w.part_o = reinterpret_cast<float *>(p);
-  p += align_up(slots * G * kD * sizeof(float));
-  w.part_ml = reinterpret_cast<float2 *>(p);
-  p += align_up(slots * G * sizeof(float2));
-  w.count = reinterpret_cast<uint32_t *>(p);
+  w.reserved = reinterpret_cast<uint32_t *>(p);
   return w;
 }
 
@@ -298,16 +282,43 @@ int sm_count(int *out) {
   return KVR_OK;
 }
 
-// Grid of the attention kernel: `per_sm` resident CTAs per SM, at least
-// kAttnMinChunksPerWorker chunks per consumer warp, at most kAttnMaxCtas CTAs.
-int attn_grid(long long W, int per_sm, int *n_ctas) {
-  int sms = 0;
-  if (int rc = sm_count(&sms)) return rc;
-  const long long per_cta = static_cast<long long>(kAttnMinChunksPerWorker) * kAttnNC;
-  long long n = std::min<long long>(static_cast<long long>(sms) * per_sm, (W + per_cta - 1) / per_cta);
-  n = std::max<long long>(1, std::min<long long>(n, kAttnMaxCtas));
-  if ((W + n - 1) / n >= (1LL << 31)) return KVR_ERR_UNSUPPORTED_SHAPE;
-  *n_ctas = static_cast<int>(n);
+// CTAs per cluster of the attention kernel: the largest Q in {8, 4, 2} whose
+// clusters for all units are resident at once (and that leaves every worker
+// at least one chunk), else 1.  Occupancy per Q is cached per device.
+template <int G, int P>
+int attn_cluster_size(const void *kern, size_t smem, long long units, long long kc, int *q_out) {
+  static int cap[kMaxDevices][4] = {};  // resident clusters for Q = 1, 2, 4, 8 (0: not yet asked)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return KVR_ERR_UNSUPPORTED_SHAPE;
+  int q = 1;
+  for (int lq = 3; lq >= 1; --lq) {
+    const int cand = 1 << lq;
+    if (static_cast<long long>(cand) * kAttnNC > kc) continue;
+    if (cap[dev][lq] == 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(cand));
+      cfg.blockDim = dim3(kAttnThreads);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(cand);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return cuda_fail(e, "cluster occupancy");
+      cap[dev][lq] = n > 0 ? n : -1;
+    }
+    if (cap[dev][lq] > 0 && units <= cap[dev][lq]) {
+      q = cand;
+      break;
+    }
+  }
+  *q_out = q;
   return KVR_OK;
 }
 
@@ -316,51 +327,39 @@ int launch_attn_gp(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &
                    const uint16_t *q, const int32_t *sel_phys, int k, int n_phys, float scale,
                    const uint8_t *filter, int filter_mode, AttnWs w, float *out, cudaStream_t st,
                    bool pdl_ok) {
+  (void)w;
   using Cfg = AttnCfg<G, P>;
   const long long units = static_cast<long long>(d->batch) * d->n_kv_heads;
   const long long kc = static_cast<long long>(k) * Cfg::CPP;
-  const long long W = units * kc;
-  int n_ctas = 0;
-  if (int rc = attn_grid(W, kAttnCPS, &n_ctas)) return rc;
   const size_t smem = Cfg::kSmem;
   auto kern = k_sparse_decode<G, P>;
   static int max_set[kMaxDevices] = {};
   if (int rc = ensure_smem(reinterpret_cast<const void *>(kern), smem, max_set)) return rc;
+  int Q = 1;
+  if (int rc = attn_cluster_size<G, P>(reinterpret_cast<const void *>(kern), smem, units, kc, &Q))
+    return rc;
+  if (units * Q > 0x7fffffffLL) return KVR_ERR_UNSUPPORTED_SHAPE;
   const float scale_log2 = scale * 1.4426950408889634f;
-  // a programmatic dependent launch (unless the stream's last operation is
-  // an event wait): the setup overlaps the kernel before it on the stream
-  cudaLaunchAttribute pdl[1];
-  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl[0].val.programmaticStreamSerializationAllowed = 1;
-  {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(n_ctas));
-    cfg.blockDim = dim3(kAttnThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cfg.attrs = pdl;
-    cfg.numAttrs = pdl_ok ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tk, tv, q, sel_phys, d->n_kv_heads, k,
-                                             n_phys, W, scale_log2, filter, filter_mode, w.part_o,
-                                             w.part_ml, out);
-    if (e != cudaSuccess) return cuda_fail(e, "k_sparse_decode");
-  }
-  // merge of the split units: a programmatic dependent launch, so its launch
-  // overlaps the streaming kernel's tail
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(units * G));
-  cfg.blockDim = dim3(kD);
-  cfg.dynamicSmemBytes = 0;
+  cfg.gridDim = dim3(static_cast<unsigned>(units * Q));
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  // clusters of Q CTAs, one per unit; a programmatic dependent launch (unless
+  // the stream's last operation is an event wait): the setup overlaps the
+  // kernel before it on the stream
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(Q);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_attn_merge<G>, static_cast<const float *>(w.part_o),
-                                           static_cast<const float2 *>(w.part_ml), d->n_kv_heads, kc,
-                                           W, n_ctas * kAttnNC, filter, filter_mode, out);
-  if (e != cudaSuccess) return cuda_fail(e, "k_attn_merge");
+  cfg.numAttrs = pdl_ok ? 2 : 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tk, tv, q, sel_phys, d->n_kv_heads, k,
+                                           n_phys, Q, scale_log2, filter, filter_mode, out);
+  if (e != cudaSuccess) return cuda_fail(e, "k_sparse_decode");
   return KVR_OK;
 }
 

@@ -58,7 +58,7 @@ def test_workspace_size_rules():
     sel = kvr.kvr_workspace_size(d, 64, kvr.KVR_OP_SELECT)
     att = kvr.kvr_workspace_size(d, 64, kvr.KVR_OP_ATTN)
     assert sel >= 8 * 8 * 1024 * 4 + 8 * 8 * 4
-    assert att >= 8 * 8 * (64 // 4) * 4 * 130 * 4      # partial (m, l, o) per split and head
+    assert att > 0                                      # a small reserved area: the split partials stay on chip
     assert kvr.kvr_workspace_size(d, 64, kvr.KVR_OP_STEP) == sel + att
     assert kvr.kvr_workspace_size(d, 2000, kvr.KVR_OP_SELECT) == 0   # k > N
     assert kvr.kvr_workspace_size(d, 64, 99) == 0
