@@ -70,7 +70,7 @@ struct AttnCfg {
   static constexpr int R = kAttnWarpRing / kStageBytes;  // stages per consumer warp
   static constexpr int S = kAttnNC * R;            // ring depth
   static constexpr int kSmem = S * kStageBytes + 1024;   // + 1 KiB to align the ring
-  static constexpr int kStatic = kAttnNC * G * kD * 4 + kAttnMaxQ * kAttnNC * G * 8 +
+  static constexpr int kStatic = kAttnNC * G * kD * 4 + kAttnNC * G * 8 +
                                  kAttnNC * kAttnIds * 4 + S * 20 + 64;
   static_assert(kAttnCPS * (kSmem + kStatic + 1024) <= kSmemPerSM, "CTAs per SM must fit");
   static_assert(CPP * C == P && NB * 8 == C && KP * 16 == C && R >= 2, "chunk tiling");
@@ -223,10 +223,9 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
   __shared__ __align__(8) uint64_t full[S], empty[S];
   __shared__ int s_ok[S];
   __shared__ int s_ids[NC][kAttnIds];  // page ids of the first kAttnIds chunks of each worker
-  // partials of the cluster's workers for this CTA's channel slice:
-  // [worker][head][channel of the slice] and (m, l) per worker and head
-  __shared__ __align__(16) float s_recv[NC * G * kD];
-  __shared__ __align__(8) float2 s_mlr[kAttnMaxQ * NC * G];
+  // this CTA's workers' partials: O per head and channel, (m, l) per head
+  __shared__ __align__(16) float s_po[NC][G][kD];
+  __shared__ __align__(8) float2 s_ml[NC][G];
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -372,9 +371,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    // ---- this worker's partial, pushed to the CTAs that merge it: channel
-    // c goes to CTA c / per, (m, l) to every CTA
-    const int j = rank * NC + cw;  // worker index in the cluster
+    // ---- this worker's partial, left in this CTA's shared memory
     float l0 = l_run[0], l1 = l_run[1];
 #pragma unroll
     for (int m = 4; m <= 16; m <<= 1) {
@@ -387,54 +384,68 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[mb][e] += __shfl_xor_sync(0xffffffffu, o[mb][e], 2);
     }
-    const uint32_t ml0 = smem_addr(s_mlr), rc0 = smem_addr(s_recv);
     if (gq == 0) {
-#pragma unroll 1
-      for (int qr = 0; qr < Q; ++qr) {
-        if (2 * tq < G)
-          st_cluster_f32x2(cluster_map(ml0 + (j * G + 2 * tq) * 8, qr), make_float2(m_run[0], l0));
-        if (2 * tq + 1 < G)
-          st_cluster_f32x2(cluster_map(ml0 + (j * G + 2 * tq + 1) * 8, qr), make_float2(m_run[1], l1));
-      }
+      if (2 * tq < G) s_ml[cw][2 * tq] = make_float2(m_run[0], l0);
+      if (2 * tq + 1 < G) s_ml[cw][2 * tq + 1] = make_float2(m_run[1], l1);
     }
 #pragma unroll
-    for (int mb = 0; mb < 8; ++mb) {
-      const int owner = (16 * mb) / per;  // per >= 16: a 16-channel block has one owner
-      const uint32_t base = cluster_map(rc0, owner);
+    for (int mb = 0; mb < 8; ++mb)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int h = 2 * tq + (e & 1), cl = 16 * mb + gq + 8 * (e >> 1) - owner * per;
-        if (h < G) st_cluster_f32(base + ((j * G + h) * per + cl) * 4, o[mb][e]);
+        const int h = 2 * tq + (e & 1);
+        if (h < G) s_po[cw][h][16 * mb + gq + 8 * (e >> 1)] = o[mb][e];
       }
-    }
     __syncwarp();
   }
 
   // ------------------------------------------------------------ merge
-  // every partial of the cluster has been pushed and is visible; after this
-  // barrier no CTA touches another's shared memory, so each may exit freely
+  // every partial of the cluster is written and visible
   cluster_sync();
   {
+    // CTA `rank` merges channels [rank per, (rank + 1) per) of the G heads:
+    // one thread per 4 channels of a head pulls them from every worker of
+    // the cluster (16-byte loads, all in flight together)
+    const int n4 = per / 4;
     const int Hq = H * G;
-    float *orow = out + (static_cast<size_t>(b) * Hq + g * G) * kD + rank * per;
+    const uint32_t po0 = smem_addr(&s_po[0][0][0]), ml0 = smem_addr(&s_ml[0][0]);
 #pragma unroll 1
-    for (int e = tid; e < G * per; e += kAttnThreads) {
-      const int h = e / per, cl = e - h * per;
-      float M = -INFINITY;
-#pragma unroll 4
-      for (int j = 0; j < nw; ++j) M = fmaxf(M, s_mlr[j * G + h].x);
-      float L = 0.f, A = 0.f;
-#pragma unroll 4
-      for (int j = 0; j < nw; ++j) {
-        const float2 ml = s_mlr[j * G + h];
-        const float sc = ml.x != -INFINITY ? exp2f(ml.x - M) : 0.f;
-        L = fmaf(sc, ml.y, L);
-        A = fmaf(sc, s_recv[(j * G + h) * per + cl], A);
+    for (int e = tid; e < G * n4; e += kAttnThreads) {
+      const int h = e / n4, c = rank * per + 4 * (e - h * n4);
+      float2 ml[kAttnMaxQ * NC];
+      float4 ov[kAttnMaxQ * NC];
+#pragma unroll
+      for (int j = 0; j < kAttnMaxQ * NC; ++j) {
+        ml[j] = make_float2(-INFINITY, 0.f);
+        ov[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < nw) {
+          const int qr = j / NC, w = j % NC;
+          ml[j] = ld_cluster_f32x2(cluster_map(ml0 + (w * G + h) * 8, qr));
+          ov[j] = ld_cluster_f32x4(cluster_map(po0 + ((w * G + h) * kD + c) * 4, qr));
+        }
       }
-      if (L <= 0.f && rank == 0 && cl == 0) set_status(KVR_ST_NO_TOKENS);
-      orow[h * kD + cl] = L > 0.f ? A / L : 0.f;
+      float M = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kAttnMaxQ * NC; ++j) M = fmaxf(M, ml[j].x);
+      float L = 0.f;
+      float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < kAttnMaxQ * NC; ++j) {
+        const float sc = ml[j].x != -INFINITY ? exp2f(ml[j].x - M) : 0.f;
+        L = fmaf(sc, ml[j].y, L);
+        A.x = fmaf(sc, ov[j].x, A.x);
+        A.y = fmaf(sc, ov[j].y, A.y);
+        A.z = fmaf(sc, ov[j].z, A.z);
+        A.w = fmaf(sc, ov[j].w, A.w);
+      }
+      if (L <= 0.f && c == 0) set_status(KVR_ST_NO_TOKENS);
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      *reinterpret_cast<float4 *>(out + (static_cast<size_t>(b) * Hq + g * G + h) * kD + c) =
+          make_float4(A.x * inv, A.y * inv, A.z * inv, A.w * inv);
     }
   }
+  // every read of this CTA's partials is done before it exits
+  cluster_arrive();
+  cluster_wait();
 }
 
 }  // namespace kvr
