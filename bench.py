@@ -238,16 +238,18 @@ def run_gpu(args, world, rank, local):
     ws = torch.zeros(ws_n, dtype=torch.uint8, device=dev)
     wa = torch.zeros(wa_n, dtype=torch.uint8, device=dev)
 
-    def step(i, ev_mid=None, ev_end=None):
+    def select_call(i):
+        kvr.kvr_speculative_select(d, st, qs[i % TRACE_LEN], summs[i % COPIES], page_table, k, wl_trace.tau,
+                                   corrected, None, sel_used, sel_used_phys, ws, ws_n)
+
+    def attn_call(i):
         c = i % COPIES
-        kvr.kvr_speculative_select(d, st, qs[i % TRACE_LEN], summs[c], page_table, k, wl_trace.tau, corrected,
-                                   None, sel_used, sel_used_phys, ws, ws_n)
-        if ev_mid is not None:
-            ev_mid.record()
         kvr.kvr_sparse_decode_attn(d, qs[i % TRACE_LEN], k_pools[c], v_pools[c], sel_used_phys, k, 0.0, out,
                                    wa, wa_n)
-        if ev_end is not None:
-            ev_end.record()
+
+    def step(i):
+        select_call(i)
+        attn_call(i)
 
     # warm-up: eager steps (the first one is step 0 of the trace)
     for i in range(max(args.warmup, 3)):
@@ -262,15 +264,16 @@ def run_gpu(args, world, rank, local):
     with torch.cuda.graph(graph):
         for i in range(L):
             step(i)
-    # a second graph with events around each call, for the per-kernel split
-    # (event nodes between the calls break the kernels' programmatic
-    # dependent launches, so its per-call times are an upper bound)
-    ev_mid = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(L)]
-    ev_end = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(L)]
-    graph_ev = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_ev):
+    # per-kernel times: graphs of L back-to-back calls of each kind (selection
+    # alone, attention alone on the rotating caches), timed after the run
+    graph_sel = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_sel):
         for i in range(L):
-            step(i, ev_mid[i], ev_end[i])
+            select_call(i)
+    graph_attn = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_attn):
+        for i in range(L):
+            attn_call(i)
     rem = args.steps % L
     graph_rem = None
     if rem:
@@ -303,14 +306,20 @@ def run_gpu(args, world, rank, local):
     status = kvr.kvr_get_status()
     value, t_max = aggregate(args.steps, elapsed, world)
 
-    # per-launch device time of the two calls, from a replay of the graph with events
-    for _ in range(2):
-        graph_ev.replay()
-    torch.cuda.synchronize()
-    attn_ms = [ev_mid[i].elapsed_time(ev_end[i]) for i in range(L)]
-    sel_ms = [ev_end[i - 1].elapsed_time(ev_mid[i]) for i in range(1, L)]
-    attn_avg = sum(attn_ms) / len(attn_ms) / 1e3
-    sel_avg = sum(sel_ms) / len(sel_ms) / 1e3 if sel_ms else None
+    # per-launch device time of the two calls, from replays of their graphs
+    def per_call(g, reps=4):
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3 / (reps * L)
+
+    attn_avg = per_call(graph_attn)
+    sel_avg = per_call(graph_sel)
 
     hbm, peak_kind = peaks()
     attn_bytes = B * H * k * P * 2 * D * 2                 # selected K and V rows read per launch
@@ -360,8 +369,8 @@ def run_gpu(args, world, rank, local):
             "parallelism": f"{world} independent replica(s)" if world > 1 else "1 GPU",
             "l2": f"{COPIES} rotating cache copies: {(COPIES - 1) * (attn_bytes + summ_bytes) / 2**20:.0f} MiB "
                   f"touched between reuses of one copy (L2 126 MB)",
-            "graph": f"steps replayed from a CUDA graph of {L} steps (per-kernel times from a second graph "
-                     f"with events between the calls)",
+            "graph": f"steps replayed from a CUDA graph of {L} steps (per-kernel times from graphs of {L} "
+                     f"back-to-back calls of each kind)",
         },
         "selected_kv_gbs": round(achieved, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",

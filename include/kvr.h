@@ -42,9 +42,9 @@
  *     nothing.  Conditions found on the device (an out-of-range page id, a
  *     wait that timed out) set bits of the status word instead.
  *   - A workspace (`ws`, `ws_bytes`) must be at least kvr_workspace_size()
- *     bytes and zero-filled before its first use; every call leaves it
- *     zero-filled again.  Calls that share a workspace must not overlap on
- *     the GPU.
+ *     bytes.  Its contents need no initialisation: a call writes every
+ *     scratch value before reading it (a reserved word per (b, g) is left
+ *     as found).  Calls that share a workspace must not overlap on the GPU.
  */
 #ifndef KVR_H
 #define KVR_H
@@ -261,20 +261,19 @@ uint64_t kvr_kv_bytes(int64_t n_layers, int64_t n_kv_heads, int64_t head_dim,
  * buffers it was handed, a serving loop that forbids allocation after
  * warm-up to keep latency flat, or a foreign-language caller with no access
  * to the process's device allocator.  It computes exactly what
- * kvr_select_pages computes (same kernel, same results), but its scratch
- * (the fp32 score rows and ticket counters) lives in a fixed array of
+ * kvr_select_pages computes (same kernels, same results), but its scratch
+ * (the fp32 score rows) lives in a fixed array of
  * KVR_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
  * the library keeps until the process exits.  The caller still passes all
  * inputs and outputs (q, summ, page_table, sel, sel_phys, scores_opt as in
  * kvr_select_pages).
- *   - Limit: B * H * N * 4 bytes of scores plus the counters must fit in
+ *   - Limit: B * H * N * 4 bytes of scores plus 4 bytes per (b, g) must fit in
  *     KVR_NOALLOC_SCRATCH_BYTES (about one million page scores); larger
  *     problems return KVR_ERR_SCRATCH_LIMIT before anything is enqueued.
  *   - The first call on each device looks up the array's device address
  *     (with that device current) and caches it; make that first call before
  *     any stream capture.
- *   - Every call clears the counters it needs on `stream`, then launches.
- *     All calls share the one array: calls that overlap on the GPU (on
+ *   - All calls share the one array: calls that overlap on the GPU (on
  *     different streams, or from several threads) race and must be
  *     serialised by the caller.
  * It never calls cudaMalloc, cudaFree or any allocating routine. */

@@ -85,8 +85,8 @@ int ensure_smem(const void *kern, size_t bytes, int *max_set) {
 // ---------------------------------------------------------------- workspace
 
 struct SelectWs {
-  float *scores;
-  uint32_t *count;
+  float *scores;      // [B][H][N] fp32 page scores between the two selection kernels
+  uint32_t *count;    // one word per unit, kept zero (reserved in the layout; unused)
 };
 struct AttnWs {
   uint32_t *reserved;  // the attention keeps its split partials on chip
@@ -742,8 +742,8 @@ uint64_t kvr_kv_bytes(int64_t n_layers, int64_t n_kv_heads, int64_t head_dim, in
 
 // ---------------------------------------------------------------- allocation-free selection
 //
-// kvr_select_pages_noalloc: the selection kernel with its scratch (score rows
-// and ticket counters) in this fixed device array instead of a caller
+// kvr_select_pages_noalloc: the selection kernels with their scratch (the
+// score rows) in this fixed device array instead of a caller
 // workspace, for callers that may not allocate device memory.  Host code
 // must not pass the array's name to a kernel (on the host it only stands in
 // for the symbol); the device address is looked up once per device below.
@@ -791,10 +791,6 @@ extern "C" int kvr_select_pages_noalloc(const kvr_dims *dims, const uint16_t *q,
   if ((rc = noalloc_scratch(&scratch))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const SelectWs w = carve_select(dims, static_cast<uint8_t *>(scratch));
-  // the ticket counters must start at zero (a previous call may have been cut short)
-  const size_t units = static_cast<size_t>(dims->batch) * dims->n_kv_heads;
-  const cudaError_t e = cudaMemsetAsync(w.count, 0, units * sizeof(uint32_t), st);
-  if (e != cudaSuccess) return cuda_fail(e, "clear scratch counters");
   return launch_select(dims, q, summ, page_table, top_k, w, sel, sel_phys, scores_opt, no_spec(),
                        st);
 }

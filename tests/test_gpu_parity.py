@@ -178,25 +178,22 @@ def test_explicit_scale():
     gh.assert_attn_close(gh.attention(dc, sel_phys, scale=0.05).cpu().numpy(), ref)
 
 
-def test_repeatable_and_workspace_left_zeroed():
-    """Five runs on poisoned outputs give bitwise-identical results (so the
-    ticket counters were reset), and the counters end at zero."""
+def test_repeatable_with_junk_filled_workspace():
+    """Five runs on poisoned outputs give bitwise-identical results, with the
+    workspaces filled with junk bytes and with zeros: no call depends on a
+    workspace's earlier contents."""
     case, dc, _ = accepted_case(2)
-    ws_s = gh.workspace(dc.dims, case.wl.top_k, kvr.KVR_OP_SELECT)
-    ws_a = gh.workspace(dc.dims, case.wl.top_k, kvr.KVR_OP_ATTN)
     first = None
-    for _ in range(5):
+    for fill in (0xA5, 0x00, 0xFF, 0x5A, 0xA5):
+        ws_s = gh.workspace(dc.dims, case.wl.top_k, kvr.KVR_OP_SELECT).fill_(fill)
+        ws_a = gh.workspace(dc.dims, case.wl.top_k, kvr.KVR_OP_ATTN).fill_(fill)
         sel, sel_phys, sc = gh.select(dc, ws=ws_s)
         out = gh.attention(dc, sel_phys, ws=ws_a)
         cur = (sel.cpu().numpy(), sc.cpu().numpy(), out.cpu().numpy())
         if first is None:
             first = cur
-        for a, b in zip(first, cur):
-            np.testing.assert_array_equal(a, b)
-    units = case.wl.batch * case.wl.n_kv_heads
-    tail = (units * 4 + 255) // 256 * 256          # the counters are the last region of each workspace
-    assert int(ws_s[-tail:].count_nonzero()) == 0
-    assert int(ws_a[-tail:].count_nonzero()) == 0
+        for x, y in zip(first, cur):
+            np.testing.assert_array_equal(x, y)
 
 
 def test_out_of_range_page_is_skipped_and_reported():
