@@ -15,9 +15,10 @@
 // zero, so each channel adds exactly one exact bf16 x bf16 product.  Per unit
 // this is a contraction [q- | q+] (G x 256) . [kmin ; kmax] (256 x pages):
 // it runs on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 out) with the
-// G heads on the 16-row side, then the G head scores of a page are summed by
-// a fixed xor butterfly.  Two pages with equal summaries go through identical
-// operations, so they get bitwise-equal scores.
+// pages on the 16-row side and the G heads as columns, then the G head scores
+// of a page are summed in a fixed order (in-lane pair, then an xor butterfly
+// over the column pairs).  Two pages with equal summaries go through
+// identical operations, so they get bitwise-equal scores.
 //
 // Two kernels.
 //   k_page_scores streams the summaries.  The rows of all (b, g) units form
@@ -26,7 +27,7 @@
 //   contiguous range of it.  Its producer lane loads the range 32 pages
 //   (16 KiB: four 64-channel boxes, 128-byte swizzled) at a time, never
 //   across a unit boundary (a shorter stage takes 8-page boxes), into the
-//   worker's R private stages; the worker scores a stage with 64 MMAs fed by
+//   worker's R private stages; the worker scores a stage with 32 MMAs fed by
 //   ldmatrix.
 //   k_topk, one CTA per unit, launched right after as a programmatic
 //   dependent launch, reads the unit's N scores and selects.
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
   long long u = f / N;
   int pos = static_cast<int>(f % N);
   const int gq = lane >> 2, tq = lane & 3, mi = lane >> 3, mr = lane & 7;
-  // [q- | q+] of head gq as A fragments: k-step kk < 8 meets kmin channels
+  // [q- | q+] of head gq as B fragments: k-step kk < 8 meets kmin channels
   // 16kk.., kk >= 8 meets kmax channels 16(kk - 8)..; words hold bf16 pairs
   uint32_t qa[16][2];
   long long q_unit = -1;
@@ -211,37 +212,43 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
       }
     }
     if (have) {
+      // S^T[page][head] on the tensor cores: pages 16 mt + gq (+8) of the
+      // stage on the 16-row side, heads 2tq, 2tq + 1 as columns; even and
+      // odd k-steps in separate accumulators.  Rows past cnt hold stale
+      // shared memory; their results are never stored.
       const uint32_t sb = ring + s * kScStageBytes;
+      float c[2][4], d[2][4];
 #pragma unroll
-      for (int nb = 0; nb < kScPages / 8; ++nb) {
-        if (8 * nb >= cnt) break;  // rows not loaded for a short stage
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int kq = 0; kq < 8; ++kq) {  // 16-byte chunks 4kq .. 4kq+3 = k-steps 2kq, 2kq+1
-          uint32_t bf[4];
-          ldsm_x4(swz<HALF>(sb, 8 * nb + mr, 4 * kq + mi), bf);
-          mma_bf16_16816(c, qa[2 * kq][0], 0u, qa[2 * kq][1], 0u, bf[0], bf[1]);
-          mma_bf16_16816(c, qa[2 * kq + 1][0], 0u, qa[2 * kq + 1][1], 0u, bf[2], bf[3]);
-        }
-        // sum the 8 row groups (heads G.. are zero rows): pages 8nb + 2tq (+1)
+        for (int x = 0; x < 4; ++x) c[mt][x] = d[mt][x] = 0.f;
 #pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          float t = c[e2];
-          t += __shfl_xor_sync(0xffffffffu, t, 4);
-          t += __shfl_xor_sync(0xffffffffu, t, 8);
-          t += __shfl_xor_sync(0xffffffffu, t, 16);
-          c[e2] = t * (1.0f / G);
+      for (int kk = 0; kk < 16; ++kk)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          uint32_t a[4];
+          ldsm_x4(swz<HALF>(sb, 16 * mt + 8 * (mi & 1) + mr, 2 * kk + (mi >> 1)), a);
+          if (kk & 1)
+            mma_bf16_16816(d[mt], a[0], a[1], a[2], a[3], qa[kk][0], qa[kk][1]);
+          else
+            mma_bf16_16816(c[mt], a[0], a[1], a[2], a[3], qa[kk][0], qa[kk][1]);
         }
-        const int p = 8 * nb + 2 * tq;
-        if (gq == 0 && p < cnt) {
-          ws_scores[f + p] = c[0];
-          if (scores_out) scores_out[f + p] = c[0];
+      // sum over the heads in a fixed order: the lane's two heads, then the
+      // four column pairs (heads G.. are zero columns)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          float t = (c[mt][2 * r] + d[mt][2 * r]) + (c[mt][2 * r + 1] + d[mt][2 * r + 1]);
+          t += __shfl_xor_sync(0xffffffffu, t, 1);
+          t += __shfl_xor_sync(0xffffffffu, t, 2);
+          t *= (1.0f / G);
+          const int p = 16 * mt + gq + 8 * r;
+          if (tq == 0 && p < cnt) {
+            ws_scores[f + p] = t;
+            if (scores_out) scores_out[f + p] = t;
+          }
         }
-        if (gq == 0 && p + 1 < cnt) {
-          ws_scores[f + p + 1] = c[1];
-          if (scores_out) scores_out[f + p + 1] = c[1];
-        }
-      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
