@@ -13,11 +13,13 @@
 // together when they fit).  The unit's k CPP chunks of C = min(P, 32) tokens
 // are cut into Q NC equal contiguous ranges, one per consumer warp (a
 // "worker") of the cluster.  A worker keeps its split's running (m, l, O) in
-// registers and leaves it in its CTA's shared memory at the end; after a
-// cluster barrier, CTA r merges channels [r D/Q, (r+1) D/Q) of the G heads
-// from all Q NC partials, read through distributed shared memory, with a
-// log-sum-exp rescale, and writes them to `out`.  A second cluster barrier
-// keeps every CTA resident until its partials have been read.  Nothing of
+// registers; at the end it stages O in one of its own (now idle) ring stages
+// and pushes it, 16 bytes per store through distributed shared memory, to
+// the CTAs that merge it: CTA r merges channels [r D/Q, (r+1) D/Q) of the G
+// heads, and every CTA gets every worker's (m, l).  After one cluster
+// barrier each CTA merges its slice from its own shared memory with a
+// log-sum-exp rescale and writes it to `out`; no CTA reads another's shared
+// memory after the barrier, so each leaves as soon as it is done.  Nothing of
 // the split goes through global memory and no second kernel is needed.
 //
 // Inside a CTA (CPS per SM) the warps share the shared-memory ring:
@@ -70,7 +72,7 @@ struct AttnCfg {
   static constexpr int R = kAttnWarpRing / kStageBytes;  // stages per consumer warp
   static constexpr int S = kAttnNC * R;            // ring depth
   static constexpr int kSmem = S * kStageBytes + 1024;   // + 1 KiB to align the ring
-  static constexpr int kStatic = kAttnNC * G * kD * 4 + kAttnNC * G * 8 +
+  static constexpr int kStatic = kAttnNC * G * kD * 4 + kAttnMaxQ * kAttnNC * G * 8 +
                                  kAttnNC * kAttnIds * 4 + S * 20 + 64;
   static_assert(kAttnCPS * (kSmem + kStatic + 1024) <= kSmemPerSM, "CTAs per SM must fit");
   static_assert(CPP * C == P && NB * 8 == C && KP * 16 == C && R >= 2, "chunk tiling");
@@ -223,9 +225,10 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
   __shared__ __align__(8) uint64_t full[S], empty[S];
   __shared__ int s_ok[S];
   __shared__ int s_ids[NC][kAttnIds];  // page ids of the first kAttnIds chunks of each worker
-  // this CTA's workers' partials: O per head and channel, (m, l) per head
-  __shared__ __align__(16) float s_po[NC][G][kD];
-  __shared__ __align__(8) float2 s_ml[NC][G];
+  // partials of the cluster's workers for this CTA's channel slice:
+  // [worker][head][channel of the slice], and (m, l) per worker and head
+  __shared__ __align__(16) float s_recv[NC * G * kD];
+  __shared__ __align__(8) float2 s_mlr[kAttnMaxQ * NC * G];
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -371,7 +374,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    // ---- this worker's partial, left in this CTA's shared memory
+    // ---- this worker's partial, pushed to the CTAs that merge it
     float l0 = l_run[0], l1 = l_run[1];
 #pragma unroll
     for (int m = 4; m <= 16; m <<= 1) {
@@ -384,68 +387,74 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[mb][e] += __shfl_xor_sync(0xffffffffu, o[mb][e], 2);
     }
-    if (gq == 0) {
-      if (2 * tq < G) s_ml[cw][2 * tq] = make_float2(m_run[0], l0);
-      if (2 * tq + 1 < G) s_ml[cw][2 * tq + 1] = make_float2(m_run[1], l1);
-    }
+    // stage O [head][channel] and (m, l) [head] in this warp's first stage,
+    // free now that its last chunk is consumed
+    float *stg = reinterpret_cast<float *>(smem + cw * R * Cfg::kStageBytes);
+    float2 *stg_ml = reinterpret_cast<float2 *>(stg + G * kD);
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int h = 2 * tq + (e & 1);
-        if (h < G) s_po[cw][h][16 * mb + gq + 8 * (e >> 1)] = o[mb][e];
+        if (h < G) stg[h * kD + 16 * mb + gq + 8 * (e >> 1)] = o[mb][e];
       }
+    if (gq == 0) {
+      if (2 * tq < G) stg_ml[2 * tq] = make_float2(m_run[0], l0);
+      if (2 * tq + 1 < G) stg_ml[2 * tq + 1] = make_float2(m_run[1], l1);
+    }
+    __syncwarp();
+    const int j = rank * NC + cw;  // this worker's index in the cluster
+    const uint32_t rc0 = smem_addr(s_recv), ml0 = smem_addr(s_mlr);
+#pragma unroll
+    for (int x = lane; x < G * kD / 4; x += 32) {  // 4 channels of one head per store
+      const int h = x / (kD / 4), c = 4 * (x - h * (kD / 4));
+      const int owner = c / per, cl = c - owner * per;
+      st_cluster_f32x4(cluster_map(rc0 + ((j * G + h) * per + cl) * 4, owner),
+                       *reinterpret_cast<const float4 *>(stg + h * kD + c));
+    }
+    if (lane < G) {
+      const float2 ml = stg_ml[lane];
+#pragma unroll 1
+      for (int qr = 0; qr < Q; ++qr) st_cluster_f32x2(cluster_map(ml0 + (j * G + lane) * 8, qr), ml);
+    }
     __syncwarp();
   }
 
   // ------------------------------------------------------------ merge
-  // every partial of the cluster is written and visible
+  // every partial of the cluster has been pushed and is visible; after this
+  // barrier no CTA touches another's shared memory
   cluster_sync();
   {
-    // CTA `rank` merges channels [rank per, (rank + 1) per) of the G heads:
-    // one thread per 4 channels of a head pulls them from every worker of
-    // the cluster (16-byte loads, all in flight together)
+    // CTA `rank` merges channels [rank per, (rank + 1) per) of the G heads,
+    // one thread per 4 channels of a head, from its own shared memory
     const int n4 = per / 4;
     const int Hq = H * G;
-    const uint32_t po0 = smem_addr(&s_po[0][0][0]), ml0 = smem_addr(&s_ml[0][0]);
 #pragma unroll 1
     for (int e = tid; e < G * n4; e += kAttnThreads) {
-      const int h = e / n4, c = rank * per + 4 * (e - h * n4);
-      float2 ml[kAttnMaxQ * NC];
-      float4 ov[kAttnMaxQ * NC];
-#pragma unroll
-      for (int j = 0; j < kAttnMaxQ * NC; ++j) {
-        ml[j] = make_float2(-INFINITY, 0.f);
-        ov[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j < nw) {
-          const int qr = j / NC, w = j % NC;
-          ml[j] = ld_cluster_f32x2(cluster_map(ml0 + (w * G + h) * 8, qr));
-          ov[j] = ld_cluster_f32x4(cluster_map(po0 + ((w * G + h) * kD + c) * 4, qr));
-        }
-      }
+      const int h = e / n4, cl = 4 * (e - h * n4);
       float M = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < kAttnMaxQ * NC; ++j) M = fmaxf(M, ml[j].x);
+#pragma unroll 4
+      for (int jj = 0; jj < nw; ++jj) M = fmaxf(M, s_mlr[jj * G + h].x);
       float L = 0.f;
       float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < kAttnMaxQ * NC; ++j) {
-        const float sc = ml[j].x != -INFINITY ? exp2f(ml[j].x - M) : 0.f;
-        L = fmaf(sc, ml[j].y, L);
-        A.x = fmaf(sc, ov[j].x, A.x);
-        A.y = fmaf(sc, ov[j].y, A.y);
-        A.z = fmaf(sc, ov[j].z, A.z);
-        A.w = fmaf(sc, ov[j].w, A.w);
+#pragma unroll 4
+      for (int jj = 0; jj < nw; ++jj) {
+        const float2 ml = s_mlr[jj * G + h];
+        const float sc = ml.x != -INFINITY ? exp2f(ml.x - M) : 0.f;
+        const float4 ov = *reinterpret_cast<const float4 *>(&s_recv[(jj * G + h) * per + cl]);
+        L = fmaf(sc, ml.y, L);
+        A.x = fmaf(sc, ov.x, A.x);
+        A.y = fmaf(sc, ov.y, A.y);
+        A.z = fmaf(sc, ov.z, A.z);
+        A.w = fmaf(sc, ov.w, A.w);
       }
+      const int c = rank * per + cl;
       if (L <= 0.f && c == 0) set_status(KVR_ST_NO_TOKENS);
       const float inv = L > 0.f ? 1.f / L : 0.f;
       *reinterpret_cast<float4 *>(out + (static_cast<size_t>(b) * Hq + g * G + h) * kD + c) =
           make_float4(A.x * inv, A.y * inv, A.z * inv, A.w * inv);
     }
   }
-  // every read of this CTA's partials is done before it exits
-  cluster_arrive();
-  cluster_wait();
 }
 
 }  // namespace kvr

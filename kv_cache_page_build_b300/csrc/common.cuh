@@ -264,8 +264,22 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t a, int rank) {
   return r;
 }
 
+// Atomic add on a 32-bit word in the shared memory of a CTA of the cluster
+// (address from cluster_map); returns the old value.
+__device__ __forceinline__ uint32_t atom_add_cluster_u32(uint32_t a, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(a), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void st_cluster_f32(uint32_t a, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32x4(uint32_t a, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
 }
 
 __device__ __forceinline__ void st_cluster_f32x2(uint32_t a, float2 v) {

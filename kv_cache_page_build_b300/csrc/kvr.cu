@@ -223,8 +223,8 @@ int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
                                              w.scores, scores);
     if (e != cudaSuccess) return cuda_fail(e, "k_page_scores");
   }
-  // 2. top-k per unit: a programmatic dependent launch; 4 keys per thread up
-  //    to 1024 pages, 16 beyond; 256 threads up to 4096 pages, 1024 beyond
+  // 2. top-k per unit: a programmatic dependent launch; 256 threads with 4,
+  //    8 or 16 keys each up to 4096 pages, 1024 threads with 16 beyond
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d->n_kv_heads, d->batch);
   cfg.dynamicSmemBytes = 0;
@@ -239,6 +239,10 @@ int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
   if (d->n_pages <= 256 * 4) {
     cfg.blockDim = dim3(256);
     e = cudaLaunchKernelEx(&cfg, k_topk<G, 256, 4>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
+                           sel, sel_phys, spec);
+  } else if (d->n_pages <= 256 * 8) {
+    cfg.blockDim = dim3(256);
+    e = cudaLaunchKernelEx(&cfg, k_topk<G, 256, 8>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
                            sel, sel_phys, spec);
   } else if (d->n_pages <= 256 * 16) {
     cfg.blockDim = dim3(256);

@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
 }
 
 // Selection of one (b, g) unit from its N <= NT * KPT scores, one CTA of NT
-// threads.  Each thread keeps KPT keys in registers: key j of lane l in warp
+// threads (256 to 1024).  Each thread keeps KPT keys in registers: key j of lane l in warp
 // w is page (w KPT + j) 32 + l, so every warp holds consecutive
 // blocks of 32 pages.  The histogram rounds issue all of a thread's shared
 // atomics back to back (histograms double-buffered, a round's bins cleared
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(NT, 1)
            int32_t *__restrict__ sel_phys_out, SpecArgs spec) {
   constexpr int NW = NT / 32, BPT = kSelBins / NT;  // warps, bins per thread
   static_assert(NT % 32 == 0 && kSelBins % NT == 0, "bins are split evenly over the threads");
-  __shared__ uint32_t s_hist[2][kSelBins];
+  __shared__ __align__(16) uint32_t s_hist[2][kSelBins];
   __shared__ uint32_t s_w1[NW], s_w2[NW];
   __shared__ uint32_t s_bin, s_bin_above, s_bin_cnt;
   __shared__ float s_cos[8];
@@ -350,13 +350,29 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
     // thread tid owns bins [BPT tid, BPT tid + BPT); clear them for the round
     // after next once read
+    // (vector accesses: a quarter warp covers 128 contiguous bytes)
     uint32_t c[BPT], mine = 0u;
+    if constexpr (BPT % 4 == 0) {
+      uint4 *hv = reinterpret_cast<uint4 *>(hist + BPT * tid);
 #pragma unroll
-    for (int e = 0; e < BPT; ++e) {
-      c[e] = hist[BPT * tid + e];
-      hist[BPT * tid + e] = 0u;
-      mine += c[e];
+      for (int v = 0; v < BPT / 4; ++v) {
+        const uint4 x = hv[v];
+        hv[v] = make_uint4(0u, 0u, 0u, 0u);
+        c[4 * v] = x.x;
+        c[4 * v + 1] = x.y;
+        c[4 * v + 2] = x.z;
+        c[4 * v + 3] = x.w;
+      }
+    } else {
+      static_assert(BPT == 2, "bins per thread");
+      uint2 *hv = reinterpret_cast<uint2 *>(hist + BPT * tid);
+      const uint2 x = hv[0];
+      hv[0] = make_uint2(0u, 0u);
+      c[0] = x.x;
+      c[1] = x.y;
     }
+#pragma unroll
+    for (int e = 0; e < BPT; ++e) mine += c[e];
     uint32_t incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -455,13 +471,19 @@ __global__ void __launch_bounds__(NT, 1)
   // Per 32-page block: ballots of the two kinds; per warp: running counts;
   // across warps: one exchange of the warp totals.
   const uint32_t lt = (1u << lane) - 1u;  // lanes below this one
+  // the warp's counts of the two kinds: this lane's counts, summed over lanes
   uint32_t w_gt = 0u, w_eq = 0u;
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
     const bool valid = base + 32 * j < N;
-    w_gt += __popc(__ballot_sync(0xffffffffu, valid && key[j] > R));
-    w_eq += __popc(__ballot_sync(0xffffffffu, valid && key[j] >= L && key[j] <= R));
+    w_gt += (valid && key[j] > R) ? 1u : 0u;
+    w_eq += (valid && key[j] >= L && key[j] <= R) ? 1u : 0u;
   }
+  w_gt |= w_eq << 16;  // both counts (<= 32 KPT each) in one word
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) w_gt += __shfl_xor_sync(0xffffffffu, w_gt, m);
+  w_eq = w_gt >> 16;
+  w_gt &= 0xffffu;
   __syncthreads();  // s_w* free; every read of the previous selection is done
   if (lane == 0) {
     s_w1[warp] = w_gt;
