@@ -1,18 +1,21 @@
 """Decode-step benchmark of libkvr on one B300 (or N independent replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload llama3.1-8b-32k|qwen3-4b-128k]
+                    [--workload llama3.1-8b-32k|qwen3-4b-128k|qwen3-4b-128k-host]
 
 One step is one speculative decode step of one attention layer over a batch
-of sequences: group similarity and correction decision, page scoring and
-top-k selection per KV head, then sparse GQA attention over the selected
-pages (two kernels).  Page summaries are built once per cache (prefill) and
-reported on their own.  Inputs are seeded synthetic caches with the layer
-shapes of Llama-3.1-8B (default) or Qwen3-4B; the queries follow the AR(1)
-trace of the speculative workload.  The cache, queries and state are resident
-in HBM before the timed region; four copies of the cache (--copies) rotate so
-that no step reads data a recent step left in L2.  Steps are replayed from a CUDA
-graph of 64 captured steps.
+of sequences, through kvr_speculative_step_overlap: the group-similarity
+correction decision; page scoring and top-k selection per KV head on a side
+stream, beside the sparse GQA attention of the KV heads that reuse their
+previous pages; then the attention of the corrected heads.  Page summaries
+are built once per cache (prefill) and reported on their own.  Inputs are
+seeded synthetic caches with the layer shapes of Llama-3.1-8B (default) or
+Qwen3-4B; the queries follow the AR(1) trace of the speculative workload.
+The cache, queries and state are resident in HBM before the timed region;
+four copies of the cache (--copies) rotate so that no step reads data a
+recent step left in L2.  Steps are replayed from a CUDA graph of 64 captured
+steps.  The "-host" workload keeps the cache in page-locked host memory and
+recalls the selected pages every step (kvr_speculative_step_recall).
 
 Prints one JSON line (rank 0).  With --impl reference the fp64 oracle is
 timed instead, on the host's cores, over a bounded sample of the workload.
@@ -248,9 +251,26 @@ def run_gpu(args, world, rank, local):
         kvr.kvr_sparse_decode_attn(d, qs[i % TRACE_LEN], k_pools[c], v_pools[c], sel_used_phys, k, 0.0, out,
                                    wa, wa_n)
 
-    def step(i):
-        select_call(i)
-        attn_call(i)
+    # one step: kvr_speculative_step_overlap (the decision, then the selection
+    # on a side stream beside the reused heads' attention, then the corrected
+    # heads' attention)
+    side = torch.cuda.Stream()
+    ev_d, ev_s = torch.cuda.Event(), torch.cuda.Event()
+    ev_d.record()
+    ev_s.record()
+    wstep = torch.zeros(kvr.kvr_workspace_size(d, k, kvr.KVR_OP_STEP), dtype=torch.uint8, device=dev)
+
+    def step(i, q=None):
+        c = i % COPIES
+        qq = qs[i % TRACE_LEN] if q is None else q
+        if args.step == "overlap":
+            kvr.kvr_speculative_step_overlap(d, st, qq, summs[c], page_table, k_pools[c], v_pools[c], k,
+                                             wl_trace.tau, 0.0, out, corrected, None, sel_used, sel_used_phys,
+                                             wstep, wstep.numel(), torch.cuda.current_stream(), side, ev_d,
+                                             ev_s)
+        else:
+            kvr.kvr_speculative_step(d, st, qq, summs[c], page_table, k_pools[c], v_pools[c], k, wl_trace.tau,
+                                     0.0, out, corrected, None, sel_used, sel_used_phys, wstep, wstep.numel())
 
     # warm-up: eager steps (the first one is step 0 of the trace)
     for i in range(max(args.warmup, 3)):
@@ -332,17 +352,13 @@ def run_gpu(args, world, rank, local):
     q_host = torch.from_numpy(tr.q.view(np.int16).copy()).pin_memory()
     out_host = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
     q_dev = torch.empty((B, Hq, D), dtype=torch.int16, device=dev)
-    wstep = torch.zeros(kvr.kvr_workspace_size(d, k, kvr.KVR_OP_STEP), dtype=torch.uint8, device=dev)
-    st_e = kvr.kvr_spec_state(q_prev.data_ptr(), sel_prev.data_ptr(), 1)
     n_e2e = min(args.steps, 2000)
     barrier(world)
     torch.cuda.synchronize()
     w0 = time.perf_counter()
     for i in range(n_e2e):
-        c = i % COPIES
         q_dev.copy_(q_host[i % TRACE_LEN], non_blocking=True)
-        kvr.kvr_speculative_step(d, st_e, q_dev, summs[c], page_table, k_pools[c], v_pools[c], k, wl_trace.tau,
-                                 0.0, out, corrected, None, sel_used, sel_used_phys, wstep, wstep.numel())
+        step(i, q_dev)
         out_host.copy_(out, non_blocking=True)
         stream.synchronize()
     e2e_s = time.perf_counter() - w0
@@ -367,6 +383,7 @@ def run_gpu(args, world, rank, local):
                         f"context {wl.context}, page {P}, top-k {k} pages; speculative, tau {wl_trace.tau}",
             "batch": B, "n_q_heads": Hq, "n_kv_heads": H, "head_dim": D, "context": wl.context,
             "page_size": P, "top_k": k, "tau": wl_trace.tau, "storage": "bf16", "accumulate": "f32",
+            "step": f"kvr_speculative_step{'_overlap' if args.step == 'overlap' else ''}",
             "parallelism": f"{world} independent replica(s)" if world > 1 else "1 GPU",
             "l2": f"{COPIES} rotating cache copies: {(COPIES - 1) * (attn_bytes + summ_bytes) / 2**20:.0f} MiB "
                   f"touched between reuses of one copy (L2 126 MB)",
@@ -388,11 +405,13 @@ def run_gpu(args, world, rank, local):
                                   "gbs": round((k_bytes + summ_bytes) / (summ_ms / 1e3) / 1e9, 1),
                                   "note": "once per cache (prefill), not in the step"},
         },
-        "gpu_launches": 3 * args.steps,  # k_page_scores, k_topk, k_sparse_decode
+        # k_page_scores, k_topk, k_sparse_decode (+ k_spec_decide and a second attention launch)
+        "gpu_launches": (5 if args.step == "overlap" else 3) * args.steps,
         "e2e": {"value": round(e2e_value, 2), "unit": "steps/s",
                 "h2d_bytes_per_step": B * Hq * D * 2, "d2h_bytes_per_step": B * Hq * D * 4,
-                "how": f"{n_e2e} eager kvr_speculative_step calls, q copied in from pinned host memory and "
-                       f"the fp32 output copied back every step, stream synchronised per step"},
+                "how": f"{n_e2e} eager kvr_speculative_step{'_overlap' if args.step == 'overlap' else ''} calls, "
+                       f"q copied in from pinned host memory "
+                       f"and the fp32 output copied back every step, stream synchronised per step"},
         "clocks": clk,
         "device_status": status,
     }
@@ -599,6 +618,8 @@ def main():
     ap.add_argument("--workload", default="llama3.1-8b-32k", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--copies", type=int, default=4, help="rotating cache copies (L2-cold timing needs >= 3)")
+    ap.add_argument("--step", default="sequential", choices=["sequential", "overlap"],
+                    help="kvr_speculative_step, or kvr_speculative_step_overlap (selection on a side stream)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
 

@@ -74,7 +74,7 @@ extern "C" {
 /* workspace kinds for kvr_workspace_size */
 #define KVR_OP_SELECT 1 /* kvr_select_pages, kvr_speculative_select */
 #define KVR_OP_ATTN 2   /* kvr_sparse_decode_attn */
-#define KVR_OP_STEP 3   /* kvr_speculative_step, kvr_speculative_step_recall */
+#define KVR_OP_STEP 3   /* kvr_speculative_step(_overlap), kvr_speculative_step_recall */
 
 typedef struct kvr_dims {
   int32_t batch;        /* B */
@@ -172,6 +172,30 @@ int kvr_speculative_step(const kvr_dims *dims, kvr_spec_state *st,
                          float *cbar_opt, int32_t *sel_used,
                          int32_t *sel_used_phys, void *ws, size_t ws_bytes,
                          void *stream);
+
+/* The same speculative decode step with the selection taken off the
+ * attention's critical path ([FreeKV] section 2.1: speculative retrieval
+ * overlaps the selection with the computation).  On `stream`: the
+ * correction decision per (b, g) (as in kvr_speculative_select), sel_used
+ * and sel_used_phys of the reused heads from sel_prev, q_prev <- q_t; record
+ * ev_decide.  On `side_stream`: wait ev_decide, score and select for the
+ * current query (sel_prev <- the new selection; sel_used and sel_used_phys
+ * of the corrected heads), record ev_select.  On `stream`: attention for
+ * the reused heads (concurrently with the selection), wait ev_select,
+ * attention for the corrected heads.  Results are bit-identical to
+ * kvr_speculative_step.  ev_decide and ev_select are caller-created
+ * cudaEvent_t passed as void*; sel_used_phys must be non-NULL.  Workspace
+ * kind KVR_OP_STEP.  Increments st->step on success. */
+int kvr_speculative_step_overlap(const kvr_dims *dims, kvr_spec_state *st,
+                                 const uint16_t *q_t, const uint16_t *summ,
+                                 const int32_t *page_table,
+                                 const uint16_t *k_pool, const uint16_t *v_pool,
+                                 int32_t top_k, float tau, float scale,
+                                 float *out, uint8_t *corrected, float *cbar_opt,
+                                 int32_t *sel_used, int32_t *sel_used_phys,
+                                 void *ws, size_t ws_bytes, void *stream,
+                                 void *side_stream, void *ev_decide,
+                                 void *ev_select);
 
 /* Host-resident cache for streamed recall ([FreeKV] section 2.2, hybrid
  * layouts: the host copy is head-major, HND).  k_host, v_host

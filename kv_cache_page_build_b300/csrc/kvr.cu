@@ -193,7 +193,7 @@ int sm_count(int *out);
 template <int G>
 int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
                     const int32_t *ptab, int k, SelectWs w, int32_t *sel, int32_t *sel_phys,
-                    float *scores, const SpecArgs &spec, cudaStream_t st) {
+                    float *scores, const SpecArgs &spec, cudaStream_t st, bool pdl_first) {
   // 1. page scores: kScCPS CTAs per SM, each warp a worker over a contiguous
   //    range of the flat page list
   auto kern = k_page_scores<G>;
@@ -208,7 +208,8 @@ int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
   CUtensorMap tsm, tsm8;
   if (int rc = make_summ_map(&tsm, summ, F, kScPages)) return rc;
   if (int rc = make_summ_map(&tsm8, summ, F, 8)) return rc;
-  {  // a programmatic dependent launch: the setup overlaps the kernel before it
+  {  // a programmatic dependent launch (unless the stream's last operation is
+     // an event wait): the setup overlaps the kernel before it
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(n_ctas));
     cfg.blockDim = dim3(kScThreads);
@@ -218,7 +219,7 @@ int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_first ? 1 : 0;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tsm, tsm8, q, d->n_kv_heads, d->n_pages, F,
                                              w.scores, scores);
     if (e != cudaSuccess) return cuda_fail(e, "k_page_scores");
@@ -258,14 +259,16 @@ int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
   return KVR_OK;
 }
 
+// pdl_first: launch the scoring kernel as a programmatic dependent launch
+// (false right after an event wait on the stream)
 int launch_select(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
                   const int32_t *ptab, int k, SelectWs w, int32_t *sel, int32_t *sel_phys,
-                  float *scores, const SpecArgs &spec, cudaStream_t st) {
+                  float *scores, const SpecArgs &spec, cudaStream_t st, bool pdl_first = true) {
   switch (d->n_q_heads / d->n_kv_heads) {
-    case 1: return launch_select_g<1>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st);
-    case 2: return launch_select_g<2>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st);
-    case 4: return launch_select_g<4>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st);
-    default: return launch_select_g<8>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st);
+    case 1: return launch_select_g<1>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first);
+    case 2: return launch_select_g<2>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first);
+    case 4: return launch_select_g<4>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first);
+    default: return launch_select_g<8>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first);
   }
 }
 
@@ -468,6 +471,24 @@ SpecArgs no_spec() {
   return s;
 }
 
+template <int G>
+int launch_spec_decide_g(const kvr_dims *d, const uint16_t *q, const int32_t *ptab, int k,
+                         const SpecArgs &spec, cudaStream_t st) {
+  k_spec_decide<G><<<dim3(d->n_kv_heads, d->batch), 32 * G, 0, st>>>(q, ptab, d->n_kv_heads,
+                                                                     d->n_pages, k, spec);
+  return check_launch("k_spec_decide");
+}
+
+int launch_spec_decide(const kvr_dims *d, const uint16_t *q, const int32_t *ptab, int k,
+                       const SpecArgs &spec, cudaStream_t st) {
+  switch (d->n_q_heads / d->n_kv_heads) {
+    case 1: return launch_spec_decide_g<1>(d, q, ptab, k, spec, st);
+    case 2: return launch_spec_decide_g<2>(d, q, ptab, k, spec, st);
+    case 4: return launch_spec_decide_g<4>(d, q, ptab, k, spec, st);
+    default: return launch_spec_decide_g<8>(d, q, ptab, k, spec, st);
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -544,11 +565,9 @@ int kvr_sparse_decode_attn(const kvr_dims *dims, const uint16_t *q, const uint16
                      static_cast<cudaStream_t>(stream));
 }
 
-static int spec_select_impl(const kvr_dims *dims, kvr_spec_state *st, const uint16_t *q_t,
-                            const uint16_t *summ, const int32_t *page_table, int32_t top_k,
-                            float tau, uint8_t *corrected, float *cbar_opt, int32_t *sel_used,
-                            int32_t *sel_used_phys, const int32_t *page2slot, int n_slots,
-                            void *ws, cudaStream_t stream) {
+static SpecArgs spec_args(const kvr_spec_state *st, float tau, uint8_t *corrected,
+                          float *cbar_opt, int32_t *sel_used, int32_t *sel_used_phys,
+                          const int32_t *page2slot, int n_slots) {
   SpecArgs s = no_spec();
   s.enabled = 1;
   s.step = st->step;
@@ -561,6 +580,16 @@ static int spec_select_impl(const kvr_dims *dims, kvr_spec_state *st, const uint
   s.sel_used_phys = sel_used_phys;
   s.page2slot = page2slot;
   s.n_slots = n_slots;
+  return s;
+}
+
+static int spec_select_impl(const kvr_dims *dims, kvr_spec_state *st, const uint16_t *q_t,
+                            const uint16_t *summ, const int32_t *page_table, int32_t top_k,
+                            float tau, uint8_t *corrected, float *cbar_opt, int32_t *sel_used,
+                            int32_t *sel_used_phys, const int32_t *page2slot, int n_slots,
+                            void *ws, cudaStream_t stream) {
+  const SpecArgs s =
+      spec_args(st, tau, corrected, cbar_opt, sel_used, sel_used_phys, page2slot, n_slots);
   return launch_select(dims, q_t, summ, page_table, top_k, carve_select(dims, (uint8_t *)ws),
                        nullptr, nullptr, nullptr, s, stream);
 }
@@ -618,6 +647,55 @@ int kvr_speculative_step(const kvr_dims *dims, kvr_spec_state *st, const uint16_
   return launch_attn(dims, q_t, k_pool, v_pool, dims->n_phys_pages, sel_used_phys, top_k, scale,
                      nullptr, 0, carve_attn(dims, top_k, (uint8_t *)ws + select_ws_bytes(dims)),
                      out, s);
+}
+
+int kvr_speculative_step_overlap(const kvr_dims *dims, kvr_spec_state *st, const uint16_t *q_t,
+                                 const uint16_t *summ, const int32_t *page_table,
+                                 const uint16_t *k_pool, const uint16_t *v_pool, int32_t top_k,
+                                 float tau, float scale, float *out, uint8_t *corrected,
+                                 float *cbar_opt, int32_t *sel_used, int32_t *sel_used_phys,
+                                 void *ws, size_t ws_bytes, void *stream, void *side_stream,
+                                 void *ev_decide, void *ev_select) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_topk(dims, top_k))) return rc;
+  if ((rc = check_spec(dims, st, q_t, summ, corrected, cbar_opt, sel_used, tau))) return rc;
+  if (!page_table || !k_pool || !v_pool || !out || !sel_used_phys || !ev_decide || !ev_select)
+    return KVR_ERR_INVALID_ARG;
+  if (!aligned16(page_table) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
+      !aligned16(sel_used_phys))
+    return KVR_ERR_ALIGN;
+  if (std::isnan(scale)) return KVR_ERR_INVALID_ARG;
+  if ((rc = check_ws(ws, ws_bytes, select_ws_bytes(dims) + attn_ws_bytes(dims, top_k)))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStream_t side = static_cast<cudaStream_t>(side_stream);
+  cudaEvent_t ed = static_cast<cudaEvent_t>(ev_decide), es = static_cast<cudaEvent_t>(ev_select);
+  SpecArgs sa = spec_args(st, tau, corrected, cbar_opt, sel_used, sel_used_phys, nullptr, 0);
+  // 1. the decision per (b, g); reused heads get sel_used from sel_prev
+  rc = launch_spec_decide(dims, q_t, page_table, top_k, sa, s);
+  if (rc) return rc;
+  st->step += 1;
+  cudaError_t e = cudaEventRecord(ed, s);
+  if (e != cudaSuccess) return cuda_fail(e, "record decide event");
+  // 2. side stream: the new selection (becomes sel_prev; sel_used of the corrected heads)
+  e = cudaStreamWaitEvent(side, ed, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "side stream wait");
+  sa.decided = 1;
+  rc = launch_select(dims, q_t, summ, page_table, top_k, carve_select(dims, (uint8_t *)ws), nullptr,
+                     nullptr, nullptr, sa, side, false);
+  if (rc) return rc;
+  e = cudaEventRecord(es, side);
+  if (e != cudaSuccess) return cuda_fail(e, "record select event");
+  // 3. attention: the reused heads alongside the selection, the corrected
+  //    heads once it is done
+  const AttnWs aw = carve_attn(dims, top_k, (uint8_t *)ws + select_ws_bytes(dims));
+  rc = launch_attn(dims, q_t, k_pool, v_pool, dims->n_phys_pages, sel_used_phys, top_k, scale,
+                   corrected, 1, aw, out, s);
+  if (rc) return rc;
+  e = cudaStreamWaitEvent(s, es, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "main stream wait");
+  return launch_attn(dims, q_t, k_pool, v_pool, dims->n_phys_pages, sel_used_phys, top_k, scale,
+                     corrected, 2, aw, out, s, false);
 }
 
 int kvr_working_set_reset(const kvr_dims *dims, const kvr_working_set *wset, void *stream) {

@@ -61,6 +61,9 @@ constexpr int kSelBins = 2048;
 
 struct SpecArgs {
   int enabled;                 // 0: plain selection
+  int decided;                 // 1: k_spec_decide has already taken the decision and
+                               //    filled sel_used for the reused heads; the top-k
+                               //    only reads `corrected` and writes the selections
   int step;                    // 0 -> every head corrected
   float tau;                   // correction threshold
   uint16_t *q_prev;            // [B][Hq][D], read then replaced by q_t
@@ -261,6 +264,67 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
   }
 }
 
+// Correction decision of the speculative step, taken before (and apart from)
+// the new selection, so that the attention of the reused heads does not wait
+// for it (FreeKV, section 2.1: speculative retrieval takes the selection off
+// the critical path).  One CTA of G warps per (b, g): warp w computes the
+// cosine of q_t and q_{t-1} for query head g G + w (4 channels per lane, fp32,
+// the same arithmetic as k_topk's own test), C = mean over the group,
+// corrected = step == 0 or C < tau.  A reused head gets sel_used = sel_prev
+// and its physical ids; q_prev <- q_t.
+template <int G>
+__global__ void __launch_bounds__(32 * G)
+    k_spec_decide(const uint16_t *__restrict__ q, const int32_t *__restrict__ page_table, int H,
+                  int N, int k, SpecArgs spec) {
+  __shared__ float s_cos[G];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = blockIdx.x, b = blockIdx.y;
+  const int Hq = H * G;
+  const size_t unit = static_cast<size_t>(b) * H + g;
+  const size_t qo = (static_cast<size_t>(b) * Hq + g * G + warp) * kD + 4 * lane;
+  const uint2 qa = *reinterpret_cast<const uint2 *>(q + qo);
+  const uint2 qb = *reinterpret_cast<const uint2 *>(spec.q_prev + qo);
+  const float x[4] = {bf_lo(qa.x), bf_hi(qa.x), bf_lo(qa.y), bf_hi(qa.y)};
+  const float y[4] = {bf_lo(qb.x), bf_hi(qb.x), bf_lo(qb.y), bf_hi(qb.y)};
+  float dot = 0.f, nx = 0.f, ny = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    dot = fmaf(x[i], y[i], dot);
+    nx = fmaf(x[i], x[i], nx);
+    ny = fmaf(y[i], y[i], ny);
+  }
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    dot += __shfl_xor_sync(0xffffffffu, dot, m);
+    nx += __shfl_xor_sync(0xffffffffu, nx, m);
+    ny += __shfl_xor_sync(0xffffffffu, ny, m);
+  }
+  if (lane == 0) s_cos[warp] = (nx > 0.f && ny > 0.f) ? dot / (sqrtf(nx) * sqrtf(ny)) : 0.f;
+  __syncthreads();
+  float cb = __int_as_float(0x7fc00000);  // NaN: no previous query at step 0
+  bool corrected = true;
+  if (spec.step > 0) {
+    float sum = 0.f;
+    for (int h = 0; h < G; ++h) sum += s_cos[h];
+    cb = sum / G;
+    corrected = cb < spec.tau;
+  }
+  if (tid == 0) {
+    spec.corrected[unit] = corrected ? 1 : 0;
+    if (spec.cbar) spec.cbar[unit] = cb;
+  }
+  // q_prev <- q_t (every warp has read its head of q_prev above)
+  *reinterpret_cast<uint2 *>(spec.q_prev + qo) = qa;
+  if (!corrected) {  // reuse: sel_used <- previous selection, with its physical ids
+    const int32_t *ptab = page_table + static_cast<size_t>(b) * N;
+    for (int i = tid; i < k; i += 32 * G) {
+      const int p = spec.sel_prev[unit * k + i];
+      spec.sel_used[unit * k + i] = p;
+      spec.sel_used_phys[unit * k + i] = (p >= 0 && p < N) ? __ldg(ptab + p) : -1;
+    }
+  }
+}
+
 // Selection of one (b, g) unit from its N <= NT * KPT scores, one CTA of NT
 // threads (256 to 1024).  Each thread keeps KPT keys in registers: key j of lane l in warp
 // w is page (w KPT + j) 32 + l, so every warp holds consecutive
@@ -292,13 +356,13 @@ __global__ void __launch_bounds__(NT, 1)
   // k_page_scores, the kernel this one depends on, passed its own wait before
   // letting this one start, and writes neither.
   uint2 qa = make_uint2(0u, 0u), qb = make_uint2(0u, 0u);
-  const bool cos_lane = spec.enabled && spec.step > 0 && warp < G;
+  const bool cos_lane = spec.enabled && !spec.decided && spec.step > 0 && warp < G;
   if (cos_lane) {
     const size_t qo = (static_cast<size_t>(b) * Hq + g * G + warp) * kD + 4 * lane;
     qa = *reinterpret_cast<const uint2 *>(q + qo);
     qb = *reinterpret_cast<const uint2 *>(spec.q_prev + qo);
   }
-  const int sp0 = spec.enabled && tid < k ? spec.sel_prev[unit * k + tid] : -1;
+  const int sp0 = spec.enabled && !spec.decided && tid < k ? spec.sel_prev[unit * k + tid] : -1;
   for (int i = tid; i < 2 * kSelBins; i += NT) (&s_hist[0][0])[i] = 0u;
 
   pdl_wait();  // the scores of k_page_scores are complete and visible
@@ -411,7 +475,10 @@ __global__ void __launch_bounds__(NT, 1)
   // ---- speculative mode: group similarity and the correction decision
   const int32_t *ptab = page_table ? page_table + static_cast<size_t>(b) * N : nullptr;
   bool corrected = true;
-  if (spec.enabled) {
+  if (spec.enabled && spec.decided) {
+    corrected = spec.corrected[unit] != 0;  // k_spec_decide's decision (complete before the scores)
+    __syncthreads();                        // every read of s_w* is done
+  } else if (spec.enabled) {
     if (cos_lane) {
       const float x[4] = {bf_lo(qa.x), bf_hi(qa.x), bf_lo(qa.y), bf_hi(qa.y)};
       const float y[4] = {bf_lo(qb.x), bf_hi(qb.x), bf_lo(qb.y), bf_hi(qb.y)};

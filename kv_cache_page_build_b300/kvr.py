@@ -70,6 +70,8 @@ _SIGS = {
                                     _P, _P, _P, _P, _P, _S, _P]),
     "kvr_speculative_step": (_I, [_D, ctypes.POINTER(kvr_spec_state), _P, _P, _P, _P, _P, _I, _F,
                                   _F, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "kvr_speculative_step_overlap": (_I, [_D, ctypes.POINTER(kvr_spec_state), _P, _P, _P, _P, _P, _I,
+                                          _F, _F, _P, _P, _P, _P, _P, _P, _S, _P, _P, _P, _P]),
     "kvr_working_set_reset": (_I, [_D, ctypes.POINTER(kvr_working_set), _P]),
     "kvr_recall_pages": (_I, [_D, ctypes.POINTER(kvr_host_kv), ctypes.POINTER(kvr_working_set),
                               _P, _P, _P, _I, _P, _P, _P]),
@@ -166,6 +168,16 @@ def kvr_speculative_step(d, st, q_t, summ, page_table, k_pool, v_pool, top_k, ta
 def kvr_working_set_reset(d, wset, stream=None):
     return _check(_lib.kvr_working_set_reset(_d(d), ctypes.byref(wset), _stream(stream)),
                   "kvr_working_set_reset")
+
+
+def kvr_speculative_step_overlap(d, st, q_t, summ, page_table, k_pool, v_pool, top_k, tau, scale, out,
+                                 corrected, cbar_opt, sel_used, sel_used_phys, ws, ws_bytes, stream,
+                                 side_stream, ev_decide, ev_select):
+    return _check(_lib.kvr_speculative_step_overlap(
+        _d(d), ctypes.byref(st), _ptr(q_t), _ptr(summ), _ptr(page_table), _ptr(k_pool), _ptr(v_pool),
+        int(top_k), float(tau), float(scale), _ptr(out), _ptr(corrected), _ptr(cbar_opt), _ptr(sel_used),
+        _ptr(sel_used_phys), _ptr(ws), int(ws_bytes), _stream(stream), _stream(side_stream),
+        _event(ev_decide), _event(ev_select)), "kvr_speculative_step_overlap")
 
 
 def kvr_recall_pages(d, host, wset, sel_new, protect, corrected, top_k, sel_slot_out, n_copied_opt,

@@ -119,6 +119,81 @@ def test_speculative_select_alone_matches_step():
         np.testing.assert_array_equal(run.corrected.cpu().numpy().astype(bool), ref["corrected"][t])
 
 
+class OverlapRun(SpecRun):
+    """The same state and outputs, stepped by kvr_speculative_step_overlap
+    (decision, then selection on a side stream beside the reused heads'
+    attention)."""
+
+    def __init__(self, wl, dc):
+        super().__init__(wl, dc)
+        self.side = torch.cuda.Stream()
+        self.ev_d, self.ev_s = torch.cuda.Event(), torch.cuda.Event()
+        self.ev_d.record()                       # torch creates the CUDA event on first record
+        self.ev_s.record()
+
+    def step(self, q_t, poison=True):
+        wl, dc = self.wl, self.dc
+        if poison:
+            self.out.fill_(float("nan"))
+            self.sel_used.fill_(-7)
+        kvr.kvr_speculative_step_overlap(dc.dims, self.st, q_t, dc.summaries(), dc.page_table, dc.k_pool,
+                                         dc.v_pool, wl.top_k, wl.tau, 0.0, self.out, self.corrected, self.cbar,
+                                         self.sel_used, self.sel_used_phys, self.ws, self.ws.numel(),
+                                         torch.cuda.current_stream(), self.side, self.ev_d, self.ev_s)
+
+
+def test_overlapped_step_matches_oracle_and_sequential_step():
+    """Every step of the 64-step trace: the overlapped step gives the oracle's
+    decisions and selections, attention within tolerance, and the same bits
+    as the sequential kvr_speculative_step."""
+    wl, case, dc, tr, ref = accepted_trace(4)
+    qs = gh.t16(tr.q)
+    ovl, seq = OverlapRun(wl, dc), SpecRun(wl, dc)
+    for t in range(wl.steps):
+        ovl.step(qs[t])
+        seq.step(qs[t])
+        torch.cuda.synchronize()
+        assert ovl.st.step == t + 1
+        np.testing.assert_array_equal(ovl.corrected.cpu().numpy().astype(bool), ref["corrected"][t],
+                                      err_msg=f"step {t}")
+        np.testing.assert_array_equal(ovl.sel_used.cpu().numpy(), ref["sel_used"][t], err_msg=f"step {t}")
+        np.testing.assert_array_equal(ovl.sel_prev.cpu().numpy(), ref["sel_new"][t], err_msg=f"step {t}")
+        gh.assert_attn_close(ovl.out.cpu().numpy(), ref["out"][t])
+        for a, b in ((ovl.out, seq.out), (ovl.sel_used, seq.sel_used), (ovl.sel_used_phys, seq.sel_used_phys),
+                     (ovl.corrected, seq.corrected), (ovl.q_prev, seq.q_prev), (ovl.sel_prev, seq.sel_prev)):
+            assert torch.equal(a, b), f"step {t}"
+        c_o, c_s = ovl.cbar.cpu().numpy(), seq.cbar.cpu().numpy()
+        assert np.array_equal(c_o, c_s, equal_nan=True), f"step {t}"
+
+
+def test_overlapped_step_replays_from_a_cuda_graph():
+    """Steps 8..15 captured into a CUDA graph (the side stream joins the
+    capture through the events) and replayed give the eager run's results."""
+    wl, case, dc, tr, ref = accepted_trace(4)
+    qs = gh.t16(tr.q)
+    eager, graph_run = OverlapRun(wl, dc), OverlapRun(wl, dc)
+    for t in range(8):
+        eager.step(qs[t])
+        graph_run.step(qs[t])
+    torch.cuda.synchronize()
+    snap = (graph_run.q_prev.clone(), graph_run.sel_prev.clone(), graph_run.st.step)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for t in range(8, 16):
+            graph_run.step(qs[t], poison=False)
+    # capture ran nothing: put the state back, then replay
+    graph_run.q_prev.copy_(snap[0])
+    graph_run.sel_prev.copy_(snap[1])
+    g.replay()
+    for t in range(8, 16):
+        eager.step(qs[t], poison=False)
+    torch.cuda.synchronize()
+    for a, b in ((eager.out, graph_run.out), (eager.sel_used, graph_run.sel_used),
+                 (eager.sel_prev, graph_run.sel_prev), (eager.q_prev, graph_run.q_prev)):
+        assert torch.equal(a, b)
+    np.testing.assert_array_equal(eager.sel_used.cpu().numpy(), ref["sel_used"][15])
+
+
 # ---------------------------------------------------------------- host-resident cache
 
 def test_recall_trace_matches_oracle_and_hbm_path():
