@@ -53,10 +53,10 @@
 
 namespace kvr {
 
-constexpr int kAttnNC = 2;                         // consumer warps per CTA
+constexpr int kAttnNC = 4;                         // consumer warps per CTA
 constexpr int kAttnThreads = 32 * (kAttnNC + 1);   // + one producer warp
 constexpr int kAttnIds = 128;                      // page ids of a worker range kept in shared memory
-constexpr int kAttnCPS = 2;                        // CTAs per SM
+constexpr int kAttnCPS = 1;                        // CTAs per SM
 constexpr int kAttnMaxQ = 8;                       // CTAs per cluster (the portable limit)
 constexpr int kAttnWarpRing = 48 * 1024;           // ring bytes of one consumer warp
 constexpr int kSmemPerSM = 228 * 1024;             // shared memory of one SM
