@@ -138,7 +138,44 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // The pool [n_phys][P][H][D] bf16 viewed as [tokens][H][D]; one box is 64
 // channels of one head over min(P, 32) consecutive token rows, written to
 // shared memory with 128-byte swizzling (the attention kernel's chunk halves).
+// A tensor map is a pure function of its base address, shape and box, so
+// the encoded maps are kept in a small per-thread cache keyed by exactly
+// those (a hit can never be stale) and eager callers skip the driver call.
+struct MapKey {
+  int kind;
+  const void *ptr;
+  uint64_t a, b, c;
+  bool operator==(const MapKey &o) const {
+    return kind == o.kind && ptr == o.ptr && a == o.a && b == o.b && c == o.c;
+  }
+};
+constexpr int kMapCache = 16;
+struct MapCache {
+  MapKey key[kMapCache];
+  CUtensorMap map[kMapCache];
+  bool valid[kMapCache] = {};
+  int next = 0;
+  bool find(const MapKey &k, CUtensorMap *out) const {
+    for (int i = 0; i < kMapCache; ++i)
+      if (valid[i] && key[i] == k) {
+        *out = map[i];
+        return true;
+      }
+    return false;
+  }
+  void put(const MapKey &k, const CUtensorMap &m) {
+    key[next] = k;
+    map[next] = m;
+    valid[next] = true;
+    next = (next + 1) % kMapCache;
+  }
+};
+thread_local MapCache t_maps;
+
 int make_pool_map(CUtensorMap *map, const void *pool, const kvr_dims *d, int64_t n_phys) {
+  const MapKey key{1, pool, static_cast<uint64_t>(d->n_kv_heads), static_cast<uint64_t>(n_phys),
+                   static_cast<uint64_t>(d->page_size)};
+  if (t_maps.find(key, map)) return KVR_OK;
   auto fn = encode_fn();
   if (!fn) {
     std::snprintf(g_err_text, sizeof g_err_text, "cuTensorMapEncodeTiled unavailable");
@@ -159,12 +196,15 @@ int make_pool_map(CUtensorMap *map, const void *pool, const kvr_dims *d, int64_t
                   static_cast<int>(r));
     return KVR_ERR_CUDA;
   }
+  t_maps.put(key, *map);
   return KVR_OK;
 }
 
 // The page summaries [B][H][N][2][D] bf16 viewed as [pages][256]; one box is
 // 64 channels of `rows` pages, written to shared memory with 128-byte swizzling.
 int make_summ_map(CUtensorMap *map, const void *summ, long long F, int rows) {
+  const MapKey key{2, summ, static_cast<uint64_t>(F), static_cast<uint64_t>(rows), 0};
+  if (t_maps.find(key, map)) return KVR_OK;
   auto fn = encode_fn();
   if (!fn) {
     std::snprintf(g_err_text, sizeof g_err_text, "cuTensorMapEncodeTiled unavailable");
@@ -183,6 +223,7 @@ int make_summ_map(CUtensorMap *map, const void *summ, long long F, int rows) {
                   static_cast<int>(r));
     return KVR_ERR_CUDA;
   }
+  t_maps.put(key, *map);
   return KVR_OK;
 }
 

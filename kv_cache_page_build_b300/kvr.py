@@ -104,10 +104,19 @@ def _ptr(x):
     return x.data_ptr()
 
 
+_torch_c = None
+
+
 def _stream(s):
+    """The raw cudaStream_t of `s`; None means torch's current stream on the
+    current device (read through torch's raw-stream accessor, which costs a
+    fraction of building a Stream object on every call)."""
+    global _torch_c
     if s is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
+        if _torch_c is None:
+            import torch
+            _torch_c = torch._C
+        return _torch_c._cuda_getCurrentRawStream(_torch_c._cuda_getDevice())
     if isinstance(s, int):
         return s
     return getattr(s, "cuda_stream", s)
