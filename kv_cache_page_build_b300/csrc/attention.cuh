@@ -233,16 +233,20 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rank = cluster_ctarank();
-  const long long u = blockIdx.x / Q;
-  const int b = static_cast<int>(u / H), g = static_cast<int>(u % H);
+  // 32-bit index arithmetic throughout (64-bit divisions are emulated and
+  // sat on the path to the first copy): u < B H, k CPP <= 2 kMaxPages and
+  // the worker count is at most 32, so every product below fits
+  const int u = static_cast<int>(blockIdx.x) / Q;
+  const int b = u / H, g = u - b * H;
   const int nw = Q * NC;                                  // workers of the unit
   const int per = kD / Q;                                 // channels merged by each CTA
-  const long long kc = static_cast<long long>(k) * CPP;   // chunks of the unit
+  const int kc = k * CPP;                                 // chunks of the unit
+  const int32_t *sel_u = sel_phys + static_cast<size_t>(u) * k;  // the unit's page ids
   // range of this CTA's worker w: chunks [a, a + n) of the unit
-  auto worker_range = [&](int w, long long &a, int &n) {
-    const long long v = static_cast<long long>(rank) * NC + w;
-    a = v * kc / nw;
-    n = static_cast<int>((v + 1) * kc / nw - a);
+  auto worker_range = [&](int w, int &a, int &n) {
+    const uint32_t v = static_cast<uint32_t>(rank * NC + w);
+    a = static_cast<int>(v * static_cast<uint32_t>(kc) / static_cast<uint32_t>(nw));
+    n = static_cast<int>((v + 1) * static_cast<uint32_t>(kc) / static_cast<uint32_t>(nw)) - a;
   };
 
   if (tid == 0) {
@@ -272,13 +276,12 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
       int idv[NC][kIdRounds];
 #pragma unroll
       for (int w = 0; w < NC; ++w) {
-        long long a;
-        int n;
+        int a, n;
         worker_range(w, a, n);
 #pragma unroll
         for (int r = 0; r < kIdRounds; ++r) {
           const int j = lane + 32 * r;
-          idv[w][r] = j < n ? __ldg(sel_phys + u * k + (a + j) / CPP) : -1;
+          idv[w][r] = j < n ? __ldg(sel_u + (a + j) / CPP) : -1;
         }
       }
 #pragma unroll
@@ -290,8 +293,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
     // lane w (< NC) feeds consumer warp w: the worker's chunks go to its R
     // stages in turn
     const bool feeder = lane < NC;
-    long long a = 0;
-    int n = 0;
+    int a = 0, n = 0;
     if (feeder) worker_range(lane, a, n);
     int i = 0;
     bool abort = false;
@@ -303,13 +305,13 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
       if (mine) {
         const int s = lane * R + i % R;
         if (i < R || mbar_test_wait(&empty[s], static_cast<uint32_t>((i / R - 1) & 1))) {
-          const long long pos = a + i;
-          const int id = i < kAttnIds ? s_ids[lane][i] : __ldg(sel_phys + u * k + pos / CPP);
+          const int pos = a + i;
+          const int id = i < kAttnIds ? s_ids[lane][i] : __ldg(sel_u + pos / CPP);
           const bool ok = id >= 0 && id < n_phys;
           s_ok[s] = ok ? 1 : 0;
           if (ok) {
             uint8_t *dst = smem + s * Cfg::kStageBytes;
-            const int row = id * P + static_cast<int>(pos % CPP) * Cfg::C;
+            const int row = id * P + (pos % CPP) * Cfg::C;
             mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
             tma_load_3d(dst, &tmap_k, &full[s], 0, g, row);
             tma_load_3d(dst + HALF, &tmap_k, &full[s], 64, g, row);
@@ -339,8 +341,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
     const int cw = warp;
     const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group and column pair
     const int Hq = H * G;
-    long long a;
-    int n;
+    int a, n;
     worker_range(cw, a, n);
 
     uint32_t qb[8][2];  // q of head gq as B fragments (k-step kk: channels 16kk + 2tq, +8)
