@@ -83,6 +83,25 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 
 // Next stage of a worker: from flat page f (page pos of its unit), at most 32
 // pages, never past the unit's end or the range end e.
+// v F / n (a worker's range boundary in the flat page list) and f = u N + pos,
+// with 32-bit division whenever the operands fit (64-bit division is emulated
+// and would sit on the path to the first copy).
+__device__ __forceinline__ long long flat_split(long long v, long long F, int n) {
+  const unsigned long long p = static_cast<unsigned long long>(v) * static_cast<unsigned long long>(F);
+  if (p <= 0xffffffffull) return static_cast<long long>(static_cast<uint32_t>(p) / static_cast<uint32_t>(n));
+  return static_cast<long long>(p / static_cast<unsigned long long>(n));
+}
+__device__ __forceinline__ void flat_divmod(long long f, int N, long long &u, int &pos) {
+  if (f <= 0xffffffffll) {
+    const uint32_t q = static_cast<uint32_t>(f) / static_cast<uint32_t>(N);
+    u = q;
+    pos = static_cast<int>(static_cast<uint32_t>(f) - q * static_cast<uint32_t>(N));
+  } else {
+    u = f / N;
+    pos = static_cast<int>(f - u * N);
+  }
+}
+
 __device__ __forceinline__ int sc_chunk(long long f, int pos, int N, long long e) {
   return static_cast<int>(min(static_cast<long long>(min(kScPages, N - pos)), e - f));
 }
@@ -126,9 +145,11 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
   if (warp == kScNC) {
     const bool feeder = lane < kScNC;
     const long long v = static_cast<long long>(blockIdx.x) * kScNC + lane;
-    const long long e = feeder ? (v + 1) * F / n_workers : 0;
-    long long f = feeder ? v * F / n_workers : 0;
-    int pos = static_cast<int>(f % N), use = 0;
+    const long long e = feeder ? flat_split(v + 1, F, n_workers) : 0;
+    long long f = feeder ? flat_split(v, F, n_workers) : 0;
+    long long uf;
+    int pos, use = 0;
+    flat_divmod(f, N, uf, pos);
     bool abort = false;
     uint64_t t_prog = global_timer_ns();
 #pragma unroll 1
@@ -174,10 +195,11 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
 
   // ------------------------------------------------------------ workers
   const long long v = static_cast<long long>(blockIdx.x) * kScNC + warp;
-  const long long e = (v + 1) * F / n_workers;
-  long long f = v * F / n_workers;
-  long long u = f / N;
-  int pos = static_cast<int>(f % N);
+  const long long e = flat_split(v + 1, F, n_workers);
+  long long f = flat_split(v, F, n_workers);
+  long long u;
+  int pos;
+  flat_divmod(f, N, u, pos);
   const int gq = lane >> 2, tq = lane & 3, mi = lane >> 3, mr = lane & 7;
   // [q- | q+] of head gq as B fragments: k-step kk < 8 meets kmin channels
   // 16kk.., kk >= 8 meets kmax channels 16(kk - 8)..; words hold bf16 pairs
@@ -187,7 +209,8 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
   for (int use = 0; f < e; ++use) {
     const int cnt = sc_chunk(f, pos, N, e);
     if (q_unit != u) {
-      const int b = static_cast<int>(u / H), g = static_cast<int>(u % H);
+      const int ui = static_cast<int>(u);  // < B H
+      const int b = ui / H, g = ui - b * H;
       const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
           q + (static_cast<size_t>(b) * Hq + g * G + min(gq, G - 1)) * kD);
       const bool on = gq < G;
