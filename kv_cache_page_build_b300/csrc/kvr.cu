@@ -265,8 +265,9 @@ int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
                                              w.scores, scores);
     if (e != cudaSuccess) return cuda_fail(e, "k_page_scores");
   }
-  // 2. top-k per unit: a programmatic dependent launch; 256 threads with 4,
-  //    8 or 16 keys each up to 4096 pages, 1024 threads with 16 beyond
+  // 2. top-k per unit: a programmatic dependent launch; threads x keys per
+  //    thread by page count (measured: fewer than 8 keys per thread costs more
+  //    in cross-warp steps than it saves)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d->n_kv_heads, d->batch);
   cfg.dynamicSmemBytes = 0;
@@ -286,9 +287,13 @@ int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
     cfg.blockDim = dim3(256);
     e = cudaLaunchKernelEx(&cfg, k_topk<G, 256, 8>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
                            sel, sel_phys, spec);
-  } else if (d->n_pages <= 256 * 16) {
-    cfg.blockDim = dim3(256);
-    e = cudaLaunchKernelEx(&cfg, k_topk<G, 256, 16>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
+  } else if (d->n_pages <= 512 * 8) {
+    cfg.blockDim = dim3(512);
+    e = cudaLaunchKernelEx(&cfg, k_topk<G, 512, 8>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
+                           sel, sel_phys, spec);
+  } else if (d->n_pages <= 512 * 16) {
+    cfg.blockDim = dim3(512);
+    e = cudaLaunchKernelEx(&cfg, k_topk<G, 512, 16>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
                            sel, sel_phys, spec);
   } else {
     cfg.blockDim = dim3(1024);

@@ -147,9 +147,10 @@ SHAPES = [
     dict(top_k=1, batch=3),
     dict(n_pages=1, top_k=1, page_size=16),
     dict(channel_scale=True, n_pages=300, top_k=40),
-    dict(n_pages=1500, top_k=100, batch=1, page_size=16),      # ragged, 16 keys per top-k thread
-    dict(n_pages=5000, top_k=130, batch=1, page_size=16, n_kv_heads=1),   # 1024-thread top-k
-    dict(n_pages=16384, top_k=256, batch=1, page_size=16, n_q_heads=4, n_kv_heads=1),  # most pages
+    dict(n_pages=1500, top_k=100, batch=1, page_size=16),      # ragged; top-k 256 threads x 8 keys
+    dict(n_pages=3000, top_k=90, batch=1, page_size=16),       # top-k 512 threads x 8 keys
+    dict(n_pages=5000, top_k=130, batch=1, page_size=16, n_kv_heads=1),   # top-k 512 x 16
+    dict(n_pages=16384, top_k=256, batch=1, page_size=16, n_q_heads=4, n_kv_heads=1),  # most pages: 1024 x 16
 ]
 
 
