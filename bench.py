@@ -182,10 +182,16 @@ def traffic_for(kernel: str, wl_name: str):
 
 
 def source_hash() -> str:
+    """Hash of the kernel sources' code: comments and whitespace are dropped,
+    so an edit of the prose alone keeps a profile's counters current."""
+    import re
     h = hashlib.sha256()
     for p in sorted(glob.glob(os.path.join(ROOT, "kv_cache_page_build_b300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 
 

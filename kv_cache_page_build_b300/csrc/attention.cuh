@@ -27,26 +27,20 @@
 //        the ring: as soon as the warp releases a stage, the lane issues the
 //        warp's next chunk into it (four tiled TMA copies: the 64-channel
 //        halves of the chunk's K and V rows for head g, 128-byte swizzled).
-//        The range's page ids are read into shared memory first, so issuing
+//        The ranges' page ids are read into shared memory first, so issuing
 //        never waits on a load.
 //   consumer  warps 0..NC-1 on the tensor cores (mma.sync m16n8k16, bf16 in,
-//        fp32 accumulators):
-//     QK   S[h][t] = q_h . K_t, the G query heads on the 16-row side (rows
-//          G..15 zero), 8 tokens per MMA column block; q stays in registers
-//          as A fragments, K fragments come from shared memory by ldmatrix.
-//     softmax  online, base 2 (logits prescaled by scale * log2 e), per
-//          chunk, on the accumulator fragments (4 lanes per head).
-//     PV   O^T[c][h] += V^T[c][t] P^T[t][h]: V fragments by transposing
-//          ldmatrix, P straight from the QK accumulators, split into a bf16
-//          high part and a bf16 residual (two MMAs) so the weights keep
-//          about 16 bits.
+//        fp32 accumulators), one chunk at a time (attn_chunk): S^T = K q^T
+//        with the chunk's tokens on the MMA's 16-row side, online softmax in
+//        base 2, then O^T += V^T P^T with P^T moved into the operand layout
+//        by movmatrix and split into a bf16 high part and residual.
 // The G x D output of a group is a 4- to 32-row contraction per page, far
 // from the tensor cores' peak; they are used because they cut the issue
-// slots per chunk about five-fold against CUDA-core FMAs, which keeps the
-// consumers well ahead of the memory stream.
+// slots per chunk several-fold against CUDA-core FMAs, which keeps the
+// consumers ahead of the memory stream.
 // Every wait on a copy is bounded; after a timeout the CTA stops issuing
-// copies, drains the ones in flight and still takes part in both cluster
-// barriers, which every thread of the cluster reaches after bounded work.
+// copies, drains the ones in flight and still takes part in the cluster
+// barrier, which every thread of the cluster reaches after bounded work.
 #pragma once
 
 #include "common.cuh"
