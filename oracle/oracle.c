@@ -70,19 +70,35 @@ int oracle_max_threads(void) {
 #endif
 }
 
+/* Tokens of logical page p that a sequence of `len` tokens has written:
+ * min(P, len - p P), at least 0 (decode-time append fills pages in order;
+ * "Key-Value (KV) Cache" wiki page, PagedAttention).  len < 0 means every
+ * page is full. */
+static int page_tokens(int P, int p, long len) {
+  if (len < 0) return P;
+  long v = len - (long)p * P;
+  return v <= 0 ? 0 : (v >= P ? P : (int)v);
+}
+
 /* Per (sequence, KV head, logical page): per-channel min and max of the keys
- * of the page's P tokens.  Returns the number of out-of-range physical ids. */
+ * of the page's written tokens (all P when seq_len is NULL; a page with none
+ * gets NaN).  Returns the number of out-of-range physical ids. */
 int oracle_summaries(int B, int H, int D, int P, int N, int n_phys,
                      const uint16_t *k_pool, const int32_t *page_table,
-                     double *kmin, double *kmax) {
+                     const int32_t *seq_len, double *kmin, double *kmax) {
   int bad = 0;
 #pragma omp parallel for collapse(2) reduction(+ : bad) schedule(static)
   for (int b = 0; b < B; b++)
     for (int g = 0; g < H; g++)
       for (int p = 0; p < N; p++) {
         int phys = page_table[(size_t)b * N + p];
+        int nt = page_tokens(P, p, seq_len ? seq_len[b] : -1);
         double *mn = kmin + (((size_t)b * H + g) * N + p) * D;
         double *mx = kmax + (((size_t)b * H + g) * N + p) * D;
+        if (nt == 0) {
+          for (int c = 0; c < D; c++) mn[c] = mx[c] = NAN;
+          continue;
+        }
         if (phys < 0 || phys >= n_phys) {
           bad++;
           for (int c = 0; c < D; c++) mn[c] = mx[c] = NAN;
@@ -90,7 +106,7 @@ int oracle_summaries(int B, int H, int D, int P, int N, int n_phys,
         }
         for (int c = 0; c < D; c++) {
           double lo = INFINITY, hi = -INFINITY;
-          for (int t = 0; t < P; t++) {
+          for (int t = 0; t < nt; t++) {
             double v = bf(k_pool[pool_at(P, H, D, phys, t, g, c)]);
             if (v < lo) lo = v;
             if (v > hi) hi = v;
@@ -158,19 +174,30 @@ void oracle_topk(int n, const double *s, int k, int32_t *sel) {
   free(r);
 }
 
-void oracle_topk_all(int units, int n, const double *s, int k, int32_t *sel) {
+/* Per unit; n_valid (may be NULL) limits unit u to its pages 0 .. n_valid[u]-1.
+ * A unit with fewer valid pages than k selects them all and pads with -1. */
+void oracle_topk_all(int units, int n, const double *s, int k, const int32_t *n_valid,
+                     int32_t *sel) {
 #pragma omp parallel for schedule(static)
-  for (int u = 0; u < units; u++) oracle_topk(n, s + (size_t)u * n, k, sel + (size_t)u * k);
+  for (int u = 0; u < units; u++) {
+    int nv = n_valid ? (n_valid[u] < n ? n_valid[u] : n) : n;
+    int kk = k < nv ? k : nv;
+    int32_t *out = sel + (size_t)u * k;
+    if (kk > 0) oracle_topk(nv, s + (size_t)u * n, kk, out);
+    for (int i = kk; i < k; i++) out[i] = -1;
+  }
 }
 
-/* Decode attention of every query head over the tokens of its KV head's
- * selected logical pages (ascending page, then token order):
+/* Decode attention of every query head over the written tokens of its KV
+ * head's selected logical pages (ascending page, then token order; all P
+ * tokens of a page when seq_len is NULL; a -1 entry is no page):
  *   l_t = scale * q . K_t,  w_t = exp(l_t - max l),  o = sum w_t V_t / sum w_t.
  * Returns the number of out-of-range page ids met. */
 int oracle_attention(int B, int Hq, int H, int D, int P, int N, int n_phys,
                      const uint16_t *q, const uint16_t *k_pool,
                      const uint16_t *v_pool, const int32_t *page_table,
-                     const int32_t *sel, int k, double scale, double *out) {
+                     const int32_t *sel, int k, const int32_t *seq_len, double scale,
+                     double *out) {
   int G = Hq / H, bad = 0;
   int T = k * P;
 #pragma omp parallel for collapse(2) reduction(+ : bad) schedule(static)
@@ -183,6 +210,10 @@ int oracle_attention(int B, int Hq, int H, int D, int P, int N, int n_phys,
       int *phys_of = (int *)malloc(sizeof(int) * (size_t)k);
       for (int i = 0; i < k; i++) {
         int lp = pages[i];
+        if (lp == -1) {
+          phys_of[i] = -1;
+          continue;
+        }
         int phys = (lp >= 0 && lp < N) ? page_table[(size_t)b * N + lp] : -1;
         if (phys < 0 || phys >= n_phys) {
           bad++;
@@ -190,11 +221,12 @@ int oracle_attention(int B, int Hq, int H, int D, int P, int N, int n_phys,
         }
         phys_of[i] = phys;
       }
+      long len = seq_len ? seq_len[b] : -1;
       double mx = -INFINITY;
       for (int i = 0; i < k; i++)
         for (int t = 0; t < P; t++) {
           double l = -INFINITY;
-          if (phys_of[i] >= 0) {
+          if (phys_of[i] >= 0 && t < page_tokens(P, pages[i], len)) {
             double dot = 0.0;
             for (int c = 0; c < D; c++)
               dot += bf(qh[c]) * bf(k_pool[pool_at(P, H, D, phys_of[i], t, g, c)]);
@@ -208,7 +240,7 @@ int oracle_attention(int B, int Hq, int H, int D, int P, int N, int n_phys,
       double wsum = 0.0;
       for (int i = 0; i < k; i++) {
         if (phys_of[i] < 0) continue;
-        for (int t = 0; t < P; t++) {
+        for (int t = 0; t < page_tokens(P, pages[i], len); t++) {
           double w = exp(logit[i * P + t] - mx);
           wsum += w;
           for (int c = 0; c < D; c++)

@@ -49,15 +49,15 @@ def lib():
         build()
         L = ctypes.CDLL(_LIB)
         i, p, d = ctypes.c_int, ctypes.c_void_p, ctypes.c_double
-        L.oracle_summaries.argtypes = [i, i, i, i, i, i, p, p, p, p]
+        L.oracle_summaries.argtypes = [i, i, i, i, i, i, p, p, p, p, p]
         L.oracle_summaries.restype = i
         L.oracle_scores.argtypes = [i, i, i, i, i, p, p, p, p]
         L.oracle_scores.restype = None
         L.oracle_topk.argtypes = [i, p, i, p]
         L.oracle_topk.restype = None
-        L.oracle_topk_all.argtypes = [i, i, p, i, p]
+        L.oracle_topk_all.argtypes = [i, i, p, i, p, p]
         L.oracle_topk_all.restype = None
-        L.oracle_attention.argtypes = [i, i, i, i, i, i, i, p, p, p, p, p, i, d, p]
+        L.oracle_attention.argtypes = [i, i, i, i, i, i, i, p, p, p, p, p, i, p, d, p]
         L.oracle_attention.restype = i
         L.oracle_group_cosine.argtypes = [i, i, i, i, p, p, p]
         L.oracle_group_cosine.restype = None
@@ -86,15 +86,26 @@ def _c(a, dtype):
 # primitives
 
 
-def summaries(k_pool, page_table, n_kv_heads=None):
-    """(kmin, kmax), each [B][H][N][D] float64, from a [n_phys][P][H][D] bf16 pool."""
+def _lens(seq_len, B):
+    if seq_len is None:
+        return None, None
+    seq_len = np.ascontiguousarray(seq_len, dtype=np.int32)
+    assert seq_len.shape == (B,)
+    return seq_len, seq_len.ctypes.data_as(ctypes.c_void_p)
+
+
+def summaries(k_pool, page_table, n_kv_heads=None, seq_len=None):
+    """(kmin, kmax), each [B][H][N][D] float64, from a [n_phys][P][H][D] bf16 pool:
+    min/max over each page's written tokens (all P without seq_len [B]; NaN for
+    a page with none)."""
     k_pool, kp = _c(k_pool, np.uint16)
     page_table, tp = _c(page_table, np.int32)
     n_phys, P, H, D = k_pool.shape
     B, N = page_table.shape
+    seq_len, lp = _lens(seq_len, B)
     kmin = np.empty((B, H, N, D))
     kmax = np.empty((B, H, N, D))
-    bad = lib().oracle_summaries(B, H, D, P, N, n_phys, kp, tp,
+    bad = lib().oracle_summaries(B, H, D, P, N, n_phys, kp, tp, lp,
                                  kmin.ctypes.data_as(ctypes.c_void_p),
                                  kmax.ctypes.data_as(ctypes.c_void_p))
     if bad:
@@ -114,19 +125,26 @@ def scores(q, kmin, kmax):
     return out
 
 
-def topk(s, k):
-    """Top-k page ids per row of s [..., N], ties to the lower id, sorted ascending."""
+def topk(s, k, n_valid=None):
+    """Top-k page ids per row of s [..., N], ties to the lower id, sorted ascending.
+    n_valid [...] (optional) limits each row to its first n_valid pages; a row
+    with fewer valid pages than k selects them all and pads with -1."""
     s = np.ascontiguousarray(s, dtype=np.float64)
     lead, n = s.shape[:-1], s.shape[-1]
     units = int(np.prod(lead)) if lead else 1
     sel = np.empty(lead + (k,), dtype=np.int32)
-    lib().oracle_topk_all(units, n, s.ctypes.data_as(ctypes.c_void_p), int(k),
+    nv, nvp = (None, None)
+    if n_valid is not None:
+        nv = np.ascontiguousarray(np.broadcast_to(n_valid, lead), dtype=np.int32)
+        nvp = nv.ctypes.data_as(ctypes.c_void_p)
+    lib().oracle_topk_all(units, n, s.ctypes.data_as(ctypes.c_void_p), int(k), nvp,
                           sel.ctypes.data_as(ctypes.c_void_p))
     return sel
 
 
-def attention(q, k_pool, v_pool, page_table, sel, scale=None):
-    """[B][Hq][D] float64 attention of each query head over its KV head's selected pages."""
+def attention(q, k_pool, v_pool, page_table, sel, scale=None, seq_len=None):
+    """[B][Hq][D] float64 attention of each query head over the written tokens
+    (all of them without seq_len [B]) of its KV head's selected pages."""
     q, qp = _c(q, np.uint16)
     k_pool, kp = _c(k_pool, np.uint16)
     v_pool, vp = _c(v_pool, np.uint16)
@@ -139,7 +157,8 @@ def attention(q, k_pool, v_pool, page_table, sel, scale=None):
     if scale is None:
         scale = 1.0 / np.sqrt(D)
     out = np.empty((B, Hq, D))
-    bad = lib().oracle_attention(B, Hq, H, D, P, N, n_phys, qp, kp, vp, tp, sp, k,
+    seq_len, lp = _lens(seq_len, B)
+    bad = lib().oracle_attention(B, Hq, H, D, P, N, n_phys, qp, kp, vp, tp, sp, k, lp,
                                  float(scale), out.ctypes.data_as(ctypes.c_void_p))
     if bad:
         raise ValueError(f"{bad} out-of-range page ids")
@@ -160,18 +179,45 @@ def group_cosine(q_t, q_prev, n_kv_heads):
 # one decode step and the speculative trace
 
 
-def select(q, k_pool, page_table, n_kv_heads, top_k, summ=None):
-    """Non-speculative selection: (sel [B][H][k], scores [B][H][N])."""
+def valid_pages(seq_len, page_size):
+    """Pages a sequence of seq_len tokens has started: ceil(seq_len / P)."""
+    return (np.asarray(seq_len, dtype=np.int64) + page_size - 1) // page_size
+
+
+def select(q, k_pool, page_table, n_kv_heads, top_k, summ=None, seq_len=None):
+    """Non-speculative selection: (sel [B][H][k], scores [B][H][N]); with
+    seq_len [B], among each sequence's started pages only."""
     if summ is None:
-        summ = summaries(k_pool, page_table)
+        summ = summaries(k_pool, page_table, seq_len=seq_len)
     s = scores(q, *summ)
-    return topk(s, top_k), s
+    nv = None
+    if seq_len is not None:
+        nv = np.repeat(valid_pages(seq_len, k_pool.shape[1])[:, None], n_kv_heads, axis=1)
+    return topk(s, top_k, nv), s
 
 
-def decode_step(q, k_pool, v_pool, page_table, n_kv_heads, top_k, scale=None, summ=None):
+def decode_step(q, k_pool, v_pool, page_table, n_kv_heads, top_k, scale=None, summ=None, seq_len=None):
     """One non-speculative decode step: returns (sel, scores, out)."""
-    sel, s = select(q, k_pool, page_table, n_kv_heads, top_k, summ)
-    return sel, s, attention(q, k_pool, v_pool, page_table, sel, scale)
+    sel, s = select(q, k_pool, page_table, n_kv_heads, top_k, summ, seq_len)
+    return sel, s, attention(q, k_pool, v_pool, page_table, sel, scale, seq_len)
+
+
+def append(k_pool, v_pool, page_table, seq_len, k_new, v_new):
+    """Decode-time append ("Key-Value (KV) Cache" wiki page: each step adds
+    the new token's K and V to the cache; PagedAttention fills pages in
+    order): token t = seq_len[b] of sequence b goes to row t mod P of
+    logical page t / P, for every KV head.  Returns new pools and lengths
+    (the inputs are not modified).  k_new, v_new: [B][H][D] bf16 bits."""
+    k_pool, v_pool = np.array(k_pool, copy=True), np.array(v_pool, copy=True)
+    seq_len = np.array(seq_len, dtype=np.int32, copy=True)
+    P = k_pool.shape[1]
+    for b in range(len(seq_len)):
+        t = int(seq_len[b])
+        phys = int(page_table[b, t // P])
+        k_pool[phys, t % P] = k_new[b]
+        v_pool[phys, t % P] = v_new[b]
+        seq_len[b] = t + 1
+    return k_pool, v_pool, seq_len
 
 
 def speculative_trace(qs, k_pool, v_pool, page_table, n_kv_heads, top_k, tau,

@@ -302,6 +302,101 @@ def test_spec_trace_jumps_are_corrected_and_reuse_is_previous_selection():
 
 # ---------------------------------------------------------------- printed numbers
 
+# ---------------------------------------------------------------- partial pages (decode-time append)
+
+LENS = np.array([37, 9], dtype=np.int32)   # page size 4: 10 and 3 pages started, last ones partial
+
+
+def test_summaries_with_lengths_equal_numpy_over_written_rows():
+    wl = small()
+    case = synth.make_case(wl)
+    kmin, kmax = oracle.summaries(case.k_pool, case.page_table, seq_len=LENS)
+    keys = logical_keys(case)                                    # [B][N][P][H][D]
+    P = wl.page_size
+    for b, L in enumerate(LENS):
+        for p in range(wl.n_pages):
+            nt = min(P, max(0, int(L) - p * P))
+            if nt == 0:
+                assert np.isnan(kmin[b, :, p]).all() and np.isnan(kmax[b, :, p]).all()
+                continue
+            rows = keys[b, p, :nt]                                # [nt][H][D]
+            np.testing.assert_array_equal(kmin[b, :, p], rows.min(axis=0))
+            np.testing.assert_array_equal(kmax[b, :, p], rows.max(axis=0))
+
+
+def test_topk_with_valid_pages_is_brute_force_and_pads():
+    rng = np.random.default_rng(4)
+    s = np.round(rng.normal(size=(3, 20)), 1)                   # ties likely
+    nv = np.array([20, 7, 3])
+    sel = oracle.topk(s, 5, nv)
+    for u in range(3):
+        order = sorted(range(nv[u]), key=lambda p: (-s[u, p], p))
+        want = sorted(order[:5]) + [-1] * max(0, 5 - nv[u])
+        assert list(sel[u]) == want
+
+
+def test_attention_with_lengths_equals_sdpa_on_written_tokens():
+    wl = small()
+    case = synth.make_case(wl)
+    P, G = wl.page_size, wl.group
+    sel = np.array([[[0, 3, 9], [2, 5, 9]], [[0, 1, 2], [2, 1, 0]]], dtype=np.int32)
+    sel = np.sort(sel, axis=-1)
+    out = oracle.attention(case.q, case.k_pool, case.v_pool, case.page_table, sel, scale=0.3, seq_len=LENS)
+    keys, vals = logical_keys(case), logical_values(case)
+    q = torch.from_numpy(f(case.q))
+    for b, L in enumerate(LENS):
+        for h in range(wl.n_q_heads):
+            g = h // G
+            rows = [(p, t) for p in sel[b, g] for t in range(min(P, max(0, int(L) - p * P)))]
+            kk = torch.from_numpy(np.stack([keys[b, p, t, g] for p, t in rows]))[None]
+            vv = torch.from_numpy(np.stack([vals[b, p, t, g] for p, t in rows]))[None]
+            ref = torch.nn.functional.scaled_dot_product_attention(q[b, h][None, None], kk, vv, scale=0.3)[0, 0]
+            np.testing.assert_allclose(out[b, h], ref.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_full_lengths_reduce_to_the_length_free_step():
+    wl = small()
+    case = synth.make_case(wl)
+    full = np.full(wl.batch, wl.n_pages * wl.page_size, dtype=np.int32)
+    a = oracle.decode_step(case.q, case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads, wl.top_k)
+    b_ = oracle.decode_step(case.q, case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads, wl.top_k,
+                            seq_len=full)
+    for x, y in zip(a, b_):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_append_writes_the_next_row_of_every_head():
+    """Appending tokens one at a time from length L0 writes exactly the rows a
+    direct copy of the source tokens would, and the summaries over the written
+    rows then equal numpy's reduction of those rows."""
+    wl = small()
+    src = synth.make_case(wl)                                    # the tokens to append
+    dst = synth.make_case(small(seed=99))                        # another cache with the same table shape
+    P, H, D = wl.page_size, wl.n_kv_heads, wl.head_dim
+    lens = np.array([5, 0], dtype=np.int32)
+    kp, vp = dst.k_pool, dst.v_pool
+    kl, vl = logical_keys(src), logical_values(src)
+    want_k, want_v = f(kp).copy(), f(vp).copy()
+    for step in range(11):
+        k_new = np.stack([src.k_pool[src.page_table[b, (lens[b] // P)], lens[b] % P] for b in range(wl.batch)])
+        v_new = np.stack([src.v_pool[src.page_table[b, (lens[b] // P)], lens[b] % P] for b in range(wl.batch)])
+        for b in range(wl.batch):
+            t = int(lens[b])
+            want_k[dst.page_table[b, t // P], t % P] = kl[b, t // P, t % P]
+            want_v[dst.page_table[b, t // P], t % P] = vl[b, t // P, t % P]
+        kp, vp, lens2 = oracle.append(kp, vp, dst.page_table, lens, k_new, v_new)
+        np.testing.assert_array_equal(lens2, lens + 1)
+        lens = lens2
+        np.testing.assert_array_equal(f(kp), want_k)
+        np.testing.assert_array_equal(f(vp), want_v)
+    kmin, kmax = oracle.summaries(kp, dst.page_table, seq_len=lens)
+    for b, L in enumerate(lens):
+        rows = f(kp)[dst.page_table[b]].reshape(-1, H, D)[:L]   # logical token order
+        last = (L - 1) // P
+        np.testing.assert_array_equal(kmin[b, :, last], rows[last * P:L].min(axis=0))
+        np.testing.assert_array_equal(kmax[b, :, last], rows[last * P:L].max(axis=0))
+
+
 def test_kv_cache_size_matches_printed_llama65b_figure():
     g = json.load(open(os.path.join(GOLDEN, "kv_cache_size_llama65b.json")))
     n = oracle.kv_cache_bytes(g["n_layers"], g["n_kv_heads"], g["head_dim"], g["n_tokens"], g["bytes_per_elem"])
