@@ -133,6 +133,53 @@ int kvr_sparse_decode_attn(const kvr_dims *dims, const uint16_t *q,
                            const int32_t *sel_phys, int32_t top_k, float scale,
                            float *out, void *ws, size_t ws_bytes, void *stream);
 
+/* ---- partial last pages and decode-time append ([KVwiki]: each decode step
+ * appends the new token's K and V; PagedAttention fills a sequence's pages
+ * in order).  seq_len [B] int32 (device) counts the tokens sequence b has
+ * written: it has started ceil(seq_len[b] / P) pages and logical page p
+ * holds min(P, seq_len[b] - p P) tokens (rows 0 .. of the page). */
+
+/* Append one token per sequence: for every KV head g, K row k_new[b][g] and
+ * V row v_new[b][g] ([B][H][D] bf16) go to row t mod P of logical page t / P
+ * (physical page page_table[b][t / P]) with t = seq_len[b]; that page's
+ * summary in summ becomes the min/max over its written tokens (the new key
+ * alone when it starts the page); then seq_len[b] = t + 1.  A sequence that
+ * is full (t >= N P) or whose page id is outside [0, n_phys) is left as is
+ * and sets KVR_ST_BAD_INDEX.  The caller maps the page before its first
+ * token.  One kernel on `stream`. */
+int kvr_append_kv(const kvr_dims *dims, const uint16_t *k_new,
+                  const uint16_t *v_new, const int32_t *page_table,
+                  int32_t *seq_len, uint16_t *k_pool, uint16_t *v_pool,
+                  uint16_t *summ, void *stream);
+
+/* kvr_build_summaries over the written tokens of each page only; pages a
+ * sequence has not started are left untouched. */
+int kvr_build_summaries_len(const kvr_dims *dims, const uint16_t *k_pool,
+                            const int32_t *page_table, const int32_t *seq_len,
+                            uint16_t *summ, void *stream);
+
+/* kvr_select_pages over the started pages of each sequence only.  A
+ * sequence with fewer started pages than top_k selects all of them
+ * (ascending) and fills the rest of its rows of sel and sel_phys with -1.
+ * Workspace kind KVR_OP_SELECT. */
+int kvr_select_pages_len(const kvr_dims *dims, const uint16_t *q,
+                         const uint16_t *summ, const int32_t *page_table,
+                         const int32_t *seq_len, int32_t top_k, int32_t *sel,
+                         int32_t *sel_phys, float *scores_opt, void *ws,
+                         size_t ws_bytes, void *stream);
+
+/* kvr_sparse_decode_attn over written tokens only: in the physical page
+ * page_table[b][(seq_len[b] - 1) / P] (the sequence's last, possibly partial
+ * page) only its written rows take part; a -1 entry of sel_phys is no page
+ * (skipped without a status bit).  sel_phys must hold started pages.
+ * Workspace kind KVR_OP_ATTN. */
+int kvr_sparse_decode_attn_len(const kvr_dims *dims, const uint16_t *q,
+                               const uint16_t *k_pool, const uint16_t *v_pool,
+                               const int32_t *page_table, const int32_t *seq_len,
+                               const int32_t *sel_phys, int32_t top_k,
+                               float scale, float *out, void *ws,
+                               size_t ws_bytes, void *stream);
+
 /* State of the speculative mode, owned by the caller.  q_prev [B][Hq][D]
  * bf16 and sel_prev [B][H][k] int32 are device buffers; `step` is a host
  * counter that the library increments on every successful step (0 before

@@ -67,7 +67,7 @@ struct AttnCfg {
   static constexpr int S = kAttnNC * R;            // ring depth
   static constexpr int kSmem = S * kStageBytes + 1024;   // + 1 KiB to align the ring
   static constexpr int kStatic = kAttnNC * G * kD * 4 + kAttnMaxQ * kAttnNC * G * 8 +
-                                 kAttnNC * kAttnIds * 4 + S * 20 + 64;
+                                 kAttnNC * kAttnIds * 4 + S * 24 + 64;
   static_assert(kAttnCPS * (kSmem + kStatic + 1024) <= kSmemPerSM, "CTAs per SM must fit");
   static_assert(CPP * C == P && NB * 8 == C && KP * 16 == C && R >= 2, "chunk tiling");
 };
@@ -93,15 +93,27 @@ __device__ __forceinline__ bool attn_unit_active(const uint8_t *filter, int filt
 //        residual rides in columns h + 4 of the same MMA (the output of head
 //        h is then column h plus column h + 4); for G = 8 it takes a second
 //        MMA.
+// nv: tokens of the chunk that exist (C except in the partial last page of
+// a sequence): the scores of the others become -inf and their V rows zero,
+// so stale rows can contribute neither weight nor NaN.
 template <int G, int P>
 __device__ __forceinline__ void attn_chunk(uint32_t kb, const uint32_t (&qb)[8][2],
                                            float scale_log2, float (&m_run)[2], float (&l_run)[2],
-                                           float (&o)[8][4], int lane) {
+                                           float (&o)[8][4], int lane, int nv) {
   using Cfg = AttnCfg<G, P>;
   constexpr int HALF = Cfg::kHalf, MT = Cfg::C / 16;
   constexpr bool kPair = G <= 4;
-  const int tq = lane & 3, mi = lane >> 3, mr = lane & 7;
+  const int gq = lane >> 2, tq = lane & 3, mi = lane >> 3, mr = lane & 7;
   const uint32_t vb = kb + 2 * HALF;
+  if (nv < Cfg::C) {  // zero V rows nv .. C-1 of both channel halves (16 bytes a lane-store)
+    for (int x = lane; x < (Cfg::C - nv) * 16; x += 32) {
+      const int row = nv + (x >> 4), half = (x >> 3) & 1, chunk = x & 7;
+      asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vb + half * HALF + row * 128 + chunk * 16),
+                   "r"(0u)
+                   : "memory");
+    }
+    __syncwarp();
+  }
   // ---- S^T, even and odd channel k-steps in separate accumulators
   float st[MT][4], su[MT][4];
 #pragma unroll
@@ -124,7 +136,10 @@ __device__ __forceinline__ void attn_chunk(uint32_t kb, const uint32_t (&qb)[8][
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) st[mt][e] = (st[mt][e] + su[mt][e]) * scale_log2;
+    for (int e = 0; e < 4; ++e) {
+      st[mt][e] = (st[mt][e] + su[mt][e]) * scale_log2;
+      if (16 * mt + gq + 8 * (e >> 1) >= nv) st[mt][e] = -INFINITY;  // no such token
+    }
     mx0 = fmaxf(mx0, fmaxf(st[mt][0], st[mt][2]));
     mx1 = fmaxf(mx1, fmaxf(st[mt][1], st[mt][3]));
   }
@@ -208,7 +223,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
                     const __grid_constant__ CUtensorMap tmap_v, const uint16_t *__restrict__ q,
                     const int32_t *__restrict__ sel_phys, int H, int k, int n_phys, int Q,
                     float scale_log2, const uint8_t *__restrict__ filter, int filter_mode,
-                    float *__restrict__ out) {
+                    float *__restrict__ out, const int32_t *__restrict__ seq_len,
+                    const int32_t *__restrict__ page_table, int N) {
   using Cfg = AttnCfg<G, P>;
   constexpr int NC = kAttnNC, CPP = Cfg::CPP, HALF = Cfg::kHalf, R = Cfg::R, S = Cfg::S;
   constexpr int kIdRounds = kAttnIds / 32;
@@ -218,6 +234,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
   const uint32_t ring = smem_addr(smem);
   __shared__ __align__(8) uint64_t full[S], empty[S];
   __shared__ int s_ok[S];
+  __shared__ int s_nv[S];  // tokens of the stage's chunk that exist
   __shared__ int s_ids[NC][kAttnIds];  // page ids of the first kAttnIds chunks of each worker
   // partials of the cluster's workers for this CTA's channel slice:
   // [worker][head][channel of the slice], and (m, l) per worker and head
@@ -284,6 +301,17 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
         for (int r = 0; r < kIdRounds; ++r) s_ids[w][lane + 32 * r] = idv[w][r];
     }
     __syncwarp();
+    // with lengths, only the sequence's last page can be partial: its
+    // physical id and written tokens (-1 ids are padding, skipped silently)
+    int last_phys = -2, last_nt = P;
+    if (seq_len) {
+      const int L = seq_len[b];
+      if (L > 0) {
+        const int pl = (L - 1) / P;
+        last_phys = pl < N ? __ldg(page_table + static_cast<size_t>(b) * N + pl) : -2;
+        last_nt = L - pl * P;
+      }
+    }
     // lane w (< NC) feeds consumer warp w: the worker's chunks go to its R
     // stages in turn
     const bool feeder = lane < NC;
@@ -301,8 +329,11 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
         if (i < R || mbar_test_wait(&empty[s], static_cast<uint32_t>((i / R - 1) & 1))) {
           const int pos = a + i;
           const int id = i < kAttnIds ? s_ids[lane][i] : __ldg(sel_u + pos / CPP);
-          const bool ok = id >= 0 && id < n_phys;
+          const int nv = id == last_phys ? min(Cfg::C, max(0, last_nt - (pos % CPP) * Cfg::C))
+                                         : Cfg::C;
+          const bool ok = id >= 0 && id < n_phys && nv > 0;
           s_ok[s] = ok ? 1 : 0;
+          s_nv[s] = nv;
           if (ok) {
             uint8_t *dst = smem + s * Cfg::kStageBytes;
             const int row = id * P + (pos % CPP) * Cfg::C;
@@ -312,7 +343,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
             tma_load_3d(dst + 2 * HALF, &tmap_v, &full[s], 0, g, row);
             tma_load_3d(dst + 3 * HALF, &tmap_v, &full[s], 64, g, row);
           } else {
-            set_status(KVR_ST_BAD_INDEX);
+            if (nv > 0 && !(seq_len && id == -1)) set_status(KVR_ST_BAD_INDEX);
             mbar_arrive(&full[s]);
           }
           ++i;
@@ -365,7 +396,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
           s_abort = 1;
         }
       }
-      if (have) attn_chunk<G, P>(ring + s * Cfg::kStageBytes, qb, scale_log2, m_run, l_run, o, lane);
+      if (have)
+        attn_chunk<G, P>(ring + s * Cfg::kStageBytes, qb, scale_log2, m_run, l_run, o, lane, s_nv[s]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }

@@ -92,6 +92,12 @@ struct AttnWs {
   uint32_t *reserved;  // the attention keeps its split partials on chip
 };
 
+// Per-sequence lengths for the attention (seq_len null: every page full).
+struct AttnLen {
+  const int32_t *seq_len = nullptr;
+  const int32_t *page_table = nullptr;
+};
+
 size_t select_ws_bytes(const kvr_dims *d) {
   const size_t units = static_cast<size_t>(d->batch) * d->n_kv_heads;
   return align_up(units * d->n_pages * sizeof(float)) + align_up(units * sizeof(uint32_t));
@@ -234,7 +240,8 @@ int sm_count(int *out);
 template <int G>
 int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
                     const int32_t *ptab, int k, SelectWs w, int32_t *sel, int32_t *sel_phys,
-                    float *scores, const SpecArgs &spec, cudaStream_t st, bool pdl_first) {
+                    float *scores, const SpecArgs &spec, cudaStream_t st, bool pdl_first,
+                    const int32_t *seq_len) {
   // 1. page scores: kScCPS CTAs per SM, each warp a worker over a contiguous
   //    range of the flat page list
   auto kern = k_page_scores<G>;
@@ -282,39 +289,41 @@ int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
   if (d->n_pages <= 256 * 4) {
     cfg.blockDim = dim3(256);
     e = cudaLaunchKernelEx(&cfg, k_topk<G, 256, 4>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
-                           sel, sel_phys, spec);
+                           sel, sel_phys, spec, seq_len, d->page_size);
   } else if (d->n_pages <= 256 * 8) {
     cfg.blockDim = dim3(256);
     e = cudaLaunchKernelEx(&cfg, k_topk<G, 256, 8>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
-                           sel, sel_phys, spec);
+                           sel, sel_phys, spec, seq_len, d->page_size);
   } else if (d->n_pages <= 512 * 8) {
     cfg.blockDim = dim3(512);
     e = cudaLaunchKernelEx(&cfg, k_topk<G, 512, 8>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
-                           sel, sel_phys, spec);
+                           sel, sel_phys, spec, seq_len, d->page_size);
   } else if (d->n_pages <= 512 * 16) {
     cfg.blockDim = dim3(512);
     e = cudaLaunchKernelEx(&cfg, k_topk<G, 512, 16>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
-                           sel, sel_phys, spec);
+                           sel, sel_phys, spec, seq_len, d->page_size);
   } else {
     cfg.blockDim = dim3(1024);
     static_assert(1024 * 16 >= kMaxPages, "the largest top-k launch covers every page count");
     e = cudaLaunchKernelEx(&cfg, k_topk<G, 1024, 16>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
-                           sel, sel_phys, spec);
+                           sel, sel_phys, spec, seq_len, d->page_size);
   }
   if (e != cudaSuccess) return cuda_fail(e, "k_topk");
   return KVR_OK;
 }
 
 // pdl_first: launch the scoring kernel as a programmatic dependent launch
-// (false right after an event wait on the stream)
+// (false right after an event wait on the stream); seq_len (may be null):
+// rank only the pages each sequence has started
 int launch_select(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
                   const int32_t *ptab, int k, SelectWs w, int32_t *sel, int32_t *sel_phys,
-                  float *scores, const SpecArgs &spec, cudaStream_t st, bool pdl_first = true) {
+                  float *scores, const SpecArgs &spec, cudaStream_t st, bool pdl_first = true,
+                  const int32_t *seq_len = nullptr) {
   switch (d->n_q_heads / d->n_kv_heads) {
-    case 1: return launch_select_g<1>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first);
-    case 2: return launch_select_g<2>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first);
-    case 4: return launch_select_g<4>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first);
-    default: return launch_select_g<8>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first);
+    case 1: return launch_select_g<1>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len);
+    case 2: return launch_select_g<2>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len);
+    case 4: return launch_select_g<4>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len);
+    default: return launch_select_g<8>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len);
   }
 }
 
@@ -379,7 +388,7 @@ template <int G, int P>
 int launch_attn_gp(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &tv,
                    const uint16_t *q, const int32_t *sel_phys, int k, int n_phys, float scale,
                    const uint8_t *filter, int filter_mode, AttnWs w, float *out, cudaStream_t st,
-                   bool pdl_ok) {
+                   bool pdl_ok, AttnLen len) {
   (void)w;
   using Cfg = AttnCfg<G, P>;
   const long long units = static_cast<long long>(d->batch) * d->n_kv_heads;
@@ -411,7 +420,8 @@ int launch_attn_gp(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &
   cfg.attrs = attr;
   cfg.numAttrs = pdl_ok ? 2 : 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tk, tv, q, sel_phys, d->n_kv_heads, k,
-                                           n_phys, Q, scale_log2, filter, filter_mode, out);
+                                           n_phys, Q, scale_log2, filter, filter_mode, out,
+                                           len.seq_len, len.page_table, d->n_pages);
   if (e != cudaSuccess) return cuda_fail(e, "k_sparse_decode");
   return KVR_OK;
 }
@@ -420,17 +430,17 @@ template <int G>
 int launch_attn_g(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &tv,
                   const uint16_t *q, const int32_t *sel_phys, int k, int n_phys, float scale,
                   const uint8_t *filter, int filter_mode, AttnWs w, float *out, cudaStream_t st,
-                  bool pdl_ok) {
+                  bool pdl_ok, AttnLen len) {
   switch (d->page_size) {
     case 16:
       return launch_attn_gp<G, 16>(d, tk, tv, q, sel_phys, k, n_phys, scale, filter, filter_mode,
-                                   w, out, st, pdl_ok);
+                                   w, out, st, pdl_ok, len);
     case 32:
       return launch_attn_gp<G, 32>(d, tk, tv, q, sel_phys, k, n_phys, scale, filter, filter_mode,
-                                   w, out, st, pdl_ok);
+                                   w, out, st, pdl_ok, len);
     default:
       return launch_attn_gp<G, 64>(d, tk, tv, q, sel_phys, k, n_phys, scale, filter, filter_mode,
-                                   w, out, st, pdl_ok);
+                                   w, out, st, pdl_ok, len);
   }
 }
 
@@ -439,7 +449,7 @@ int launch_attn_g(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &t
 int launch_attn(const kvr_dims *d, const uint16_t *q, const uint16_t *k_pool,
                 const uint16_t *v_pool, int64_t n_phys, const int32_t *sel_phys, int k,
                 float scale, const uint8_t *filter, int filter_mode, AttnWs w, float *out,
-                cudaStream_t st, bool pdl_ok = true) {
+                cudaStream_t st, bool pdl_ok = true, AttnLen len = AttnLen()) {
   CUtensorMap tk, tv;
   int rc = make_pool_map(&tk, k_pool, d, n_phys);
   if (rc) return rc;
@@ -448,10 +458,10 @@ int launch_attn(const kvr_dims *d, const uint16_t *q, const uint16_t *k_pool,
   if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(kD));
   const int np = static_cast<int>(n_phys);
   switch (d->n_q_heads / d->n_kv_heads) {
-    case 1: return launch_attn_g<1>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok);
-    case 2: return launch_attn_g<2>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok);
-    case 4: return launch_attn_g<4>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok);
-    default: return launch_attn_g<8>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok);
+    case 1: return launch_attn_g<1>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
+    case 2: return launch_attn_g<2>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
+    case 4: return launch_attn_g<4>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
+    default: return launch_attn_g<8>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
   }
 }
 
@@ -549,34 +559,74 @@ size_t kvr_workspace_size(const kvr_dims *dims, int32_t top_k, int32_t op) {
   }
 }
 
-int kvr_build_summaries(const kvr_dims *dims, const uint16_t *k_pool, const int32_t *page_table,
-                        uint16_t *summ, void *stream) {
+static int build_summaries_impl(const kvr_dims *dims, const uint16_t *k_pool,
+                                const int32_t *page_table, const int32_t *seq_len,
+                                uint16_t *summ, void *stream) {
   int rc = check_dims(dims);
   if (rc) return rc;
   if (!k_pool || !page_table || !summ) return KVR_ERR_INVALID_ARG;
-  if (!aligned16(k_pool) || !aligned16(page_table) || !aligned16(summ)) return KVR_ERR_ALIGN;
+  if (!aligned16(k_pool) || !aligned16(page_table) || !aligned16(summ) ||
+      (seq_len && !aligned16(seq_len)))
+    return KVR_ERR_ALIGN;
   const int cols = dims->n_kv_heads * 16;
   const int ppc = cols >= kSumThreads ? 1 : kSumThreads / cols;
   const dim3 grid((dims->n_pages + ppc - 1) / ppc, dims->batch);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (dims->page_size) {
     case 16:
-      k_build_summaries<16><<<grid, kSumThreads, 0, st>>>(k_pool, page_table, summ,
+      k_build_summaries<16><<<grid, kSumThreads, 0, st>>>(k_pool, page_table, seq_len, summ,
                                                           dims->n_kv_heads, dims->n_pages,
                                                           dims->n_phys_pages, ppc);
       break;
     case 32:
-      k_build_summaries<32><<<grid, kSumThreads, 0, st>>>(k_pool, page_table, summ,
+      k_build_summaries<32><<<grid, kSumThreads, 0, st>>>(k_pool, page_table, seq_len, summ,
                                                           dims->n_kv_heads, dims->n_pages,
                                                           dims->n_phys_pages, ppc);
       break;
     default:
-      k_build_summaries<64><<<grid, kSumThreads, 0, st>>>(k_pool, page_table, summ,
+      k_build_summaries<64><<<grid, kSumThreads, 0, st>>>(k_pool, page_table, seq_len, summ,
                                                           dims->n_kv_heads, dims->n_pages,
                                                           dims->n_phys_pages, ppc);
       break;
   }
   return check_launch("k_build_summaries");
+}
+
+int kvr_build_summaries(const kvr_dims *dims, const uint16_t *k_pool, const int32_t *page_table,
+                        uint16_t *summ, void *stream) {
+  return build_summaries_impl(dims, k_pool, page_table, nullptr, summ, stream);
+}
+
+int kvr_build_summaries_len(const kvr_dims *dims, const uint16_t *k_pool,
+                            const int32_t *page_table, const int32_t *seq_len, uint16_t *summ,
+                            void *stream) {
+  if (!seq_len) return KVR_ERR_INVALID_ARG;
+  return build_summaries_impl(dims, k_pool, page_table, seq_len, summ, stream);
+}
+
+int kvr_append_kv(const kvr_dims *dims, const uint16_t *k_new, const uint16_t *v_new,
+                  const int32_t *page_table, int32_t *seq_len, uint16_t *k_pool,
+                  uint16_t *v_pool, uint16_t *summ, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (!k_new || !v_new || !page_table || !seq_len || !k_pool || !v_pool || !summ)
+    return KVR_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(page_table) || !aligned16(seq_len) ||
+      !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(summ))
+    return KVR_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const dim3 grid(dims->batch);
+#define KVR_APPEND(PP)                                                                        \
+  k_append<PP><<<grid, kAppendThreads, 0, st>>>(k_new, v_new, page_table, seq_len, k_pool,    \
+                                                v_pool, summ, dims->n_kv_heads, dims->n_pages, \
+                                                dims->n_phys_pages)
+  switch (dims->page_size) {
+    case 16: KVR_APPEND(16); break;
+    case 32: KVR_APPEND(32); break;
+    default: KVR_APPEND(64); break;
+  }
+#undef KVR_APPEND
+  return check_launch("k_append");
 }
 
 int kvr_select_pages(const kvr_dims *dims, const uint16_t *q, const uint16_t *summ,
@@ -609,6 +659,47 @@ int kvr_sparse_decode_attn(const kvr_dims *dims, const uint16_t *q, const uint16
   return launch_attn(dims, q, k_pool, v_pool, dims->n_phys_pages, sel_phys, top_k, scale, nullptr,
                      0, carve_attn(dims, top_k, (uint8_t *)ws), out,
                      static_cast<cudaStream_t>(stream));
+}
+
+int kvr_select_pages_len(const kvr_dims *dims, const uint16_t *q, const uint16_t *summ,
+                         const int32_t *page_table, const int32_t *seq_len, int32_t top_k,
+                         int32_t *sel, int32_t *sel_phys, float *scores_opt, void *ws,
+                         size_t ws_bytes, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_topk(dims, top_k))) return rc;
+  if (!q || !summ || !page_table || !seq_len || !sel) return KVR_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(summ) || !aligned16(page_table) || !aligned16(seq_len) ||
+      !aligned16(sel) || (sel_phys && !aligned16(sel_phys)) ||
+      (scores_opt && !aligned16(scores_opt)))
+    return KVR_ERR_ALIGN;
+  if ((rc = check_ws(ws, ws_bytes, select_ws_bytes(dims)))) return rc;
+  return launch_select(dims, q, summ, page_table, top_k, carve_select(dims, (uint8_t *)ws), sel,
+                       sel_phys, scores_opt, no_spec(), static_cast<cudaStream_t>(stream), true,
+                       seq_len);
+}
+
+int kvr_sparse_decode_attn_len(const kvr_dims *dims, const uint16_t *q, const uint16_t *k_pool,
+                               const uint16_t *v_pool, const int32_t *page_table,
+                               const int32_t *seq_len, const int32_t *sel_phys, int32_t top_k,
+                               float scale, float *out, void *ws, size_t ws_bytes,
+                               void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_topk(dims, top_k))) return rc;
+  if (!q || !k_pool || !v_pool || !page_table || !seq_len || !sel_phys || !out)
+    return KVR_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(page_table) ||
+      !aligned16(seq_len) || !aligned16(sel_phys) || !aligned16(out))
+    return KVR_ERR_ALIGN;
+  if (std::isnan(scale)) return KVR_ERR_INVALID_ARG;
+  if ((rc = check_ws(ws, ws_bytes, attn_ws_bytes(dims, top_k)))) return rc;
+  AttnLen len;
+  len.seq_len = seq_len;
+  len.page_table = page_table;
+  return launch_attn(dims, q, k_pool, v_pool, dims->n_phys_pages, sel_phys, top_k, scale, nullptr,
+                     0, carve_attn(dims, top_k, (uint8_t *)ws), out,
+                     static_cast<cudaStream_t>(stream), true, len);
 }
 
 static SpecArgs spec_args(const kvr_spec_state *st, float tau, uint8_t *corrected,

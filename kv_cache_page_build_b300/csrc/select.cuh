@@ -360,7 +360,8 @@ template <int G, int NT, int KPT>
 __global__ void __launch_bounds__(NT, 1)
     k_topk(const uint16_t *__restrict__ q, const int32_t *__restrict__ page_table, int H, int N,
            int k, const float *__restrict__ ws_scores, int32_t *__restrict__ sel_out,
-           int32_t *__restrict__ sel_phys_out, SpecArgs spec) {
+           int32_t *__restrict__ sel_phys_out, SpecArgs spec,
+           const int32_t *__restrict__ seq_len, int P) {
   constexpr int NW = NT / 32, BPT = kSelBins / NT;  // warps, bins per thread
   static_assert(NT % 32 == 0 && kSelBins % NT == 0, "bins are split evenly over the threads");
   __shared__ __align__(16) uint32_t s_hist[2][kSelBins];
@@ -373,6 +374,8 @@ __global__ void __launch_bounds__(NT, 1)
   const int Hq = H * G;
   const size_t unit = static_cast<size_t>(b) * H + g;
   const int base = warp * KPT * 32 + lane;  // page of key j: base + 32 j
+  // pages the sequence has started (all N without lengths); only these rank
+  const int Nv = seq_len ? min(N, max(0, (seq_len[b] + P - 1) / P)) : N;
 
   // Inputs of the speculative mode, loaded now and used after the top-k: the
   // query slices and the previous selection.  Safe before the wait:
@@ -394,13 +397,13 @@ __global__ void __launch_bounds__(NT, 1)
   const float *row = ws_scores + unit * N;
   float sv[KPT];
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) sv[j] = base + 32 * j < N ? __ldg(row + base + 32 * j) : 0.f;
+  for (int j = 0; j < KPT; ++j) sv[j] = base + 32 * j < Nv ? __ldg(row + base + 32 * j) : 0.f;
   uint32_t key[KPT];
   uint32_t kmn = 0xffffffffu, kmx = 0u;
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
     key[j] = score_key(sv[j]);
-    if (base + 32 * j < N) {
+    if (base + 32 * j < Nv) {
       kmn = min(kmn, key[j]);
       kmx = max(kmx, key[j]);
     }
@@ -423,7 +426,8 @@ __global__ void __launch_bounds__(NT, 1)
   }
   // invariant: `need` of the `cnt` keys in [L, R] are still to be taken;
   // every key above R is taken
-  uint32_t need = static_cast<uint32_t>(k), cnt = static_cast<uint32_t>(N);
+  const int n_take = min(k, Nv);  // keys selected in all (slots 0 .. n_take-1)
+  uint32_t need = static_cast<uint32_t>(n_take), cnt = static_cast<uint32_t>(Nv);
   int buf = 0;
 #pragma unroll 1
   while (cnt != need && L != R) {
@@ -432,7 +436,7 @@ __global__ void __launch_bounds__(NT, 1)
     uint32_t *hist = s_hist[buf];
 #pragma unroll
     for (int j = 0; j < KPT; ++j)
-      if (base + 32 * j < N && key[j] >= L && key[j] <= R)
+      if (base + 32 * j < Nv && key[j] >= L && key[j] <= R)
         atomicAdd(&hist[(key[j] - L) >> shift], 1u);
     __syncthreads();
     // thread tid owns bins [BPT tid, BPT tid + BPT); clear them for the round
@@ -565,7 +569,7 @@ __global__ void __launch_bounds__(NT, 1)
   uint32_t w_gt = 0u, w_eq = 0u;
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
-    const bool valid = base + 32 * j < N;
+    const bool valid = base + 32 * j < Nv;
     w_gt += (valid && key[j] > R) ? 1u : 0u;
     w_eq += (valid && key[j] >= L && key[j] <= R) ? 1u : 0u;
   }
@@ -590,7 +594,7 @@ __global__ void __launch_bounds__(NT, 1)
   int nsel = 0;
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {  // the ballots again, now in page order
-    const bool valid = base + 32 * j < N;
+    const bool valid = base + 32 * j < Nv;
     const bool is_gt = valid && key[j] > R, is_eq = valid && key[j] >= L && key[j] <= R;
     const uint32_t m_gt = __ballot_sync(0xffffffffu, is_gt);
     const uint32_t m_eq = __ballot_sync(0xffffffffu, is_eq);
@@ -608,6 +612,13 @@ __global__ void __launch_bounds__(NT, 1)
                                       : sel_phys_out != nullptr;
 #pragma unroll
   for (int j = 0; j < KPT; ++j) phys[j] = want_phys && pos[j] >= 0 ? __ldg(ptab + base + 32 * j) : -1;
+  // fewer started pages than k (lengths only): slots n_take .. k-1, which no
+  // selected key takes, are -1
+  if (!spec.enabled)
+    for (int i = n_take + tid; i < k; i += NT) {
+      sel_out[unit * k + i] = -1;
+      if (sel_phys_out) sel_phys_out[unit * k + i] = -1;
+    }
   if (nsel == 0) return;
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {

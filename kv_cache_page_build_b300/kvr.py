@@ -72,6 +72,10 @@ _SIGS = {
                                   _F, _P, _P, _P, _P, _P, _P, _S, _P]),
     "kvr_speculative_step_overlap": (_I, [_D, ctypes.POINTER(kvr_spec_state), _P, _P, _P, _P, _P, _I,
                                           _F, _F, _P, _P, _P, _P, _P, _P, _S, _P, _P, _P, _P]),
+    "kvr_append_kv": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "kvr_build_summaries_len": (_I, [_D, _P, _P, _P, _P, _P]),
+    "kvr_select_pages_len": (_I, [_D, _P, _P, _P, _P, _I, _P, _P, _P, _P, _S, _P]),
+    "kvr_sparse_decode_attn_len": (_I, [_D, _P, _P, _P, _P, _P, _P, _I, _F, _P, _P, _S, _P]),
     "kvr_working_set_reset": (_I, [_D, ctypes.POINTER(kvr_working_set), _P]),
     "kvr_recall_pages": (_I, [_D, ctypes.POINTER(kvr_host_kv), ctypes.POINTER(kvr_working_set),
                               _P, _P, _P, _I, _P, _P, _P]),
@@ -187,6 +191,31 @@ def kvr_speculative_step_overlap(d, st, q_t, summ, page_table, k_pool, v_pool, t
         int(top_k), float(tau), float(scale), _ptr(out), _ptr(corrected), _ptr(cbar_opt), _ptr(sel_used),
         _ptr(sel_used_phys), _ptr(ws), int(ws_bytes), _stream(stream), _stream(side_stream),
         _event(ev_decide), _event(ev_select)), "kvr_speculative_step_overlap")
+
+
+def kvr_append_kv(d, k_new, v_new, page_table, seq_len, k_pool, v_pool, summ, stream=None):
+    return _check(_lib.kvr_append_kv(_d(d), _ptr(k_new), _ptr(v_new), _ptr(page_table), _ptr(seq_len),
+                                     _ptr(k_pool), _ptr(v_pool), _ptr(summ), _stream(stream)), "kvr_append_kv")
+
+
+def kvr_build_summaries_len(d, k_pool, page_table, seq_len, summ, stream=None):
+    return _check(_lib.kvr_build_summaries_len(_d(d), _ptr(k_pool), _ptr(page_table), _ptr(seq_len),
+                                               _ptr(summ), _stream(stream)), "kvr_build_summaries_len")
+
+
+def kvr_select_pages_len(d, q, summ, page_table, seq_len, top_k, sel, sel_phys, scores_opt, ws, ws_bytes,
+                         stream=None):
+    return _check(_lib.kvr_select_pages_len(_d(d), _ptr(q), _ptr(summ), _ptr(page_table), _ptr(seq_len),
+                                            int(top_k), _ptr(sel), _ptr(sel_phys), _ptr(scores_opt), _ptr(ws),
+                                            int(ws_bytes), _stream(stream)), "kvr_select_pages_len")
+
+
+def kvr_sparse_decode_attn_len(d, q, k_pool, v_pool, page_table, seq_len, sel_phys, top_k, scale, out, ws,
+                               ws_bytes, stream=None):
+    return _check(_lib.kvr_sparse_decode_attn_len(_d(d), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table),
+                                                  _ptr(seq_len), _ptr(sel_phys), int(top_k), float(scale),
+                                                  _ptr(out), _ptr(ws), int(ws_bytes), _stream(stream)),
+                  "kvr_sparse_decode_attn_len")
 
 
 def kvr_recall_pages(d, host, wset, sel_new, protect, corrected, top_k, sel_slot_out, n_copied_opt,
