@@ -371,6 +371,26 @@ def run_gpu(args, world, rank, local):
     e2e_value, _ = aggregate(n_e2e, e2e_s, world)
     status |= kvr.kvr_get_status()
 
+    # decode-time append (kvr_append_kv), timed last: graphs of L appends into
+    # the last L token slots of cache copy 0 (its lengths set L tokens short)
+    app_len = torch.full((B,), N * P - L, dtype=torch.int32, device=dev)
+    k_rows = torch.zeros((B, H, D), dtype=torch.int16, device=dev)
+    graph_app = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_app):
+        for _ in range(L):
+            kvr.kvr_append_kv(d, k_rows, k_rows, page_table, app_len, k_pools[0], v_pools[0], summs[0])
+    app_len.fill_(N * P - L)
+    graph_app.replay()
+    torch.cuda.synchronize()
+    ta, tb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    app_len.fill_(N * P - L)
+    ta.record()
+    graph_app.replay()
+    tb.record()
+    torch.cuda.synchronize()
+    app_avg = ta.elapsed_time(tb) / 1e3 / L
+    status |= kvr.kvr_get_status()
+
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -407,6 +427,10 @@ def run_gpu(args, world, rank, local):
             "selection (k_page_scores + k_topk)": {"us": round(sel_avg * 1e6, 3) if sel_avg else None,
                                                    "bytes": summ_bytes,
                                                    "gbs": round(summ_bytes / sel_avg / 1e9, 1) if sel_avg else None},
+            "k_append (decode-time append, one token per sequence)": {
+                "us": round(app_avg * 1e6, 3), "bytes": B * H * (2 * D * 2 + 2 * 2 * D * 2),
+                "note": "latency-bound: K and V rows written and the page summary read and written per "
+                        "(sequence, KV head)"},
             "k_build_summaries": {"us": round(summ_ms * 1e3, 3), "bytes": k_bytes + summ_bytes,
                                   "gbs": round((k_bytes + summ_bytes) / (summ_ms / 1e3) / 1e9, 1),
                                   "note": "once per cache (prefill), not in the step"},
