@@ -149,3 +149,34 @@ def test_speculative_and_recall_arguments_rejected_before_launch():
     ws.k_slots = FAKE + 8
     assert lib.kvr_recall_pages(ctypes.byref(d), ctypes.byref(host), ctypes.byref(ws), FAKE, FAKE, None, 64,
                                 None, None, None) == kvr.KVR_ERR_ALIGN
+
+
+def test_append_and_length_arguments_rejected_before_launch():
+    lib = kvr.raw()
+    d = D()
+    big = 1 << 40
+    # append: every buffer is required, each 16-byte aligned
+    args = [FAKE] * 7
+    for i in range(7):
+        a = list(args)
+        a[i] = None
+        assert lib.kvr_append_kv(ctypes.byref(d), *a, None) == kvr.KVR_ERR_INVALID_ARG
+        a[i] = FAKE + 4
+        assert lib.kvr_append_kv(ctypes.byref(d), *a, None) == kvr.KVR_ERR_ALIGN
+    assert lib.kvr_append_kv(ctypes.byref(D(head_dim=64)), *args, None) == kvr.KVR_ERR_UNSUPPORTED_SHAPE
+    # summaries, selection and attention with lengths need the lengths
+    assert lib.kvr_build_summaries_len(ctypes.byref(d), FAKE, FAKE, None, FAKE, None) == kvr.KVR_ERR_INVALID_ARG
+    assert lib.kvr_build_summaries_len(ctypes.byref(d), FAKE, FAKE, FAKE + 2, FAKE, None) == kvr.KVR_ERR_ALIGN
+    assert lib.kvr_select_pages_len(ctypes.byref(d), FAKE, FAKE, FAKE, None, 8, FAKE, FAKE, None, FAKE, big,
+                                    None) == kvr.KVR_ERR_INVALID_ARG
+    assert lib.kvr_select_pages_len(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE + 4, 8, FAKE, FAKE, None, FAKE, big,
+                                    None) == kvr.KVR_ERR_ALIGN
+    assert lib.kvr_select_pages_len(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, 2000, FAKE, FAKE, None, FAKE, big,
+                                    None) == kvr.KVR_ERR_UNSUPPORTED_SHAPE
+    need = kvr.kvr_workspace_size(d, 64, kvr.KVR_OP_ATTN)
+    assert lib.kvr_sparse_decode_attn_len(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, None, FAKE, 64, 0.0, FAKE, FAKE,
+                                          need, None) == kvr.KVR_ERR_INVALID_ARG
+    assert lib.kvr_sparse_decode_attn_len(ctypes.byref(d), FAKE, FAKE, FAKE, None, FAKE, FAKE, 64, 0.0, FAKE, FAKE,
+                                          need, None) == kvr.KVR_ERR_INVALID_ARG
+    assert lib.kvr_sparse_decode_attn_len(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 0.0, FAKE, FAKE,
+                                          need - 1, None) == kvr.KVR_ERR_WORKSPACE
