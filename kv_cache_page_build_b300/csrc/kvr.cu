@@ -146,7 +146,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // shared memory with 128-byte swizzling (the attention kernel's chunk halves).
 // A tensor map is a pure function of its base address, shape and box, so
 // the encoded maps are kept in a small per-thread cache keyed by exactly
-// those (a hit can never be stale) and eager callers skip the driver call.
+// those (a hit can never be stale) and eager callers skip re-encoding.
 struct MapKey {
   int kind;
   const void *ptr;
