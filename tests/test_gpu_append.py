@@ -189,3 +189,28 @@ def test_decode_loop_append_select_attend():
         ref = oracle.attention(q, kp, vp, case.page_table, sel_gpu, seq_len=lens)
         gh.assert_attn_close(out.cpu().numpy(), ref)
     assert compared >= 24
+
+
+@pytest.mark.parametrize("n_q_heads,n_kv_heads", [(8, 8), (16, 2)], ids=["G1", "G8"])
+def test_lengths_for_other_group_sizes(n_q_heads, n_kv_heads):
+    """G = 1 (spare residual columns mostly empty) and G = 8 (the residual in
+    a second MMA) with a partial last page and a sequence shorter than k."""
+    wl = synth.custom(batch=2, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads, head_dim=128, page_size=32,
+                      n_pages=20, top_k=5)
+    case = synth.make_case(wl)
+    dc = gh.DevCase(case)
+    lens_np = np.array([300, 70], dtype=np.int32)
+    L = torch.tensor(lens_np, device="cuda")
+    summ = dev_summaries(dc, L)
+    sel_ref, _, out_ref = oracle.decode_step(case.q, case.k_pool, case.v_pool, case.page_table,
+                                             wl.n_kv_heads, 5, seq_len=lens_np)
+    sel = torch.full((wl.batch, wl.n_kv_heads, 5), -7, dtype=torch.int32, device="cuda")
+    sel_phys = torch.full_like(sel, -7)
+    ws = gh.workspace(dc.dims, 5, kvr.KVR_OP_SELECT)
+    kvr.kvr_select_pages_len(dc.dims, dc.q, summ, dc.page_table, L, 5, sel, sel_phys, None, ws, ws.numel())
+    np.testing.assert_array_equal(sel.cpu().numpy(), sel_ref)
+    out = torch.full((wl.batch, wl.n_q_heads, wl.head_dim), float("nan"), dtype=torch.float32, device="cuda")
+    wa = gh.workspace(dc.dims, 5, kvr.KVR_OP_ATTN)
+    kvr.kvr_sparse_decode_attn_len(dc.dims, dc.q, dc.k_pool, dc.v_pool, dc.page_table, L, sel_phys, 5, 0.0, out,
+                                   wa, wa.numel())
+    gh.assert_attn_close(out.cpu().numpy(), out_ref)
