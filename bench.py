@@ -170,28 +170,79 @@ def cpu_baseline(wl_name: str, seconds: float = 12.0):
 
 def traffic_for(kernel: str, wl_name: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
+    the kernel's current source (else None)."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{wl_name}.traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f)
-    if rec.get("source_sha256") != source_hash():
+    if rec.get("source_sha256") != kernel_source_hash(kernel):
         return None
     return rec.get("dram_bytes_per_launch")
 
 
-def source_hash() -> str:
-    """Hash of the kernel sources' code: comments and whitespace are dropped,
-    so an edit of the prose alone keeps a profile's counters current."""
+# What a kernel's DRAM traffic per launch depends on: its device code and
+# the host functions that choose its launch shape and tensor maps.
+KERNEL_SOURCES = {
+    "k_sparse_decode": (("attention.cuh", "common.cuh"),
+                        ("make_pool_map", "attn_cluster_size", "launch_attn_gp", "launch_attn_g",
+                         "launch_attn")),
+}
+
+
+def _code(text: str) -> str:
+    """C/C++ text with comments dropped and whitespace collapsed."""
     import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def _function(code: str, name: str) -> str:
+    """The definition of function `name` in collapsed code: from its return
+    type to its closing brace (the first `name(` followed by a body)."""
+    import re
+    for m in re.finditer(r"\b" + re.escape(name) + r" ?\(", code):
+        i = m.end()
+        depth = 1
+        while i < len(code) and depth:
+            depth += {"(": 1, ")": -1}.get(code[i], 0)
+            i += 1
+        j = i
+        while j < len(code) and code[j] not in "{;":
+            j += 1
+        if j >= len(code) or code[j] != "{":
+            continue                               # a call or a declaration
+        depth, k = 1, j + 1
+        while k < len(code) and depth:
+            depth += {"{": 1, "}": -1}.get(code[k], 0)
+            k += 1
+        start = code.rfind(";", 0, m.start())
+        start = max(start, code.rfind("}", 0, m.start())) + 1
+        return code[start:k]
+    raise KeyError(name)
+
+
+def kernel_source_hash(kernel: str, read=None) -> str:
+    """Hash of what the kernel's traffic depends on (KERNEL_SOURCES), plus
+    the status bits of the C header; comments and whitespace are ignored, so
+    an edit of the prose alone keeps a profile's counters current.  `read`
+    maps a repository path to its text (default: the working tree)."""
+    import re
+    if read is None:
+        def read(rel):
+            with open(os.path.join(ROOT, rel)) as f:
+                return f.read()
+    files, funcs = KERNEL_SOURCES[kernel]
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "kv_cache_page_build_b300", "csrc", "*"))):
-        with open(p) as f:
-            text = f.read()
-        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
-        text = re.sub(r"//[^\n]*", " ", text)
-        h.update(" ".join(text.split()).encode())
+    for name in files:
+        h.update(_code(read(f"kv_cache_page_build_b300/csrc/{name}")).encode())
+    host = _code(read("kv_cache_page_build_b300/csrc/kvr.cu"))
+    for fn in funcs:
+        h.update(_function(host, fn).encode())
+    for line in read("include/kvr.h").splitlines():
+        if re.match(r"#define KVR_ST_", line):
+            h.update(_code(line).encode())
     return h.hexdigest()
 
 
@@ -636,6 +687,241 @@ def run_gpu_recall(args, world, rank, local):
     }
 
 
+# ---------------------------------------------------------------- multi-layer pipeline
+
+# bf16 weight bytes one decode step reads per transformer layer: (QKV
+# projection, output projection + gated FFN); the pipeline's stand-in reads
+# as many.  Llama-3.1-8B: hidden 4096, 32/8 heads of 128, FFN 14336.
+# Qwen3-4B: hidden 2560, 32/8 heads of 128, FFN 9728.
+MODEL_BYTES = {
+    "llama3.1-8b-32k": (4096 * (4096 + 2 * 1024) * 2, (4096 * 4096 + 3 * 4096 * 14336) * 2),
+    "qwen3-4b-128k": (2560 * (4096 + 2 * 1024) * 2, (4096 * 2560 + 3 * 2560 * 9728) * 2),
+}
+MODEL_BYTES["qwen3-4b-128k-host"] = MODEL_BYTES["qwen3-4b-128k"]
+
+BREAKDOWN = (("qkv_stand_in", 0, 1), ("selection_main", 1, 2), ("attention_reused", 2, 3),
+             ("exposed_wait", 3, 4), ("attention_corrected", 4, 5), ("post_stand_in", 5, 6),
+             ("layer_total", 0, 6), ("side_stream", 7, 8), ("prefetch_stream", 9, 10))
+
+
+def run_gpu_pipeline(args, world, rank, local):
+    """A decode step through --layers attention layers with kvr_pipeline_step.
+    Each layer has its own copy of the workload's cache (in HBM, or in
+    page-locked host memory for the -host workload), its own summaries,
+    state and working set, and its own phase of the query trace; the
+    stand-in reads the model's projection weights (one buffer shared by the
+    layers, larger than L2) before and after each attention.  Timed from a
+    CUDA graph of steps; the latency breakdown comes from an eager run with
+    the pipeline's timing marks; the same layers stepped one at a time
+    (kvr_speculative_step, or kvr_speculative_step_recall, between the same
+    stand-in reads) are timed beside it."""
+    import types
+    import torch
+    from kv_cache_page_build_b300 import kvr, synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cid, tid = WORKLOADS[args.workload]
+    host_mode = args.workload.endswith("-host")
+    wl_trace = synth.WORKLOADS[tid]
+    case = synth.make_case(cid)
+    tr = synth.make_trace(wl_trace, case)
+    wl = case.wl
+    B, Hq, H, D, P, N, k = (wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.page_size, wl.n_pages,
+                            wl.top_k)
+    S, nL, tau = 2 * k, args.layers, wl_trace.tau
+    d = kvr.kvr_dims(**wl.dims())
+    qs = torch.from_numpy(tr.q.view(np.int16).copy()).to(dev)
+    T = qs.shape[0]
+    page_table = torch.from_numpy(case.page_table).to(dev)
+    k0 = torch.from_numpy(case.k_pool.view(np.int16)).to(dev)
+    summ0 = torch.empty((B, H, N, 2, D), dtype=torch.int16, device=dev)
+    kvr.kvr_build_summaries(d, k0, page_table, summ0)
+    torch.cuda.synchronize()
+    if host_mode:
+        del k0
+        kh, vh = synth.host_hnd(case)
+        caches = [(torch.from_numpy(kh.view(np.int16)).pin_memory(), torch.from_numpy(vh.view(np.int16)).pin_memory())
+                  for _ in range(nL)]
+        del kh, vh
+    else:
+        v0 = torch.from_numpy(case.v_pool.view(np.int16)).to(dev)
+        caches = [(k0.clone(), v0.clone()) for _ in range(nL)]
+        del k0, v0
+    del case
+    summs = [summ0.clone() for _ in range(nL)]
+    del summ0
+    qkv_b, post_b = MODEL_BYTES[args.workload]
+    weights = torch.randint(-2 ** 31, 2 ** 31 - 1, ((qkv_b + post_b) // 4,), dtype=torch.int32, device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    compute = kvr.stand_in(weights, qkv_b, post_b, sink)
+    # one workspace for the pipeline's layers (it orders their uses) and one for the sequential run
+    ws = torch.zeros(kvr.kvr_workspace_size(d, k, kvr.KVR_OP_STEP), dtype=torch.uint8, device=dev)
+    ws_seq = torch.zeros_like(ws)
+
+    def events(n, timing=False):
+        evs = [torch.cuda.Event(enable_timing=timing) for _ in range(n)]
+        for e in evs:
+            e.record()
+        return evs
+
+    def make_layer(i):
+        o = types.SimpleNamespace(summ=summs[i])
+        o.q_prev = torch.zeros((B, Hq, D), dtype=torch.int16, device=dev)
+        o.sel_prev = torch.zeros((B, H, k), dtype=torch.int32, device=dev)
+        o.st = kvr.kvr_spec_state(o.q_prev.data_ptr(), o.sel_prev.data_ptr(), 0)
+        o.out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+        o.corrected = torch.empty((B, H), dtype=torch.uint8, device=dev)
+        o.sel_used = torch.empty((B, H, k), dtype=torch.int32, device=dev)
+        o.idx = torch.empty((B, H, k), dtype=torch.int32, device=dev)
+        o.ev = events(3)
+        o.phase = (7 * i) % T
+        if host_mode:
+            o.host = kvr.kvr_host_kv(caches[i][0].data_ptr(), caches[i][1].data_ptr())
+            o.k_slots = torch.zeros((B, S, P, H, D), dtype=torch.int16, device=dev)
+            o.v_slots = torch.zeros_like(o.k_slots)
+            o.p2s = torch.empty((B, H, N), dtype=torch.int32, device=dev)
+            o.s2p = torch.empty((B, H, S), dtype=torch.int32, device=dev)
+            o.wset = kvr.kvr_working_set(o.k_slots.data_ptr(), o.v_slots.data_ptr(), o.p2s.data_ptr(),
+                                         o.s2p.data_ptr(), S)
+            kvr.kvr_working_set_reset(d, o.wset)
+            o.n_copied = torch.zeros(1, dtype=torch.int32, device=dev)
+            o.extra = dict(host=o.host, wset=o.wset, n_copied_opt=o.n_copied)
+        else:
+            o.extra = dict(page_table=page_table, k_pool=caches[i][0], v_pool=caches[i][1])
+        return o
+
+    pipe, seq = [make_layer(i) for i in range(nL)], [make_layer(i) for i in range(nL)]
+    side, pf = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def pipe_step(i, marks=None):
+        io = [kvr.layer(o.st, qs[(i + o.phase) % T], o.summ, o.out, o.corrected, None, o.sel_used, o.idx, ws,
+                        ws.numel(), o.ev, **o.extra) for o in pipe]
+        kvr.kvr_pipeline_step(d, io, compute, k, tau, 0.0, torch.cuda.current_stream(), side, pf, marks)
+
+    def seq_step(i):
+        cur = torch.cuda.current_stream()
+        for o in seq:
+            q = qs[(i + o.phase) % T]
+            kvr.kvr_stand_in_read(compute, 0, qkv_b)
+            if host_mode:
+                kvr.kvr_speculative_step_recall(d, o.st, q, o.summ, o.host, o.wset, k, tau, 0.0, o.out, o.corrected,
+                                                None, o.sel_used, o.idx, o.n_copied, ws_seq, ws_seq.numel(), cur,
+                                                side, o.ev[0], o.ev[1])
+            else:
+                kvr.kvr_speculative_step(d, o.st, q, o.summ, page_table, o.extra["k_pool"], o.extra["v_pool"], k,
+                                         tau, 0.0, o.out, o.corrected, None, o.sel_used, o.idx, ws_seq,
+                                         ws_seq.numel())
+            kvr.kvr_stand_in_read(compute, qkv_b, post_b)
+
+    def join():
+        for o in pipe:
+            torch.cuda.current_stream().wait_event(o.ev[2])
+
+    for i in range(max(args.warmup, 3)):           # step 0 of each layer's trace phase first
+        pipe_step(i)
+        seq_step(i)
+    torch.cuda.synchronize()
+    G = 8
+
+    def capture(fn, first):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            for o in pipe:
+                o.ev[2].record()                    # the cross-step wait needs a record inside the capture
+            for i in range(first, first + G):
+                fn(i)
+            join()
+        return g
+
+    w0 = max(args.warmup, 3)
+    g_pipe, g_seq = capture(pipe_step, w0), capture(seq_step, w0)
+    g_pipe.replay()
+    g_seq.replay()
+    for o in pipe:
+        o.ev[2].record()                            # last recorded inside a capture: record it for eager steps
+    torch.cuda.synchronize()
+    reps = max(1, args.steps // G)
+
+    def timed(g):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    clocks = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or local))
+    time.sleep(0.3)
+    barrier(world)
+    t_pipe = timed(g_pipe)
+    t_seq = timed(g_seq)
+    barrier(world)
+    clk = clocks.stop()
+    n_steps = reps * G
+    value, t_max = aggregate(n_steps, t_pipe, world)
+    seq_value, t_seq_max = aggregate(n_steps, t_seq, world)
+
+    # latency breakdown: eager steps with the timing marks, per-layer means (us)
+    marks = events(nL * kvr.KVR_PIPE_MARKS, timing=True)
+    sums = {name: 0.0 for name, _, _ in BREAKDOWN}
+    M = 24
+    for i in range(M):
+        pipe_step(w0 + i, marks)
+        torch.cuda.synchronize()
+        for l in range(nL):
+            m = marks[l * kvr.KVR_PIPE_MARKS:(l + 1) * kvr.KVR_PIPE_MARKS]
+            for name, a, b in BREAKDOWN:
+                sums[name] += m[a].elapsed_time(m[b]) * 1e3
+    breakdown = {name: round(v / (M * nL), 2) for name, v in sums.items()}
+    status = kvr.kvr_get_status()
+    per_layer = 2 + (6 if host_mode else 5)       # stand-ins; decide or 2 selection kernels, recalls, attentions
+    return {
+        "metric": METRIC + "; here whole multi-layer steps",
+        "value": round(value, 2),
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": n_steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_max / n_steps * 1e3, 5),
+        "us_per_layer": round(t_max / n_steps / nL * 1e6, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{args.workload}, {nL}-layer pipeline: {B} sequences x {Hq}/{H} heads, head_dim {D}, "
+                        f"context {wl.context}, page {P}, top-k {k}; cache "
+                        + ("in page-locked host memory, recalled into a 2k-slot working set" if host_mode
+                           else "in HBM") + f"; speculative, tau {tau}; stand-in reads of {qkv_b} + {post_b} "
+                        f"bytes of projection weights per layer",
+            "layers": nL, "batch": B, "n_q_heads": Hq, "n_kv_heads": H, "head_dim": D, "context": wl.context,
+            "page_size": P, "top_k": k, "tau": tau, "stand_in_bytes": [qkv_b, post_b],
+            "parallelism": f"{world} independent replica(s)" if world > 1 else "1 GPU",
+            "l2": "each layer's cache is its own copy and the stand-in streams more than L2 between layers",
+            "graph": f"steps replayed from a CUDA graph of {G} steps",
+        },
+        "sequential": {"value": round(seq_value, 2), "unit": "steps/s",
+                       "ms_per_step": round(t_seq_max / n_steps * 1e3, 5),
+                       "how": "the same layers one call at a time: " + (
+                           "kvr_speculative_step_recall" if host_mode else "kvr_speculative_step") +
+                       " between the same stand-in reads, from a CUDA graph"},
+        "breakdown_us_per_layer": breakdown,
+        "breakdown_how": f"eager steps with the pipeline's timing marks, mean over {M} steps x {nL} layers; "
+                         "side_stream = selection (HBM) or the corrected heads' recall (host), prefetch_stream = "
+                         "the recall of the other heads' pages for the next step (host)",
+        "roofline": None,
+        "gpu_launches": per_layer * nL * n_steps,
+        "clocks": clk,
+        "device_status": status,
+    }
+
+
 # ---------------------------------------------------------------- main
 
 
@@ -648,8 +934,10 @@ def main():
     ap.add_argument("--workload", default="llama3.1-8b-32k", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--copies", type=int, default=4, help="rotating cache copies (L2-cold timing needs >= 3)")
-    ap.add_argument("--step", default="sequential", choices=["sequential", "overlap"],
-                    help="kvr_speculative_step, or kvr_speculative_step_overlap (selection on a side stream)")
+    ap.add_argument("--step", default="sequential", choices=["sequential", "overlap", "pipeline"],
+                    help="kvr_speculative_step, kvr_speculative_step_overlap (selection on a side stream), or "
+                         "kvr_pipeline_step over --layers layers with stand-in projections")
+    ap.add_argument("--layers", type=int, default=4, help="attention layers of --step pipeline")
     args = ap.parse_args()
     world, rank, local = dist_setup()
 
@@ -670,9 +958,14 @@ def main():
         print(json.dumps(line))
         return
 
-    res = (run_gpu_recall if args.workload.endswith("-host") else run_gpu)(args, world, rank, local)
+    if args.step == "pipeline":
+        res = run_gpu_pipeline(args, world, rank, local)
+    else:
+        res = (run_gpu_recall if args.workload.endswith("-host") else run_gpu)(args, world, rank, local)
     if rank == 0:
-        if world == 1 and not args.no_cpu_baseline:
+        if args.step == "pipeline":
+            res["cpu_baseline"] = None
+        elif world == 1 and not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(args.workload)
         else:
             res["cpu_baseline"] = None

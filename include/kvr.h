@@ -311,6 +311,105 @@ int kvr_speculative_step_recall(const kvr_dims *dims, kvr_spec_state *st,
                                 void *side_stream, void *ev_select,
                                 void *ev_recall);
 
+/* ---- multi-layer decode pipeline ([FreeKV] section 2.1: the selection and
+ * recall of a layer overlap that layer's attention and FFN and the next
+ * layer's QKV projection; only heads that are corrected wait for them).
+ *
+ * One attention layer of a pipeline step.  The fields are those of the
+ * single-layer calls: with host == NULL the layer's cache is HBM-resident
+ * (page_table, k_pool, v_pool; sel_used_idx receives physical page ids, as
+ * sel_used_phys of kvr_speculative_step_overlap); with host != NULL it is in
+ * host memory (host, wset; sel_used_idx receives working-set slots, as
+ * sel_used_slot of kvr_speculative_step_recall).  q is this step's query of
+ * the layer.  ev are caller-created cudaEvent_t passed as void*: ev[0] and
+ * ev[1] always, ev[2] for a host-resident layer; they carry the layer's
+ * dependencies from one pipeline step to the next, so a layer keeps its
+ * events for the whole run (layers may share them).  Workspace kind
+ * KVR_OP_STEP; layers may share one workspace. */
+typedef struct kvr_layer {
+  kvr_spec_state *st;
+  const uint16_t *q;
+  const uint16_t *summ;
+  const int32_t *page_table;
+  const uint16_t *k_pool;
+  const uint16_t *v_pool;
+  const kvr_host_kv *host;
+  const kvr_working_set *wset;
+  float *out;
+  uint8_t *corrected;
+  float *cbar_opt;
+  int32_t *sel_used;
+  int32_t *sel_used_idx;
+  uint32_t *n_copied_opt;
+  void *ws;
+  size_t ws_bytes;
+  void *ev[3];
+} kvr_layer;
+
+/* Stand-in for the rest of each transformer layer.  A decode-time projection
+ * is bound by reading its weights once, so each one is modelled by a kernel
+ * that reads the same number of bytes: before a layer's selection, bytes
+ * [0, qkv_bytes) of `weights` (the QKV projection); after its attention,
+ * bytes [qkv_bytes, qkv_bytes + post_bytes) (the output projection and the
+ * FFN).  Each read adds the 32-bit words it read, modulo 2^32, into *sink
+ * (device).  qkv_bytes and post_bytes are multiples of 16; either may be 0. */
+typedef struct kvr_stand_in {
+  const void *weights;
+  uint64_t qkv_bytes;
+  uint64_t post_bytes;
+  uint32_t *sink;
+} kvr_stand_in;
+
+/* One stand-in read on its own, on `stream`: bytes [offset, offset + bytes)
+ * of compute->weights, summed into compute->sink (as the pipeline's reads;
+ * for running the same model without the pipeline).  offset and bytes are
+ * multiples of 16. */
+int kvr_stand_in_read(const kvr_stand_in *compute, uint64_t offset,
+                      uint64_t bytes, void *stream);
+
+/* Events a pipeline step records per layer when `marks` is given (index
+ * layer * KVR_PIPE_MARKS + m), for a latency breakdown by
+ * cudaEventElapsedTime:
+ *   0 main, layer start           1 main, after the QKV stand-in
+ *   2 main, after the selection (HBM) or speculative selection (host)
+ *   3 main, after the reused heads' attention
+ *   4 main, once the side stream's work this layer waits for is done
+ *   5 main, after the corrected heads' attention
+ *   6 main, after the output/FFN stand-in
+ *   7, 8 side stream: start and end of the selection (HBM) or of the recall
+ *        of the corrected heads' pages (host)
+ *   9, 10 prefetch stream: start and end of the recall of the other heads'
+ *        pages for the next step (host; an HBM layer records both right after
+ *        8 on the side stream) */
+#define KVR_PIPE_MARKS 11
+
+/* One decode step through n_layers attention layers, in layer order.  Per
+ * layer, on `stream`: the QKV stand-in (if compute != NULL), then
+ *   HBM-resident: the correction decision (kvr_speculative_step_overlap's
+ *     first part), the selection on `side_stream`, the reused heads'
+ *     attention beside it, a wait for the selection, the corrected heads'
+ *     attention;
+ *   host-resident: a wait for this layer's prefetch of the previous step,
+ *     the speculative selection, then on `side_stream` the recall of the
+ *     corrected heads' pages and on `prefetch_stream` (after it) the recall
+ *     of the other heads' new selection for the next step; the reused heads'
+ *     attention beside them, a wait for the first recall only, the corrected
+ *     heads' attention;
+ * then the output/FFN stand-in.  Every layer's results are bit-identical to
+ * kvr_speculative_step_overlap (HBM) or kvr_speculative_step_recall (host)
+ * called layer by layer.  Every argument of every layer is checked before
+ * anything is enqueued; a CUDA error part-way returns KVR_ERR_CUDA with the
+ * earlier layers enqueued (their st->step advanced).  marks: NULL or
+ * n_layers * KVR_PIPE_MARKS cudaEvent_t (created with timing).  A host
+ * layer's prefetch is joined to `stream` only by that layer's wait in the
+ * next step: a caller that ends a CUDA-graph capture after a step, or needs
+ * the working sets settled, first makes `stream` wait on each host layer's
+ * ev[2]. */
+int kvr_pipeline_step(const kvr_dims *dims, int32_t n_layers, kvr_layer *layers,
+                      const kvr_stand_in *compute, int32_t top_k, float tau,
+                      float scale, void *stream, void *side_stream,
+                      void *prefetch_stream, void *const *marks);
+
 /* Synchronise `stream`, then read and clear the device status word (a bit
  * set of KVR_ST_*).  Returns KVR_OK or KVR_ERR_CUDA. */
 int kvr_get_status(void *stream, uint32_t *status_out);

@@ -2,8 +2,9 @@
 //
 // Host side only: argument checks (before anything is enqueued), workspace
 // carving, tensor-map encoding for the K/V pools, kernel dispatch over the
-// supported (G, P) instances and the event wiring of the recall step.  All
-// compute is in the kernels of the included .cuh files.
+// supported (G, P) instances and the event wiring of the overlapped steps
+// and of the multi-layer pipeline.  All compute is in the kernels of the
+// included .cuh files.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -14,6 +15,7 @@
 
 #include "attention.cuh"
 #include "common.cuh"
+#include "pipeline.cuh"
 #include "recall.cuh"
 #include "select.cuh"
 #include "summaries.cuh"
@@ -480,7 +482,8 @@ int mapped_host_pointer(const void *host, void **dev) {
 
 int launch_recall(const kvr_dims *d, const kvr_host_kv *host, const kvr_working_set *wset,
                   const int32_t *sel_new, const int32_t *protect, const uint8_t *corrected,
-                  int k, int32_t *sel_slot_out, uint32_t *n_copied, cudaStream_t st) {
+                  int k, int32_t *sel_slot_out, uint32_t *n_copied, cudaStream_t st,
+                  int unit_filter = 0) {
   void *kh = nullptr, *vh = nullptr;
   int rc = mapped_host_pointer(host->k_host, &kh);
   if (rc) return rc;
@@ -492,7 +495,7 @@ int launch_recall(const kvr_dims *d, const kvr_host_kv *host, const kvr_working_
   k_recall<PP><<<grid, kRecallThreads, smem, st>>>(                                             \
       static_cast<const uint16_t *>(kh), static_cast<const uint16_t *>(vh), wset->k_slots,      \
       wset->v_slots, wset->page2slot, wset->slot2page, S, sel_new, protect, corrected,          \
-      d->n_kv_heads, d->n_pages, k, sel_slot_out, n_copied)
+      unit_filter, d->n_kv_heads, d->n_pages, k, sel_slot_out, n_copied)
   switch (d->page_size) {
     case 16: KVR_RECALL(16); break;
     case 32: KVR_RECALL(32); break;
@@ -724,11 +727,11 @@ static int spec_select_impl(const kvr_dims *dims, kvr_spec_state *st, const uint
                             const uint16_t *summ, const int32_t *page_table, int32_t top_k,
                             float tau, uint8_t *corrected, float *cbar_opt, int32_t *sel_used,
                             int32_t *sel_used_phys, const int32_t *page2slot, int n_slots,
-                            void *ws, cudaStream_t stream) {
+                            void *ws, cudaStream_t stream, bool pdl_first = true) {
   const SpecArgs s =
       spec_args(st, tau, corrected, cbar_opt, sel_used, sel_used_phys, page2slot, n_slots);
   return launch_select(dims, q_t, summ, page_table, top_k, carve_select(dims, (uint8_t *)ws),
-                       nullptr, nullptr, nullptr, s, stream);
+                       nullptr, nullptr, nullptr, s, stream, pdl_first);
 }
 
 static int check_spec(const kvr_dims *dims, const kvr_spec_state *st, const uint16_t *q_t,
@@ -912,6 +915,162 @@ int kvr_speculative_step_recall(const kvr_dims *dims, kvr_spec_state *st, const 
   if (e != cudaSuccess) return cuda_fail(e, "main stream wait");
   return launch_attn(dims, q_t, wset->k_slots, wset->v_slots, n_phys, sel_used_slot, top_k, scale,
                      corrected, 2, aw, out, s, false);
+}
+
+// ---------------------------------------------------------------- multi-layer pipeline
+
+// The stand-in for a projection: k_stand_in over `bytes` of the weights from
+// `offset` (nothing for bytes == 0 or no stand-in).
+static int launch_stand_in(const kvr_stand_in *c, uint64_t offset, uint64_t bytes,
+                           cudaStream_t st) {
+  if (!c || bytes == 0) return KVR_OK;
+  int sms = 0;
+  if (int rc = sm_count(&sms)) return rc;
+  const uint64_t n16 = bytes / 16;
+  const uint64_t want = (n16 + kStandInThreads - 1) / kStandInThreads;
+  const uint64_t cap = static_cast<uint64_t>(sms) * kStandInCPS;
+  const unsigned grid = static_cast<unsigned>(std::max<uint64_t>(1, std::min(want, cap)));
+  const uint8_t *base = static_cast<const uint8_t *>(c->weights) + offset;
+  k_stand_in<<<grid, kStandInThreads, 0, st>>>(reinterpret_cast<const uint4 *>(base), n16, c->sink);
+  return check_launch("k_stand_in");
+}
+
+static int check_stand_in(const kvr_stand_in *c) {
+  if (!c->weights || !c->sink) return KVR_ERR_INVALID_ARG;
+  if ((c->qkv_bytes | c->post_bytes) & 15u) return KVR_ERR_INVALID_ARG;
+  if (c->qkv_bytes > UINT64_MAX - c->post_bytes) return KVR_ERR_INVALID_ARG;
+  if (!aligned16(c->weights) || (reinterpret_cast<uintptr_t>(c->sink) & 3u)) return KVR_ERR_ALIGN;
+  return KVR_OK;
+}
+
+int kvr_stand_in_read(const kvr_stand_in *compute, uint64_t offset, uint64_t bytes, void *stream) {
+  if (!compute) return KVR_ERR_INVALID_ARG;
+  int rc = check_stand_in(compute);
+  if (rc) return rc;
+  if ((offset | bytes) & 15u || offset > UINT64_MAX - bytes) return KVR_ERR_INVALID_ARG;
+  return launch_stand_in(compute, offset, bytes, static_cast<cudaStream_t>(stream));
+}
+
+static int check_layer(const kvr_dims *dims, const kvr_layer &L, int32_t top_k, float tau) {
+  int rc = check_spec(dims, L.st, L.q, L.summ, L.corrected, L.cbar_opt, L.sel_used, tau);
+  if (rc) return rc;
+  if (!L.out || !L.sel_used_idx || !L.ev[0] || !L.ev[1]) return KVR_ERR_INVALID_ARG;
+  if (!aligned16(L.out) || !aligned16(L.sel_used_idx)) return KVR_ERR_ALIGN;
+  if (L.host) {
+    if ((rc = check_wset(dims, L.wset, top_k))) return rc;
+    if (!L.host->k_host || !L.host->v_host || !L.ev[2]) return KVR_ERR_INVALID_ARG;
+    if (!aligned16(L.host->k_host) || !aligned16(L.host->v_host)) return KVR_ERR_ALIGN;
+  } else {
+    if (!L.page_table || !L.k_pool || !L.v_pool) return KVR_ERR_INVALID_ARG;
+    if (!aligned16(L.page_table) || !aligned16(L.k_pool) || !aligned16(L.v_pool))
+      return KVR_ERR_ALIGN;
+  }
+  return check_ws(L.ws, L.ws_bytes, select_ws_bytes(dims) + attn_ws_bytes(dims, top_k));
+}
+
+int kvr_pipeline_step(const kvr_dims *dims, int32_t n_layers, kvr_layer *layers,
+                      const kvr_stand_in *compute, int32_t top_k, float tau, float scale,
+                      void *stream, void *side_stream, void *prefetch_stream,
+                      void *const *marks) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_topk(dims, top_k))) return rc;
+  if (n_layers <= 0 || !layers || std::isnan(scale)) return KVR_ERR_INVALID_ARG;
+  if (compute && (rc = check_stand_in(compute))) return rc;
+  for (int l = 0; l < n_layers; ++l)
+    if ((rc = check_layer(dims, layers[l], top_k, tau))) return rc;
+  if (marks)
+    for (int64_t i = 0; i < static_cast<int64_t>(n_layers) * KVR_PIPE_MARKS; ++i)
+      if (!marks[i]) return KVR_ERR_INVALID_ARG;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStream_t side = static_cast<cudaStream_t>(side_stream);
+  cudaStream_t pf = static_cast<cudaStream_t>(prefetch_stream);
+  auto record = [](void *ev, cudaStream_t st) {
+    const cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(ev), st);
+    return e == cudaSuccess ? KVR_OK : cuda_fail(e, "pipeline event record");
+  };
+  auto wait = [](cudaStream_t st, void *ev) {
+    const cudaError_t e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(ev), 0);
+    return e == cudaSuccess ? KVR_OK : cuda_fail(e, "pipeline stream wait");
+  };
+  auto mark = [&](int l, int m, cudaStream_t st) {
+    return marks ? record(marks[static_cast<int64_t>(l) * KVR_PIPE_MARKS + m], st) : KVR_OK;
+  };
+  const uint64_t qkv = compute ? compute->qkv_bytes : 0;
+  const uint64_t post = compute ? compute->post_bytes : 0;
+#define KVR_TRY(x) \
+  if ((rc = (x))) return rc
+  for (int l = 0; l < n_layers; ++l) {
+    kvr_layer &L = layers[l];
+    const AttnWs aw = carve_attn(dims, top_k, static_cast<uint8_t *>(L.ws) + select_ws_bytes(dims));
+    KVR_TRY(mark(l, 0, s));
+    KVR_TRY(launch_stand_in(compute, 0, qkv, s));
+    KVR_TRY(mark(l, 1, s));
+    if (!L.host) {
+      // the decision on the main stream, the selection beside the reused
+      // heads' attention (as kvr_speculative_step_overlap)
+      SpecArgs sa = spec_args(L.st, tau, L.corrected, L.cbar_opt, L.sel_used, L.sel_used_idx,
+                              nullptr, 0);
+      KVR_TRY(launch_spec_decide(dims, L.q, L.page_table, top_k, sa, s));
+      L.st->step += 1;
+      KVR_TRY(mark(l, 2, s));
+      KVR_TRY(record(L.ev[0], s));
+      KVR_TRY(wait(side, L.ev[0]));
+      KVR_TRY(mark(l, 7, side));
+      sa.decided = 1;
+      KVR_TRY(launch_select(dims, L.q, L.summ, L.page_table, top_k,
+                            carve_select(dims, static_cast<uint8_t *>(L.ws)), nullptr, nullptr,
+                            nullptr, sa, side, false));
+      KVR_TRY(mark(l, 8, side));
+      KVR_TRY(record(L.ev[1], side));
+      KVR_TRY(mark(l, 9, side));
+      KVR_TRY(mark(l, 10, side));
+      KVR_TRY(launch_attn(dims, L.q, L.k_pool, L.v_pool, dims->n_phys_pages, L.sel_used_idx, top_k,
+                          scale, L.corrected, 1, aw, L.out, s));
+      KVR_TRY(mark(l, 3, s));
+      KVR_TRY(wait(s, L.ev[1]));
+      KVR_TRY(mark(l, 4, s));
+      KVR_TRY(launch_attn(dims, L.q, L.k_pool, L.v_pool, dims->n_phys_pages, L.sel_used_idx, top_k,
+                          scale, L.corrected, 2, aw, L.out, s, false));
+    } else {
+      // this layer's maps and slots as the previous step's prefetch left them
+      KVR_TRY(wait(s, L.ev[2]));
+      KVR_TRY(spec_select_impl(dims, L.st, L.q, L.summ, nullptr, top_k, tau, L.corrected,
+                               L.cbar_opt, L.sel_used, L.sel_used_idx, L.wset->page2slot,
+                               L.wset->n_slots, L.ws, s, false));
+      L.st->step += 1;
+      KVR_TRY(mark(l, 2, s));
+      KVR_TRY(record(L.ev[0], s));
+      // side stream: the pages the corrected heads need now
+      KVR_TRY(wait(side, L.ev[0]));
+      KVR_TRY(mark(l, 7, side));
+      KVR_TRY(launch_recall(dims, L.host, L.wset, L.st->sel_prev, L.sel_used, L.corrected, top_k,
+                            L.sel_used_idx, L.n_copied_opt, side, 2));
+      KVR_TRY(mark(l, 8, side));
+      KVR_TRY(record(L.ev[1], side));
+      // prefetch stream, after it: the other heads' new selection (next step)
+      KVR_TRY(wait(pf, L.ev[1]));
+      KVR_TRY(mark(l, 9, pf));
+      KVR_TRY(launch_recall(dims, L.host, L.wset, L.st->sel_prev, L.sel_used, L.corrected, top_k,
+                            L.sel_used_idx, L.n_copied_opt, pf, 1));
+      KVR_TRY(mark(l, 10, pf));
+      KVR_TRY(record(L.ev[2], pf));
+      const int64_t n_phys = static_cast<int64_t>(dims->batch) * L.wset->n_slots;
+      KVR_TRY(launch_attn(dims, L.q, L.wset->k_slots, L.wset->v_slots, n_phys, L.sel_used_idx,
+                          top_k, scale, L.corrected, 1, aw, L.out, s, false));
+      KVR_TRY(mark(l, 3, s));
+      KVR_TRY(wait(s, L.ev[1]));
+      KVR_TRY(mark(l, 4, s));
+      KVR_TRY(launch_attn(dims, L.q, L.wset->k_slots, L.wset->v_slots, n_phys, L.sel_used_idx,
+                          top_k, scale, L.corrected, 2, aw, L.out, s, false));
+    }
+    KVR_TRY(mark(l, 5, s));
+    KVR_TRY(launch_stand_in(compute, qkv, post, s));
+    KVR_TRY(mark(l, 6, s));
+  }
+#undef KVR_TRY
+  return KVR_OK;
 }
 
 int kvr_get_status(void *stream, uint32_t *status_out) {

@@ -18,6 +18,11 @@
 //            in the same pass as the transfer.
 // With n_slots >= 2k the two sets of k pages always fit: one set is read by
 // the running step while the other is being filled.
+//
+// unit_filter splits one recall into two launches over disjoint units (the
+// units never share a slot, a map entry or a page): 0 = every unit, 1 = the
+// units with corrected == 0 (the speculative prefetch for the next step),
+// 2 = the units with corrected != 0 (the pages this step still needs).
 #pragma once
 
 #include "common.cuh"
@@ -45,7 +50,7 @@ __global__ void __launch_bounds__(kRecallThreads)
              uint16_t *__restrict__ k_slots, uint16_t *__restrict__ v_slots,
              int32_t *__restrict__ page2slot, int32_t *__restrict__ slot2page, int S,
              const int32_t *__restrict__ sel_new, const int32_t *__restrict__ protect,
-             const uint8_t *__restrict__ corrected, int H, int N, int k,
+             const uint8_t *__restrict__ corrected, int unit_filter, int H, int N, int k,
              int32_t *__restrict__ sel_slot_out, uint32_t *__restrict__ n_copied) {
   extern __shared__ __align__(16) int32_t rsm[];
   int32_t *keep = rsm;               // [S]
@@ -56,6 +61,9 @@ __global__ void __launch_bounds__(kRecallThreads)
   const int tid = threadIdx.x;
   const int g = blockIdx.x, b = blockIdx.y;
   const size_t unit = static_cast<size_t>(b) * H + g;
+  if (unit_filter != 0 && corrected != nullptr &&
+      (unit_filter == 2) != (corrected[unit] != 0))
+    return;  // the whole CTA leaves before its first barrier
   int32_t *p2s = page2slot + unit * N;
   int32_t *s2p = slot2page + unit * S;
   const int32_t *sn = sel_new + unit * k;

@@ -55,6 +55,21 @@ class kvr_working_set(ctypes.Structure):
                 ("n_slots", ctypes.c_int32)]
 
 
+class kvr_layer(ctypes.Structure):
+    _fields_ = [("st", ctypes.POINTER(kvr_spec_state)), ("q", ctypes.c_void_p), ("summ", ctypes.c_void_p),
+                ("page_table", ctypes.c_void_p), ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("host", ctypes.POINTER(kvr_host_kv)), ("wset", ctypes.POINTER(kvr_working_set)),
+                ("out", ctypes.c_void_p), ("corrected", ctypes.c_void_p), ("cbar_opt", ctypes.c_void_p),
+                ("sel_used", ctypes.c_void_p), ("sel_used_idx", ctypes.c_void_p),
+                ("n_copied_opt", ctypes.c_void_p), ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t),
+                ("ev", ctypes.c_void_p * 3)]
+
+
+class kvr_stand_in(ctypes.Structure):
+    _fields_ = [("weights", ctypes.c_void_p), ("qkv_bytes", ctypes.c_uint64), ("post_bytes", ctypes.c_uint64),
+                ("sink", ctypes.c_void_p)]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int32
 _S = ctypes.c_size_t
@@ -82,6 +97,9 @@ _SIGS = {
     "kvr_speculative_step_recall": (_I, [_D, ctypes.POINTER(kvr_spec_state), _P, _P,
                                          ctypes.POINTER(kvr_host_kv), ctypes.POINTER(kvr_working_set),
                                          _I, _F, _F, _P, _P, _P, _P, _P, _P, _P, _S, _P, _P, _P, _P]),
+    "kvr_pipeline_step": (_I, [_D, _I, ctypes.POINTER(kvr_layer), ctypes.POINTER(kvr_stand_in), _I, _F, _F,
+                               _P, _P, _P, ctypes.POINTER(_P)]),
+    "kvr_stand_in_read": (_I, [ctypes.POINTER(kvr_stand_in), ctypes.c_uint64, ctypes.c_uint64, _P]),
     "kvr_get_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "kvr_select_pages_noalloc": (_I, [_D, _P, _P, _P, _I, _P, _P, _P, _P]),
     "kvr_error_string": (ctypes.c_char_p, [_I]),
@@ -239,6 +257,53 @@ def _event(e):
     if e is None or isinstance(e, int):
         return e
     return e.cuda_event
+
+
+def layer(st, q, summ, out, corrected, cbar_opt, sel_used, sel_used_idx, ws, ws_bytes, events,
+          page_table=None, k_pool=None, v_pool=None, host=None, wset=None, n_copied_opt=None) -> kvr_layer:
+    """A kvr_layer for kvr_pipeline_step: HBM-resident (page_table, k_pool,
+    v_pool) or host-resident (host, wset); `events` are two (HBM) or three
+    (host) CUDA events kept by the layer for the whole run.  The struct keeps
+    st, host and wset alive; the tensors stay the caller's."""
+    L = kvr_layer()
+    L.st = ctypes.pointer(st)
+    for name, v in (("q", q), ("summ", summ), ("page_table", page_table), ("k_pool", k_pool),
+                    ("v_pool", v_pool), ("out", out), ("corrected", corrected), ("cbar_opt", cbar_opt),
+                    ("sel_used", sel_used), ("sel_used_idx", sel_used_idx), ("n_copied_opt", n_copied_opt),
+                    ("ws", ws)):
+        setattr(L, name, _ptr(v))
+    if host is not None:
+        L.host = ctypes.pointer(host)
+        L.wset = ctypes.pointer(wset)
+    L.ws_bytes = int(ws_bytes)
+    for i, e in enumerate(events):
+        L.ev[i] = _event(e)
+    return L
+
+
+def stand_in(weights, qkv_bytes, post_bytes, sink) -> kvr_stand_in:
+    """The stand-in for the rest of each layer: reads of qkv_bytes and
+    post_bytes of `weights` (device), summed into `sink` (device uint32)."""
+    return kvr_stand_in(_ptr(weights), int(qkv_bytes), int(post_bytes), _ptr(sink))
+
+
+def kvr_stand_in_read(compute, offset, nbytes, stream=None):
+    return _check(_lib.kvr_stand_in_read(ctypes.byref(compute), int(offset), int(nbytes), _stream(stream)),
+                  "kvr_stand_in_read")
+
+
+def kvr_pipeline_step(d, layers, compute, top_k, tau, scale, stream, side_stream, prefetch_stream, marks=None):
+    """One decode step through len(layers) layers (a list of kvr_layer);
+    `compute` a kvr_stand_in or None; `marks` None or
+    len(layers) * KVR_PIPE_MARKS timing events, recorded once beforehand."""
+    arr = (kvr_layer * len(layers))(*layers)
+    mk = None
+    if marks is not None:
+        mk = (_P * len(marks))(*[_event(m) for m in marks])
+    rc = _lib.kvr_pipeline_step(_d(d), len(layers), arr, ctypes.byref(compute) if compute is not None else None,
+                                int(top_k), float(tau), float(scale), _stream(stream), _stream(side_stream),
+                                _stream(prefetch_stream), mk)
+    return _check(rc, "kvr_pipeline_step")
 
 
 def kvr_select_pages_noalloc(d, q, summ, page_table, top_k, sel, sel_phys, scores_opt, stream=None):

@@ -180,3 +180,62 @@ def test_append_and_length_arguments_rejected_before_launch():
                                           need, None) == kvr.KVR_ERR_INVALID_ARG
     assert lib.kvr_sparse_decode_attn_len(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 0.0, FAKE, FAKE,
                                           need - 1, None) == kvr.KVR_ERR_WORKSPACE
+
+
+def test_pipeline_arguments_rejected_before_launch():
+    """Every layer and the stand-in are checked before anything is enqueued:
+    a bad second layer leaves the first layer's state untouched."""
+    d = D()
+    big = 1 << 40
+    st0, st1 = kvr.kvr_spec_state(FAKE, FAKE, 0), kvr.kvr_spec_state(FAKE, FAKE, 0)
+
+    def hbm_layer(st, **kw):
+        args = dict(st=st, q=FAKE, summ=FAKE, out=FAKE, corrected=FAKE, cbar_opt=None, sel_used=FAKE,
+                    sel_used_idx=FAKE, ws=FAKE, ws_bytes=big, events=[FAKE, FAKE],
+                    page_table=FAKE, k_pool=FAKE, v_pool=FAKE)
+        args.update(kw)
+        return kvr.layer(**args)
+
+    def call(layers, compute=None, marks=None, n=None, top_k=64):
+        lib = kvr.raw()
+        arr = (kvr.kvr_layer * max(1, len(layers)))(*layers)
+        mk = None if marks is None else (ctypes.c_void_p * len(marks))(*marks)
+        return lib.kvr_pipeline_step(ctypes.byref(d), len(layers) if n is None else n, arr,
+                                     ctypes.byref(compute) if compute is not None else None, top_k, 0.8, 0.0,
+                                     None, None, None, mk)
+
+    good = hbm_layer(st0)
+    assert call([good], n=0) == kvr.KVR_ERR_INVALID_ARG
+    assert call([good], top_k=0) == kvr.KVR_ERR_INVALID_ARG
+    assert call([good, hbm_layer(st1, events=[FAKE])]) == kvr.KVR_ERR_INVALID_ARG      # ev[1] missing
+    assert call([good, hbm_layer(st1, k_pool=None)]) == kvr.KVR_ERR_INVALID_ARG
+    assert call([good, hbm_layer(st1, out=FAKE + 4)]) == kvr.KVR_ERR_ALIGN
+    assert call([good, hbm_layer(st1, ws_bytes=16)]) == kvr.KVR_ERR_WORKSPACE
+    assert call([good, hbm_layer(kvr.kvr_spec_state(FAKE, FAKE, -1))]) == kvr.KVR_ERR_INVALID_ARG
+    # a host layer needs its working set (double-buffered) and a third event
+    host = kvr.kvr_host_kv(FAKE, FAKE)
+    wset = kvr.kvr_working_set(FAKE, FAKE, FAKE, FAKE, 128)
+    assert call([good, hbm_layer(st1, host=host, wset=wset)]) == kvr.KVR_ERR_INVALID_ARG
+    small = kvr.kvr_working_set(FAKE, FAKE, FAKE, FAKE, 127)
+    assert call([good, hbm_layer(st1, host=host, wset=small, events=[FAKE] * 3)]) == kvr.KVR_ERR_UNSUPPORTED_SHAPE
+    # the stand-in: byte counts in 16-byte words, aligned weights, a sink
+    assert call([good, good], compute=kvr.stand_in(FAKE, 24, 0, FAKE)) == kvr.KVR_ERR_INVALID_ARG
+    assert call([good, good], compute=kvr.stand_in(FAKE, 32, 16, None)) == kvr.KVR_ERR_INVALID_ARG
+    assert call([good, good], compute=kvr.stand_in(FAKE + 8, 32, 16, FAKE)) == kvr.KVR_ERR_ALIGN
+    assert call([good, good], compute=kvr.stand_in(FAKE, 1 << 63, 1 << 63, FAKE)) == kvr.KVR_ERR_INVALID_ARG
+    # timing marks: all n_layers * KVR_PIPE_MARKS present
+    marks = [FAKE] * (2 * kvr.KVR_PIPE_MARKS)
+    marks[-1] = None
+    assert call([good, good], marks=marks) == kvr.KVR_ERR_INVALID_ARG
+    assert st0.step == 0 and st1.step == 0
+
+
+def test_stand_in_read_arguments_rejected_before_launch():
+    lib = kvr.raw()
+    ok = kvr.stand_in(FAKE, 32, 32, FAKE)
+    assert lib.kvr_stand_in_read(None, 0, 16, None) == kvr.KVR_ERR_INVALID_ARG
+    assert lib.kvr_stand_in_read(ctypes.byref(ok), 8, 16, None) == kvr.KVR_ERR_INVALID_ARG
+    assert lib.kvr_stand_in_read(ctypes.byref(ok), 0, 20, None) == kvr.KVR_ERR_INVALID_ARG
+    assert lib.kvr_stand_in_read(ctypes.byref(ok), 1 << 63, 1 << 63, None) == kvr.KVR_ERR_INVALID_ARG
+    assert lib.kvr_stand_in_read(ctypes.byref(kvr.stand_in(FAKE, 32, 32, FAKE + 2)), 0, 16,
+                                 None) == kvr.KVR_ERR_ALIGN

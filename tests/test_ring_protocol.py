@@ -36,7 +36,6 @@ def run(R, n_chunks, seed, early_producer=False):
     t, issued, consumed, reads = 0, 0, 0, []
     while consumed < n_chunks:
         t += 1
-        progressed = False
         # copies land after a random delay (complete_tx completes full's phase)
         for item in sorted(in_flight):
             if item[0] <= t:
@@ -44,7 +43,6 @@ def run(R, n_chunks, seed, early_producer=False):
                 _, s, c = item
                 stage[s] = c
                 full[s].complete()
-                progressed = True
         choice = rng.random()
         if choice < 0.5 and issued < n_chunks:          # producer step
             i = issued
@@ -53,7 +51,6 @@ def run(R, n_chunks, seed, early_producer=False):
             if ok:
                 in_flight.append((t + rng.randint(1, 12), s, i))
                 issued += 1
-                progressed = True
         elif consumed < issued or in_flight:              # consumer step
             i = consumed
             s = i % R
@@ -61,10 +58,8 @@ def run(R, n_chunks, seed, early_producer=False):
                 reads.append((i, stage[s]))
                 consumed += 1
                 empty[s].complete()
-                progressed = True
         if t > 20000:
             raise RuntimeError("no progress")
-        del progressed
     return reads
 
 
