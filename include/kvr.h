@@ -400,7 +400,9 @@ int kvr_stand_in_read(const kvr_stand_in *compute, uint64_t offset,
  * called layer by layer.  Every argument of every layer is checked before
  * anything is enqueued; a CUDA error part-way returns KVR_ERR_CUDA with the
  * earlier layers enqueued (their st->step advanced).  marks: NULL or
- * n_layers * KVR_PIPE_MARKS cudaEvent_t (created with timing).  A host
+ * n_layers * KVR_PIPE_MARKS cudaEvent_t (created with timing); during a
+ * stream capture they are recorded as external events, so the captured
+ * graph records them on every replay (its last step leaves its times).  A host
  * layer's prefetch is joined to `stream` only by that layer's wait in the
  * next step: a caller that ends a CUDA-graph capture after a step, or needs
  * the working sets settled, first makes `stream` wait on each host layer's

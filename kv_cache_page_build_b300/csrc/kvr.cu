@@ -994,8 +994,18 @@ int kvr_pipeline_step(const kvr_dims *dims, int32_t n_layers, kvr_layer *layers,
     const cudaError_t e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(ev), 0);
     return e == cudaSuccess ? KVR_OK : cuda_fail(e, "pipeline stream wait");
   };
+  // timing marks: while the stream is being captured they are recorded as
+  // external events, so that the graph records them on every replay (the
+  // flag is refused outside a capture)
   auto mark = [&](int l, int m, cudaStream_t st) {
-    return marks ? record(marks[static_cast<int64_t>(l) * KVR_PIPE_MARKS + m], st) : KVR_OK;
+    if (!marks) return KVR_OK;
+    cudaEvent_t ev = static_cast<cudaEvent_t>(marks[static_cast<int64_t>(l) * KVR_PIPE_MARKS + m]);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e == cudaSuccess)
+      e = cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal)
+                                              : cudaEventRecord(ev, st);
+    return e == cudaSuccess ? KVR_OK : cuda_fail(e, "pipeline timing mark");
   };
   const uint64_t qkv = compute ? compute->qkv_bytes : 0;
   const uint64_t post = compute ? compute->post_bytes : 0;
@@ -1023,9 +1033,9 @@ int kvr_pipeline_step(const kvr_dims *dims, int32_t n_layers, kvr_layer *layers,
                             carve_select(dims, static_cast<uint8_t *>(L.ws)), nullptr, nullptr,
                             nullptr, sa, side, false));
       KVR_TRY(mark(l, 8, side));
-      KVR_TRY(record(L.ev[1], side));
-      KVR_TRY(mark(l, 9, side));
+      KVR_TRY(mark(l, 9, side));   // before ev[1], which joins them to `stream`
       KVR_TRY(mark(l, 10, side));
+      KVR_TRY(record(L.ev[1], side));
       KVR_TRY(launch_attn(dims, L.q, L.k_pool, L.v_pool, dims->n_phys_pages, L.sel_used_idx, top_k,
                           scale, L.corrected, 1, aw, L.out, s));
       KVR_TRY(mark(l, 3, s));
