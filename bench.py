@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload llama3.1-8b-32k|qwen3-4b-128k|qwen3-4b-128k-host]
+                    [--step sequential|overlap|pipeline] [--layers L]
 
 One step is one speculative decode step of one attention layer over a batch
 of sequences, through kvr_speculative_step_overlap: the group-similarity
@@ -16,6 +17,10 @@ four copies of the cache (--copies) rotate so that no step reads data a
 recent step left in L2.  Steps are replayed from a CUDA graph of 64 captured
 steps.  The "-host" workload keeps the cache in page-locked host memory and
 recalls the selected pages every step (kvr_speculative_step_recall).
+``--step pipeline`` runs a decode step through --layers layers with
+kvr_pipeline_step instead (stand-in projection reads between the
+attentions), beside the same layers stepped one call at a time, and reports
+a per-layer latency breakdown.
 
 Prints one JSON line (rank 0).  With --impl reference the fp64 oracle is
 timed instead, on the host's cores, over a bounded sample of the workload.
