@@ -33,7 +33,7 @@
  *     1 <= k <= N <= 16384; H <= 64; B <= 65535.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Every call only enqueues work on its stream(s) and returns;
- *     it never synchronises, except kvr_get_status.
+ *     it never synchronises, except kvr_get_status and kvr_stream_wait.
  *   - The caller allocates and owns every buffer, workspace, state and
  *     stream.  The library allocates no device memory; its only device state
  *     is a 32-bit status word (see kvr_get_status).
@@ -415,6 +415,15 @@ int kvr_pipeline_step(const kvr_dims *dims, int32_t n_layers, kvr_layer *layers,
 /* Synchronise `stream`, then read and clear the device status word (a bit
  * set of KVR_ST_*).  Returns KVR_OK or KVR_ERR_CUDA. */
 int kvr_get_status(void *stream, uint32_t *status_out);
+
+/* Bounded host-side wait: return once all work enqueued on `stream` has
+ * finished, or after timeout_us microseconds of host time, whichever comes
+ * first (polling cudaStreamQuery; the thread yields between polls).
+ * Returns KVR_OK when the stream is idle, KVR_ERR_TIMEOUT when the deadline
+ * passed first (the work keeps running; the caller may wait again or give
+ * up on it), KVR_ERR_CUDA when the stream reports an error.  timeout_us = 0
+ * polls once. */
+int kvr_stream_wait(void *stream, uint64_t timeout_us);
 
 /* Static description of an error code (never NULL).  For KVR_ERR_CUDA the
  * text of the last CUDA error seen by the library is appended. */

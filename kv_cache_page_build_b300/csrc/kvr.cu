@@ -8,10 +8,12 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <chrono>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <thread>
 
 #include "attention.cuh"
 #include "common.cuh"
@@ -1098,6 +1100,23 @@ int kvr_get_status(void *stream, uint32_t *status_out) {
   if (e != cudaSuccess) return cuda_fail(e, "status clear");
   *status_out = v;
   return KVR_OK;
+}
+
+int kvr_stream_wait(void *stream, uint64_t timeout_us) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    const cudaError_t e = cudaStreamQuery(s);
+    if (e == cudaSuccess) return KVR_OK;
+    if (e != cudaErrorNotReady) return cuda_fail(e, "stream wait");
+    // "not ready" is a state, not an error: keep it out of the launch checks
+    if (cudaPeekAtLastError() == cudaErrorNotReady) (void)cudaGetLastError();
+    const auto us = std::chrono::duration_cast<std::chrono::microseconds>(
+                        std::chrono::steady_clock::now() - t0)
+                        .count();
+    if (static_cast<uint64_t>(us) >= timeout_us) return KVR_ERR_TIMEOUT;
+    std::this_thread::yield();
+  }
 }
 
 const char *kvr_error_string(int code) {

@@ -101,6 +101,7 @@ _SIGS = {
                                _P, _P, _P, ctypes.POINTER(_P)]),
     "kvr_stand_in_read": (_I, [ctypes.POINTER(kvr_stand_in), ctypes.c_uint64, ctypes.c_uint64, _P]),
     "kvr_get_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
+    "kvr_stream_wait": (_I, [_P, ctypes.c_uint64]),
     "kvr_select_pages_noalloc": (_I, [_D, _P, _P, _P, _I, _P, _P, _P, _P]),
     "kvr_error_string": (ctypes.c_char_p, [_I]),
     "kvr_kv_bytes": (ctypes.c_uint64, [ctypes.c_int64] * 5),
@@ -318,6 +319,16 @@ def kvr_get_status(stream=None) -> int:
     v = ctypes.c_uint32(0)
     _check(_lib.kvr_get_status(_stream(stream), ctypes.byref(v)), "kvr_get_status")
     return int(v.value)
+
+
+def kvr_stream_wait(stream=None, timeout_us: int = 0) -> bool:
+    """True once the stream's work has finished, False if timeout_us passed
+    first (KVR_ERR_TIMEOUT); other errors raise."""
+    rc = _lib.kvr_stream_wait(_stream(stream), int(timeout_us))
+    if rc == KVR_ERR_TIMEOUT:
+        return False
+    _check(rc, "kvr_stream_wait")
+    return True
 
 
 def kvr_error_string(code: int) -> str:
