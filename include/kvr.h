@@ -413,7 +413,9 @@ int kvr_pipeline_step(const kvr_dims *dims, int32_t n_layers, kvr_layer *layers,
                       void *prefetch_stream, void *const *marks);
 
 /* Synchronise `stream`, then read and clear the device status word (a bit
- * set of KVR_ST_*).  Returns KVR_OK or KVR_ERR_CUDA. */
+ * set of KVR_ST_*).  Returns KVR_OK or KVR_ERR_CUDA.  A kernel still running
+ * on another stream may set a bit between the read and the clear; for an
+ * exact reading, let every stream that runs library kernels finish first. */
 int kvr_get_status(void *stream, uint32_t *status_out);
 
 /* Bounded host-side wait: return once all work enqueued on `stream` has

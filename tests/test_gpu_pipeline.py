@@ -141,7 +141,9 @@ class Pipeline:
             wl, case, dc, qs, ref = layer_data(i)
             cache = None
             if host:
-                cache = self.caches.setdefault(i, HostCache(case))
+                if i not in self.caches:
+                    self.caches[i] = HostCache(case)
+                cache = self.caches[i]
             self.layers.append(PipeLayer(wl, dc, cache))
             self.qs.append(qs)
         self.dims = self.layers[0].dc.dims
