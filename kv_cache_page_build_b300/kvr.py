@@ -297,9 +297,13 @@ def kvr_pipeline_step(d, layers, compute, top_k, tau, scale, stream, side_stream
     """One decode step through len(layers) layers (a list of kvr_layer);
     `compute` a kvr_stand_in or None; `marks` None or
     len(layers) * KVR_PIPE_MARKS timing events, recorded once beforehand."""
+    if not layers:
+        raise KvrError(KVR_ERR_INVALID_ARG, "kvr_pipeline_step: no layers")
     arr = (kvr_layer * len(layers))(*layers)
     mk = None
     if marks is not None:
+        if len(marks) != len(layers) * KVR_PIPE_MARKS:      # the library reads exactly that many
+            raise KvrError(KVR_ERR_INVALID_ARG, f"kvr_pipeline_step: {len(marks)} marks for {len(layers)} layers")
         mk = (_P * len(marks))(*[_event(m) for m in marks])
     rc = _lib.kvr_pipeline_step(_d(d), len(layers), arr, ctypes.byref(compute) if compute is not None else None,
                                 int(top_k), float(tau), float(scale), _stream(stream), _stream(side_stream),

@@ -239,3 +239,16 @@ def test_stand_in_read_arguments_rejected_before_launch():
     assert lib.kvr_stand_in_read(ctypes.byref(ok), 1 << 63, 1 << 63, None) == kvr.KVR_ERR_INVALID_ARG
     assert lib.kvr_stand_in_read(ctypes.byref(kvr.stand_in(FAKE, 32, 32, FAKE + 2)), 0, 16,
                                  None) == kvr.KVR_ERR_ALIGN
+
+
+def test_pipeline_binding_checks_the_marks_length():
+    """The library reads n_layers * KVR_PIPE_MARKS event handles; the binding
+    refuses a list of another length (and an empty layer list) itself."""
+    st = kvr.kvr_spec_state(FAKE, FAKE, 0)
+    L = kvr.layer(st, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 1 << 40, [FAKE, FAKE],
+                  page_table=FAKE, k_pool=FAKE, v_pool=FAKE)
+    with pytest.raises(kvr.KvrError):
+        kvr.kvr_pipeline_step(D(), [L], None, 64, 0.8, 0.0, 0, 0, 0, marks=[FAKE] * 3)
+    with pytest.raises(kvr.KvrError):
+        kvr.kvr_pipeline_step(D(), [], None, 64, 0.8, 0.0, 0, 0, 0)
+    assert st.step == 0
