@@ -399,14 +399,18 @@ int kvr_stand_in_read(const kvr_stand_in *compute, uint64_t offset,
  * kvr_speculative_step_overlap (HBM) or kvr_speculative_step_recall (host)
  * called layer by layer.  Every argument of every layer is checked before
  * anything is enqueued; a CUDA error part-way returns KVR_ERR_CUDA with the
- * earlier layers enqueued (their st->step advanced).  marks: NULL or
+ * work before it enqueued (st->step has advanced for every layer whose
+ * selection was enqueued).  marks: NULL or
  * n_layers * KVR_PIPE_MARKS cudaEvent_t (created with timing); during a
  * stream capture they are recorded as external events, so the captured
  * graph records them on every replay (its last step leaves its times).  A host
  * layer's prefetch is joined to `stream` only by that layer's wait in the
  * next step: a caller that ends a CUDA-graph capture after a step, or needs
  * the working sets settled, first makes `stream` wait on each host layer's
- * ev[2]. */
+ * ev[2].  That wait at the start of a step is on an event of the previous
+ * step, and a capture may not wait on an event recorded outside it: a
+ * caller that captures steps first records each host layer's ev[2] on the
+ * capturing stream. */
 int kvr_pipeline_step(const kvr_dims *dims, int32_t n_layers, kvr_layer *layers,
                       const kvr_stand_in *compute, int32_t top_k, float tau,
                       float scale, void *stream, void *side_stream,
