@@ -109,14 +109,19 @@ class ClockSampler:
     def __init__(self, index):
         self.proc = None
         self.path = None
+        self.f = None
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                                           "-lms", "100", "-i", str(index)], stdout=self.f, stderr=subprocess.DEVNULL)
-        except Exception:
+        except Exception:                  # no nvidia-smi: the line carries no clock record
             self.proc = None
+            if self.f is not None:
+                self.f.close()
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
 
     def stop(self):
         if self.proc is None:
@@ -137,11 +142,11 @@ class ClockSampler:
         if not rows:
             return None
         sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
-        mx = max(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mxs = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": reasons,
-                "samples": len(rows)}
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mxs) if mxs else None,
+                "reasons": reasons, "samples": len(rows)}
 
 
 # ---------------------------------------------------------------- oracle leg
