@@ -352,7 +352,8 @@ typedef struct kvr_layer {
  * [0, qkv_bytes) of `weights` (the QKV projection); after its attention,
  * bytes [qkv_bytes, qkv_bytes + post_bytes) (the output projection and the
  * FFN).  Each read adds the 32-bit words it read, modulo 2^32, into *sink
- * (device).  qkv_bytes and post_bytes are multiples of 16; either may be 0. */
+ * (device).  qkv_bytes and post_bytes are multiples of 16, either may be 0,
+ * and `weights` (device, 16-byte aligned) holds at least their sum. */
 typedef struct kvr_stand_in {
   const void *weights;
   uint64_t qkv_bytes;
@@ -363,7 +364,7 @@ typedef struct kvr_stand_in {
 /* One stand-in read on its own, on `stream`: bytes [offset, offset + bytes)
  * of compute->weights, summed into compute->sink (as the pipeline's reads;
  * for running the same model without the pipeline).  offset and bytes are
- * multiples of 16. */
+ * multiples of 16, and the range lies inside the caller's weights buffer. */
 int kvr_stand_in_read(const kvr_stand_in *compute, uint64_t offset,
                       uint64_t bytes, void *stream);
 
