@@ -202,6 +202,35 @@ def decode_step(q, k_pool, v_pool, page_table, n_kv_heads, top_k, scale=None, su
     return sel, s, attention(q, k_pool, v_pool, page_table, sel, scale, seq_len)
 
 
+def multi_query_step(qs, k_pool, v_pool, page_table, n_kv_heads, top_k, seq_len, scale=None, summ=None):
+    """Several new query tokens per sequence in one step (no page treats
+    this; it is the reading this oracle takes for it).  qs [B][T][Hq][D]
+    bf16 bits are the queries of each sequence's last T tokens, whose K and
+    V are already in the cache (seq_len [B] >= T counts them).
+
+    * One selection per (sequence, KV head) serves the whole step: the page
+      score is the mean of the upper bound over the step's T x G query rows
+      (FreeKV section 2.1 averages over a KV head's query heads for group
+      consistency; here the group is every query row that will read the
+      pages), over the sequence's started pages.
+    * Query tau (0 <= tau < T) attends causally: over the selected pages'
+      tokens at positions below seq_len - T + tau + 1.
+
+    Returns (sel [B][H][k], scores [B][H][N], out [B][T][Hq][D])."""
+    qs = np.asarray(qs)
+    B, T = qs.shape[0], qs.shape[1]
+    seq_len = np.asarray(seq_len, dtype=np.int32)
+    assert seq_len.shape == (B,) and np.all(seq_len >= T)
+    if summ is None:
+        summ = summaries(k_pool, page_table, seq_len=seq_len)
+    s = sum(scores(qs[:, t], *summ) for t in range(T)) / T
+    nv = np.repeat(valid_pages(seq_len, np.asarray(k_pool).shape[1])[:, None], n_kv_heads, axis=1)
+    sel = topk(s, top_k, nv)
+    out = np.stack([attention(qs[:, t], k_pool, v_pool, page_table, sel, scale, seq_len - (T - 1 - t))
+                    for t in range(T)], axis=1)
+    return sel, s, out
+
+
 def append(k_pool, v_pool, page_table, seq_len, k_new, v_new):
     """Decode-time append ("Key-Value (KV) Cache" wiki page: each step adds
     the new token's K and V to the cache; PagedAttention fills pages in

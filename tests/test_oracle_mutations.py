@@ -10,7 +10,8 @@ import oracle
 import oracle.oracle as om
 from tests import test_oracle_pins as pins
 
-REAL = {name: getattr(om, name) for name in ("summaries", "scores", "topk", "attention", "group_cosine")}
+REAL = {name: getattr(om, name) for name in ("summaries", "scores", "topk", "attention", "group_cosine",
+                                             "multi_query_step")}
 PIN_TESTS = [f for name, f in inspect.getmembers(pins, inspect.isfunction)
              if name.startswith("test_") and "golden" not in name and "kv_cache_size" not in name]
 
@@ -78,6 +79,26 @@ def _lengths_off_by_one(k_pool, page_table, n_kv_heads=None, seq_len=None):
                              seq_len=None if seq_len is None else np.asarray(seq_len) - 1)
 
 
+def _causal_one_late(qs, k_pool, v_pool, page_table, n_kv_heads, top_k, seq_len, scale=None, summ=None):
+    sel, s, _ = REAL["multi_query_step"](qs, k_pool, v_pool, page_table, n_kv_heads, top_k, seq_len, scale, summ)
+    T = np.asarray(qs).shape[1]
+    lens = np.asarray(seq_len, dtype=np.int32)
+    out = np.stack([REAL["attention"](np.asarray(qs)[:, t], k_pool, v_pool, page_table, sel, scale,
+                                      np.minimum(lens, lens - T + t + 2)) for t in range(T)], axis=1)
+    return sel, s, out                               # query tau also sees token tau + 1
+
+
+def _last_query_selects(qs, k_pool, v_pool, page_table, n_kv_heads, top_k, seq_len, scale=None, summ=None):
+    qs = np.asarray(qs)
+    T = qs.shape[1]
+    last = np.repeat(qs[:, -1:], T, axis=1)
+    sel, s, _ = REAL["multi_query_step"](last, k_pool, v_pool, page_table, n_kv_heads, top_k, seq_len, scale,
+                                         summ)
+    out = np.stack([REAL["attention"](qs[:, t], k_pool, v_pool, page_table, sel, scale,
+                                      np.asarray(seq_len) - T + t + 1) for t in range(T)], axis=1)
+    return sel, s, out
+
+
 MUTATIONS = {
     "min/max swapped": ("summaries", _swap_minmax),
     "summary of the first token only": ("summaries", _one_token_summary),
@@ -91,6 +112,8 @@ MUTATIONS = {
     "query heads mapped to the wrong KV head in attention": ("attention", _head_map),
     "cosine without the norms": ("group_cosine", _cosine_without_norms),
     "written tokens counted one short": ("summaries", _lengths_off_by_one),
+    "several queries: causal limit one token late": ("multi_query_step", _causal_one_late),
+    "several queries: selection from the last query only": ("multi_query_step", _last_query_selects),
 }
 
 

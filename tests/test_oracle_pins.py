@@ -397,6 +397,95 @@ def test_append_writes_the_next_row_of_every_head():
         np.testing.assert_array_equal(kmax[b, :, last], rows[last * P:L].max(axis=0))
 
 
+# ---------------------------------------------------------------- several queries per step
+
+def _brute_topk_valid(s, k, started):
+    """Top-k over each sequence's started pages by a full sort (ties to the
+    lower id), ascending, -1 padded: [B][H][k]."""
+    B, H, N = s.shape
+    out = np.full((B, H, k), -1, dtype=np.int32)
+    for b in range(B):
+        for g in range(H):
+            n = int(started[b])
+            order = sorted(range(n), key=lambda p: (-s[b, g, p], p))[:k]
+            out[b, g, :len(order)] = sorted(order)
+    return out
+
+
+def _multi_case(T=3, **kw):
+    wl = small(**kw)
+    case = synth.make_case(wl)
+    rng = np.random.default_rng(123)
+    qs = synth.f64_to_bf16_bits(rng.standard_normal((wl.batch, T, wl.n_q_heads, wl.head_dim)))
+    lens = np.array([wl.n_pages * wl.page_size - 3, 2 * wl.page_size + 1], dtype=np.int32)[:wl.batch]
+    return wl, case, qs, lens
+
+
+def test_multi_query_with_one_query_is_the_decode_step():
+    wl, case, qs, lens = _multi_case(T=1)
+    sel, s, out = oracle.multi_query_step(qs, case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads,
+                                          wl.top_k, lens)
+    ref = oracle.decode_step(qs[:, 0], case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads, wl.top_k,
+                             seq_len=lens)
+    np.testing.assert_array_equal(sel, ref[0])
+    np.testing.assert_array_equal(s, ref[1])
+    np.testing.assert_array_equal(out[:, 0], ref[2])
+
+
+def test_multi_query_score_is_the_mean_over_the_wider_group():
+    """The step's score equals the single-query score of a KV head whose
+    group holds all T x G query rows (one call, one mean)."""
+    wl, case, qs, lens = _multi_case(T=3)
+    B, T, Hq, D = qs.shape
+    H, G = wl.n_kv_heads, wl.group
+    sel, s, _ = oracle.multi_query_step(qs, case.k_pool, case.v_pool, case.page_table, H, wl.top_k, lens)
+    wide = qs.reshape(B, T, H, G, D).transpose(0, 2, 1, 3, 4).reshape(B, H * T * G, D)
+    summ = oracle.summaries(case.k_pool, case.page_table, seq_len=lens)
+    s_wide = oracle.scores(wide, *summ)
+    np.testing.assert_allclose(s, s_wide, rtol=1e-12, atol=1e-12)
+    started = (lens + wl.page_size - 1) // wl.page_size
+    np.testing.assert_array_equal(sel, _brute_topk_valid(s_wide, wl.top_k, started))
+
+
+def test_multi_query_attention_is_causal_sdpa():
+    """Query tau of sequence b attends over the selected tokens at positions
+    below L - T + tau + 1 (float64 SDPA on the gathered tokens)."""
+    wl, case, qs, lens = _multi_case(T=3)
+    B, T, Hq, D = qs.shape
+    P, G = wl.page_size, wl.group
+    sel, _, out = oracle.multi_query_step(qs, case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads,
+                                          wl.top_k, lens, scale=0.25)
+    keys, vals = logical_keys(case), logical_values(case)
+    for b, L in enumerate(lens):
+        for t in range(T):
+            limit = int(L) - T + t + 1
+            for h in range(Hq):
+                g = h // G
+                rows = [(p, r) for p in sel[b, g] if p >= 0 for r in range(P) if p * P + r < limit]
+                assert rows, "a query with no token to attend"
+                kk = torch.from_numpy(np.stack([keys[b, p, r, g] for p, r in rows]))[None]
+                vv = torch.from_numpy(np.stack([vals[b, p, r, g] for p, r in rows]))[None]
+                qq = torch.from_numpy(f(qs[b, t, h]))[None, None]
+                ref = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, scale=0.25)[0, 0]
+                np.testing.assert_allclose(out[b, t, h], ref.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_multi_query_later_tokens_stay_out_of_earlier_queries():
+    """Changing the value of each sequence's newest token changes only the
+    last query's output (every page selected, so that token is read)."""
+    wl, case, qs, lens = _multi_case(T=3, top_k=12)
+    T = qs.shape[1]
+    args = (case.k_pool, case.page_table, wl.n_kv_heads, wl.top_k, lens)
+    _, _, out = oracle.multi_query_step(qs, case.k_pool, case.v_pool, *args[1:])
+    v2 = np.array(case.v_pool, copy=True)
+    P = wl.page_size
+    for b, L in enumerate(lens):
+        v2[case.page_table[b, (L - 1) // P], (L - 1) % P] ^= 0x0040     # flip a mantissa bit of every channel
+    _, _, out2 = oracle.multi_query_step(qs, case.k_pool, v2, *args[1:])
+    np.testing.assert_array_equal(out[:, :T - 1], out2[:, :T - 1])
+    assert np.all(np.abs(out[:, T - 1] - out2[:, T - 1]).max(axis=-1) > 0)
+
+
 def test_kv_cache_size_matches_printed_llama65b_figure():
     g = json.load(open(os.path.join(GOLDEN, "kv_cache_size_llama65b.json")))
     n = oracle.kv_cache_bytes(g["n_layers"], g["n_kv_heads"], g["head_dim"], g["n_tokens"], g["bytes_per_elem"])
