@@ -33,6 +33,7 @@ import numpy as np
 # substream tags
 _T_TABLE, _T_K, _T_V, _T_Q, _T_PLANT_POS, _T_PLANT_NOISE = 1, 2, 3, 4, 5, 6
 _T_SCALE, _T_RHO, _T_JUMPS, _T_EPS = 7, 8, 9, 10
+_T_MULTI = 11
 
 _CHUNK_PAGES = 64
 
@@ -326,6 +327,35 @@ def make_trace(wl, case: Case,
             state[b] = cand
             qs[t, b] = bits
     return Trace(qs, rho, jumps, attempts)
+
+
+def make_multi_queries(case: Case, T: int, accept: Optional[Callable[[int, np.ndarray], bool]] = None,
+                       rho: float = 0.9, max_attempts: int = 200) -> np.ndarray:
+    """T query tokens per sequence for one step of several queries: an AR(1)
+    run q_tau = rho q_{tau-1} + sqrt(1 - rho^2) eps_tau from the case's
+    query, in float64, each token handed out rounded to bf16.
+    ``accept(b, rows)`` (rows [T][Hq][D] bits, optional) may reject row b,
+    whose innovations are then redrawn with the next attempt counter.
+    Returns [B][T][Hq][D] bf16 bits."""
+    wl = case.wl
+    c = np.sqrt(1.0 - rho * rho)
+    out = np.empty((wl.batch, T) + case.q.shape[1:], dtype=np.uint16)
+    for b in range(wl.batch):
+        n = 0
+        while True:
+            state = bf16_bits_to_f64(case.q[b])
+            rows = []
+            for t in range(T):
+                state = rho * state + c * _rng(wl.seed, _T_MULTI, b, t, n).standard_normal(state.shape)
+                rows.append(f64_to_bf16_bits(state))
+            rows = np.stack(rows)
+            if accept is None or accept(b, rows):
+                break
+            n += 1
+            if n >= max_attempts:
+                raise RuntimeError(f"{wl.name}: no accepted queries for row {b} in {max_attempts} draws")
+        out[b] = rows
+    return out
 
 
 def custom(name="custom", **kw) -> Workload:

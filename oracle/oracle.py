@@ -297,6 +297,23 @@ def topk_margin(s, k):
     return srt[..., k - 1] - srt[..., k]
 
 
+def accept_multi_query(summ, n_kv_heads, top_k, seq_len, page_size, margin=MARGIN):
+    """Predicate for synth.make_multi_queries: row b's T queries are kept
+    when the step's page score (the mean over its T x G query rows, as in
+    multi_query_step) has a top-k margin of at least `margin` among the
+    sequence's started pages, for every KV head."""
+    kmin, kmax = summ
+    started = valid_pages(seq_len, page_size)
+
+    def accept(b, q_rows):                        # q_rows [T][Hq][D] bf16 bits
+        T = q_rows.shape[0]
+        s = sum(scores(q_rows[t][None], kmin[b:b + 1], kmax[b:b + 1]) for t in range(T)) / T
+        n = int(started[b])
+        assert s.shape[1] == n_kv_heads
+        return bool(np.all(topk_margin(s[..., :n], top_k) >= margin))
+    return accept
+
+
 def accept_single_step(top_k, margin=MARGIN):
     """Predicate for synth.make_case: row b's top-k boundary margin >= margin
     for every KV head (summaries recomputed, planted pages depend on q)."""

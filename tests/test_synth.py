@@ -110,3 +110,26 @@ def test_trace_rejection_redraws_only_the_rejected_row():
     np.testing.assert_array_equal(tr.q[2, 0], plain.q[2, 0])
     assert not np.array_equal(tr.q[2, 1], plain.q[2, 1])
     assert tr.attempts[2, 1] == 1
+
+
+def test_multi_queries_are_deterministic_and_keep_the_margin():
+    """Several queries per step: T AR(1) tokens per sequence from the case's
+    query, redrawn until the step's mean page score has a top-k margin of at
+    least 1e-3 among the started pages; the same seed gives the same bits."""
+    wl = synth.custom(batch=2, n_q_heads=8, n_kv_heads=2, head_dim=32, page_size=8, n_pages=40, top_k=6)
+    case = synth.make_case(wl)
+    lens = np.array([wl.n_pages * wl.page_size - 3, 17 * wl.page_size + 2], dtype=np.int32)
+    summ = oracle.summaries(case.k_pool, case.page_table, seq_len=lens)
+    acc = oracle.accept_multi_query(summ, wl.n_kv_heads, wl.top_k, lens, wl.page_size)
+    qs = synth.make_multi_queries(case, 4, accept=acc)
+    assert qs.shape == (2, 4, 8, 32) and qs.dtype == np.uint16
+    np.testing.assert_array_equal(qs, synth.make_multi_queries(case, 4, accept=acc))
+    _, s, _ = oracle.multi_query_step(qs, case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads, wl.top_k,
+                                      lens, summ=summ)
+    started = oracle.valid_pages(lens, wl.page_size)
+    for b in range(wl.batch):
+        assert np.all(oracle.topk_margin(s[b, :, :started[b]], wl.top_k) >= 1e-3)
+    # the AR(1) run keeps successive tokens close (rho = 0.9)
+    x = synth.bf16_bits_to_f64(qs)
+    cos = (x[:, 1:] * x[:, :-1]).sum(-1) / np.linalg.norm(x[:, 1:], axis=-1) / np.linalg.norm(x[:, :-1], axis=-1)
+    assert cos.mean() > 0.8
