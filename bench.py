@@ -1,26 +1,31 @@
 """Decode-step benchmark of libkvr on one B300 (or N independent replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload llama3.1-8b-32k|qwen3-4b-128k|qwen3-4b-128k-host]
-                    [--step sequential|overlap|pipeline] [--layers L]
+                    [--workload qwen3-4b-128k|llama3.1-8b-32k|qwen3-4b-128k-host]
+                    [--step sequential|overlap|pipeline] [--layers L] [--no-extras]
 
 One step is one speculative decode step of one attention layer over a batch
-of sequences, through kvr_speculative_step_overlap: the group-similarity
-correction decision; page scoring and top-k selection per KV head on a side
-stream, beside the sparse GQA attention of the KV heads that reuse their
-previous pages; then the attention of the corrected heads.  Page summaries
-are built once per cache (prefill) and reported on their own.  Inputs are
-seeded synthetic caches with the layer shapes of Llama-3.1-8B (default) or
-Qwen3-4B; the queries follow the AR(1) trace of the speculative workload.
-The cache, queries and state are resident in HBM before the timed region;
-four copies of the cache (--copies) rotate so that no step reads data a
-recent step left in L2.  Steps are replayed from a CUDA graph of 64 captured
-steps.  The "-host" workload keeps the cache in page-locked host memory and
-recalls the selected pages every step (kvr_speculative_step_recall).
-``--step pipeline`` runs a decode step through --layers layers with
-kvr_pipeline_step instead (stand-in projection reads between the
-attentions), beside the same layers stepped one call at a time, and reports
-a per-layer latency breakdown.
+of sequences, through kvr_speculative_step (default): page scoring, then the
+top-k selection per KV head with the group-similarity correction decision,
+then the sparse GQA attention over the pages each KV head uses this step.
+``--step overlap`` runs kvr_speculative_step_overlap instead (the selection
+on a side stream beside the reused heads' attention).  Page summaries are
+built once per cache (prefill) and reported on their own.  Inputs are seeded
+synthetic caches with the layer shapes of Qwen3-4B at 128K context (default)
+or Llama-3.1-8B at 32K; the queries follow the AR(1) trace of the speculative
+workload.  The cache, queries and state are resident in HBM before the timed
+region; four copies of the cache (--copies) rotate so that no step reads
+data a recent step left in L2.  Exactly K steps are timed: a CUDA graph of
+min(64, K) captured steps is replayed K // 64 times, plus a graph of the
+remaining steps.  Per-kernel times come from graphs of 64 back-to-back calls
+of each kind, replayed until at least --kernel-launches calls have run.  The
+line's "also" key holds compact records of the other HBM workload and of the
+host-resident one (--no-extras drops them).  The "-host" workload keeps the
+cache in page-locked host memory and recalls the selected pages every step
+(kvr_speculative_step_recall).  ``--step pipeline`` runs a decode step
+through --layers layers with kvr_pipeline_step instead (stand-in projection
+reads between the attentions), beside the same layers stepped one call at a
+time, and reports a per-layer latency breakdown.
 
 Prints one JSON line (rank 0).  With --impl reference the fp64 oracle is
 timed instead, on the host's cores, over a bounded sample of the workload.
@@ -256,13 +261,42 @@ def kernel_source_hash(kernel: str, read=None) -> str:
     return h.hexdigest()
 
 
-def run_gpu(args, world, rank, local):
+def _clock_sampler(dev, local):
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    return ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or local))
+
+
+def _graph_time(torch, g, launches_per_replay, min_launches):
+    """Mean device time per launch of a graph of `launches_per_replay` calls,
+    replayed back to back (after two untimed replays) until at least
+    `min_launches` launches have run; CUDA events around the replays."""
+    reps = max(1, -(-min_launches // launches_per_replay))
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / (reps * launches_per_replay), reps * launches_per_replay
+
+
+def measure_hbm(wl_name, args, world, local, steps, warmup, e2e_calls, kernel_launches, clocks=True):
+    """One HBM-resident workload: speculative decode steps (selection, then
+    attention) over `copies` rotating copies of the cache, timed from a CUDA
+    graph; per-kernel times from graphs of back-to-back calls; end-to-end
+    eager calls with host copies; the decode-time append.  Returns a dict of
+    raw measurements (seconds, bytes)."""
     import torch
     from kv_cache_page_build_b300 import kvr, synth
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    cid, tid = WORKLOADS[args.workload]
+    cid, tid = WORKLOADS[wl_name]
     COPIES = max(1, args.copies)
     wl_trace = synth.WORKLOADS[tid]
     case = synth.make_case(cid)
@@ -279,12 +313,12 @@ def run_gpu(args, world, rank, local):
     v_pools = [to_dev(case.v_pool.view(np.int16)) for _ in range(COPIES)]
     page_table = to_dev(case.page_table)
     qs = to_dev(tr.q.view(np.int16))                               # [T][B][Hq][D]
+    q_host = torch.from_numpy(tr.q.view(np.int16).copy()).pin_memory()
     TRACE_LEN = qs.shape[0]
     summs = [torch.empty((B, H, N, 2, D), dtype=torch.int16, device=dev) for _ in range(COPIES)]
     del case
 
-    # summaries (prefill-time): time one build per copy
-    stream = torch.cuda.current_stream()
+    # summaries (prefill-time): one build per copy, timed together
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     kvr.kvr_build_summaries(d, k_pools[0], page_table, summs[0])
     torch.cuda.synchronize()
@@ -293,8 +327,7 @@ def run_gpu(args, world, rank, local):
         kvr.kvr_build_summaries(d, k_pools[c], page_table, summs[c])
     e1.record()
     torch.cuda.synchronize()
-    summ_ms = e0.elapsed_time(e1) / COPIES
-    k_bytes = B * N * P * H * D * 2
+    summ_s = e0.elapsed_time(e1) / 1e3 / COPIES
 
     # speculative state and outputs
     q_prev = torch.zeros((B, Hq, D), dtype=torch.int16, device=dev)
@@ -318,9 +351,6 @@ def run_gpu(args, world, rank, local):
         kvr.kvr_sparse_decode_attn(d, qs[i % TRACE_LEN], k_pools[c], v_pools[c], sel_used_phys, k, 0.0, out,
                                    wa, wa_n)
 
-    # one step: kvr_speculative_step_overlap (the decision, then the selection
-    # on a side stream beside the reused heads' attention, then the corrected
-    # heads' attention)
     side = torch.cuda.Stream()
     ev_d, ev_s = torch.cuda.Event(), torch.cuda.Event()
     ev_d.record()
@@ -340,29 +370,19 @@ def run_gpu(args, world, rank, local):
                                      0.0, out, corrected, None, sel_used, sel_used_phys, wstep, wstep.numel())
 
     # warm-up: eager steps (the first one is step 0 of the trace)
-    for i in range(max(args.warmup, 3)):
+    for i in range(max(warmup, 3)):
         step(i)
     torch.cuda.synchronize()
     assert kvr.kvr_get_status() == 0
 
-    # capture L steps (starting at a trace position multiple of the trace
-    # length) into a graph; the timed graph holds nothing but the steps
-    L = min(TRACE_LEN, args.steps)
+    # the timed steps: a graph of L steps replayed steps // L times, plus a
+    # graph of the remainder, so that exactly `steps` steps run
+    L = min(64, steps)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         for i in range(L):
             step(i)
-    # per-kernel times: graphs of L back-to-back calls of each kind (selection
-    # alone, attention alone on the rotating caches), timed after the run
-    graph_sel = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_sel):
-        for i in range(L):
-            select_call(i)
-    graph_attn = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_attn):
-        for i in range(L):
-            attn_call(i)
-    rem = args.steps % L
+    rem = steps % L
     graph_rem = None
     if rem:
         graph_rem = torch.cuda.CUDAGraph()
@@ -371,15 +391,19 @@ def run_gpu(args, world, rank, local):
                 step(i)
     for _ in range(2):
         graph.replay()
+        if graph_rem is not None:
+            graph_rem.replay()
     torch.cuda.synchronize()
-
-    reps = args.steps // L
-    props = torch.cuda.get_device_properties(dev)
-    uuid = str(getattr(props, "uuid", "") or "")
-    clocks = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or local))
-    time.sleep(0.3)
+    reps = steps // L
+    sampler = _clock_sampler(dev, local) if clocks else None
+    if sampler is not None:
+        time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
+    # untimed replays enqueued right before the timed ones, so the GPU runs
+    # at its working clocks when the timed region starts (no idle gap)
+    for _ in range(max(1, -(-256 // L))):
+        graph.replay()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
     for _ in range(reps):
@@ -389,137 +413,150 @@ def run_gpu(args, world, rank, local):
     t1.record()
     torch.cuda.synchronize()
     barrier(world)
-    clk = clocks.stop() if clocks else None
+    clk = sampler.stop() if sampler is not None else None
     elapsed = t0.elapsed_time(t1) / 1e3
     status = kvr.kvr_get_status()
-    value, t_max = aggregate(args.steps, elapsed, world)
+    value, t_max = aggregate(steps, elapsed, world)
 
-    # per-launch device time of the two calls, from replays of their graphs
-    def per_call(g, reps=4):
-        g.replay()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(reps):
-            g.replay()
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / 1e3 / (reps * L)
+    # per-launch device time of the selection and of the attention: graphs
+    # of 64 back-to-back calls of each kind, replayed until at least
+    # `kernel_launches` calls have run
+    LK = 64
+    graph_sel = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_sel):
+        for i in range(LK):
+            select_call(i)
+    graph_attn = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_attn):
+        for i in range(LK):
+            attn_call(i)
+    attn_avg, n_attn = _graph_time(torch, graph_attn, LK, kernel_launches)
+    sel_avg, n_sel = _graph_time(torch, graph_sel, LK, kernel_launches)
+    status |= kvr.kvr_get_status()
 
-    attn_avg = per_call(graph_attn)
-    sel_avg = per_call(graph_sel)
-
-    hbm, peak_kind = peaks()
-    attn_bytes = B * H * k * P * 2 * D * 2                 # selected K and V rows read per launch
-    summ_bytes = B * H * N * 2 * D * 2                     # summaries read by the selection
-    achieved = attn_bytes / attn_avg / 1e9
-    traffic = traffic_for("k_sparse_decode", args.workload)
-
-    # end to end through the public API with host buffers (eager calls)
-    q_host = torch.from_numpy(tr.q.view(np.int16).copy()).pin_memory()
+    # end to end through the public entry point with host buffers: q copied
+    # in from pinned memory and the output copied back every step, the
+    # stream synchronised per step; untimed warm-up calls on the same buffers
     out_host = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
     q_dev = torch.empty((B, Hq, D), dtype=torch.int16, device=dev)
-    n_e2e = min(args.steps, 2000)
-    barrier(world)
-    torch.cuda.synchronize()
-    w0 = time.perf_counter()
-    for i in range(n_e2e):
+    stream = torch.cuda.current_stream()
+
+    def e2e_step(i):
         q_dev.copy_(q_host[i % TRACE_LEN], non_blocking=True)
         step(i, q_dev)
         out_host.copy_(out, non_blocking=True)
         stream.synchronize()
+
+    for i in range(200):
+        e2e_step(i)
+    barrier(world)
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for i in range(e2e_calls):
+        e2e_step(i)
     e2e_s = time.perf_counter() - w0
-    e2e_value, _ = aggregate(n_e2e, e2e_s, world)
+    e2e_value, _ = aggregate(e2e_calls, e2e_s, world)
     status |= kvr.kvr_get_status()
 
-    # decode-time append (kvr_append_kv), timed last: graphs of L appends into
-    # the last L token slots of cache copy 0 (its lengths set L tokens short)
-    app_len = torch.full((B,), N * P - L, dtype=torch.int32, device=dev)
+    # decode-time append (kvr_append_kv), timed last: a graph of LK appends
+    # into the last LK token slots of cache copy 0 (its lengths set LK tokens
+    # short), re-armed and replayed
+    app_len = torch.full((B,), N * P - LK, dtype=torch.int32, device=dev)
     k_rows = torch.zeros((B, H, D), dtype=torch.int16, device=dev)
     graph_app = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph_app):
-        for _ in range(L):
+        for _ in range(LK):
             kvr.kvr_append_kv(d, k_rows, k_rows, page_table, app_len, k_pools[0], v_pools[0], summs[0])
-    app_len.fill_(N * P - L)
-    graph_app.replay()
-    torch.cuda.synchronize()
-    ta, tb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    app_len.fill_(N * P - L)
-    ta.record()
-    graph_app.replay()
-    tb.record()
-    torch.cuda.synchronize()
-    app_avg = ta.elapsed_time(tb) / 1e3 / L
+    app_times = []
+    for _ in range(6):
+        app_len.fill_(N * P - LK)
+        torch.cuda.synchronize()
+        ta, tb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ta.record()
+        graph_app.replay()
+        tb.record()
+        torch.cuda.synchronize()
+        app_times.append(ta.elapsed_time(tb) / 1e3 / LK)
+    app_avg = statistics.median(app_times[1:])
     status |= kvr.kvr_get_status()
+    res = dict(wl=wl, tau=wl_trace.tau, copies=COPIES, steps=steps, L=L, value=value, t_max=t_max,
+               attn_avg=attn_avg, n_attn=n_attn, sel_avg=sel_avg, n_sel=n_sel, app_avg=app_avg, summ_s=summ_s,
+               e2e_value=e2e_value, e2e_calls=e2e_calls, clk=clk, status=status,
+               attn_bytes=B * H * k * P * 2 * D * 2,          # selected K and V rows read per launch
+               summ_bytes=B * H * N * 2 * D * 2,               # summaries read by the selection
+               k_bytes=B * N * P * H * D * 2)
+    del k_pools, v_pools, summs, qs
+    torch.cuda.empty_cache()
+    return res
 
-    result = {
-        "metric": METRIC,
-        "value": round(value, 2),
-        "unit": "steps/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(t_max / args.steps * 1e3, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "f32",
-        "data": "synthetic",
-        "config": {
-            "workload": f"{args.workload}: {wl.batch} sequences x {Hq}/{H} heads, head_dim {D}, "
-                        f"context {wl.context}, page {P}, top-k {k} pages; speculative, tau {wl_trace.tau}",
-            "batch": B, "n_q_heads": Hq, "n_kv_heads": H, "head_dim": D, "context": wl.context,
-            "page_size": P, "top_k": k, "tau": wl_trace.tau, "storage": "bf16", "accumulate": "f32",
-            "step": f"kvr_speculative_step{'_overlap' if args.step == 'overlap' else ''}",
-            "parallelism": f"{world} independent replica(s)" if world > 1 else "1 GPU",
-            "l2": f"{COPIES} rotating cache copies: {(COPIES - 1) * (attn_bytes + summ_bytes) / 2**20:.0f} MiB "
-                  f"touched between reuses of one copy (L2 126 MB)",
-            "graph": f"steps replayed from a CUDA graph of {L} steps (per-kernel times from graphs of {L} "
-                     f"back-to-back calls of each kind)",
-        },
-        "selected_kv_gbs": round(achieved, 1),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "k_sparse_decode", "bytes_per_launch": attn_bytes,
-                     "launch_us": round(attn_avg * 1e6, 3)},
-        "kernels": {
-            "attention (k_sparse_decode)": {"us": round(attn_avg * 1e6, 3), "bytes": attn_bytes,
-                                                           "gbs": round(achieved, 1)},
-            "selection (k_page_scores + k_topk)": {"us": round(sel_avg * 1e6, 3) if sel_avg else None,
-                                                   "bytes": summ_bytes,
-                                                   "gbs": round(summ_bytes / sel_avg / 1e9, 1) if sel_avg else None},
-            "k_append (decode-time append, one token per sequence)": {
-                "us": round(app_avg * 1e6, 3), "bytes": B * H * (2 * D * 2 + 2 * 2 * D * 2),
-                "note": "latency-bound: K and V rows written and the page summary read and written per "
-                        "(sequence, KV head)"},
-            "k_build_summaries": {"us": round(summ_ms * 1e3, 3), "bytes": k_bytes + summ_bytes,
-                                  "gbs": round((k_bytes + summ_bytes) / (summ_ms / 1e3) / 1e9, 1),
-                                  "note": "once per cache (prefill), not in the step"},
-        },
-        # k_page_scores, k_topk, k_sparse_decode (+ k_spec_decide and a second attention launch)
-        "gpu_launches": (5 if args.step == "overlap" else 3) * args.steps,
-        "e2e": {"value": round(e2e_value, 2), "unit": "steps/s",
-                "h2d_bytes_per_step": B * Hq * D * 2, "d2h_bytes_per_step": B * Hq * D * 4,
-                "how": f"{n_e2e} eager kvr_speculative_step{'_overlap' if args.step == 'overlap' else ''} calls, "
-                       f"q copied in from pinned host memory "
-                       f"and the fp32 output copied back every step, stream synchronised per step"},
-        "clocks": clk,
-        "device_status": status,
+
+def hbm_kernels(r):
+    """The per-kernel figures of one HBM workload."""
+    hbm, _ = peaks()
+    gbs = r["attn_bytes"] / r["attn_avg"] / 1e9
+    sel_gbs = r["summ_bytes"] / r["sel_avg"] / 1e9
+    wl = r["wl"]
+    build_bytes = r["k_bytes"] + r["summ_bytes"]
+    return {
+        "attention (k_sparse_decode)": {"us": round(r["attn_avg"] * 1e6, 3), "bytes": r["attn_bytes"],
+                                        "gbs": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                                        "launches_timed": r["n_attn"]},
+        "selection (k_page_scores + k_topk)": {"us": round(r["sel_avg"] * 1e6, 3), "bytes": r["summ_bytes"],
+                                               "gbs": round(sel_gbs, 1), "frac": round(sel_gbs / hbm, 4),
+                                               "launches_timed": r["n_sel"]},
+        "k_append (decode-time append, one token per sequence)": {
+            "us": round(r["app_avg"] * 1e6, 3), "bytes": wl.batch * wl.n_kv_heads * (2 * wl.head_dim * 2 +
+                                                                                    2 * 2 * wl.head_dim * 2),
+            "note": "latency-bound: K and V rows written and the page summary read and written per "
+                    "(sequence, KV head)"},
+        "k_build_summaries": {"us": round(r["summ_s"] * 1e6, 3), "bytes": build_bytes,
+                              "gbs": round(build_bytes / r["summ_s"] / 1e9, 1),
+                              "note": "once per cache (prefill), not in the step"},
     }
-    return result
 
 
-def run_gpu_recall(args, world, rank, local):
+def hbm_config(name, r, world):
+    wl = r["wl"]
+    B, Hq, H, D, P, k = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.page_size, wl.top_k
+    return {
+        "workload": f"{name}: {B} sequences x {Hq}/{H} heads, head_dim {D}, context {wl.context}, page {P}, "
+                    f"top-k {k} pages; speculative, tau {r['tau']}",
+        "batch": B, "n_q_heads": Hq, "n_kv_heads": H, "head_dim": D, "context": wl.context, "page_size": P,
+        "top_k": k, "tau": r["tau"], "storage": "bf16", "accumulate": "f32",
+        "parallelism": f"{world} independent replica(s)" if world > 1 else "1 GPU",
+        "l2": f"{r['copies']} rotating cache copies: "
+              f"{(r['copies'] - 1) * (r['attn_bytes'] + r['summ_bytes']) / 2**20:.0f} MiB touched between reuses "
+              f"of one copy (L2 126 MB)",
+        "graph": f"steps replayed from a CUDA graph of {r['L']} steps; per-kernel times from graphs of 64 "
+                 f"back-to-back calls of each kind, {r['n_attn']} attention and {r['n_sel']} selection launches "
+                 f"timed",
+    }
+
+
+def hbm_summary(name, r):
+    """A compact record of a workload that is not the line's headline."""
+    hbm, _ = peaks()
+    gbs = r["attn_bytes"] / r["attn_avg"] / 1e9
+    return {"workload": hbm_config(name, r, 1)["workload"], "steps_per_s": round(r["value"], 2),
+            "steps": r["steps"], "ms_per_step": round(r["t_max"] / r["steps"] * 1e3, 5),
+            "roofline": {"bound": "hbm", "kernel": "k_sparse_decode", "achieved": round(gbs, 1), "peak": hbm,
+                         "unit": "GB/s", "frac": round(gbs / hbm, 4)},
+            "kernels": hbm_kernels(r),
+            "e2e_steps_per_s": round(r["e2e_value"], 2), "clocks": r["clk"], "device_status": r["status"]}
+
+
+def measure_recall(args, world, local, reps, warmup, e2e_calls, clocks=True):
     """The host-resident workload: the K/V cache in page-locked host memory
     (head-major), summaries and a 2k-slot working set per (sequence, KV head)
     in HBM; each step selects speculatively, recalls the missing pages on a
-    side stream and attends over the working set (kvr_speculative_step_recall)."""
+    side stream and attends over the working set (kvr_speculative_step_recall).
+    Steps replay from a CUDA graph of the 32-step query trace, `reps` times."""
     import torch
     from kv_cache_page_build_b300 import kvr, synth
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    cid, tid = WORKLOADS[args.workload]
+    cid, tid = WORKLOADS["qwen3-4b-128k-host"]
     wl_trace = synth.WORKLOADS[tid]
     case = synth.make_case(cid)
     tr = synth.make_trace(wl_trace, case)
@@ -530,17 +567,25 @@ def run_gpu_recall(args, world, rank, local):
     d = kvr.kvr_dims(**wl.dims())
     page_bytes = 2 * P * D * 2                      # K and V of one (sequence, head, page)
 
-    # prefill: the summaries come from a device copy of K, which is then dropped
+    # prefill: the summaries come from a device copy of K; the head-major
+    # host copy of K and V is laid out on the device and copied to
+    # page-locked host memory, then the device copies are dropped
     page_table = torch.from_numpy(case.page_table).to(dev)
     summ = torch.empty((B, H, N, 2, D), dtype=torch.int16, device=dev)
-    k_dev = torch.from_numpy(case.k_pool.view(np.int16)).to(dev)
-    kvr.kvr_build_summaries(d, k_dev, page_table, summ)
+    host_pools = []
+    for pool in (case.k_pool, case.v_pool):
+        p_dev = torch.from_numpy(pool.view(np.int16)).to(dev)
+        if not host_pools:
+            kvr.kvr_build_summaries(d, p_dev, page_table, summ)
+        hnd = p_dev[page_table.reshape(-1).long()].view(B, N, P, H, D).permute(0, 3, 1, 2, 4).contiguous()
+        h = torch.empty(hnd.shape, dtype=torch.int16).pin_memory()
+        h.copy_(hnd)
+        host_pools.append(h)
+        del p_dev, hnd
     torch.cuda.synchronize()
-    del k_dev
-    kh, vh = synth.host_hnd(case)
-    k_host = torch.from_numpy(kh.view(np.int16)).pin_memory()
-    v_host = torch.from_numpy(vh.view(np.int16)).pin_memory()
-    del kh, vh, case
+    k_host, v_host = host_pools
+    del case
+    torch.cuda.empty_cache()
     k_slots = torch.zeros((B, S, P, H, D), dtype=torch.int16, device=dev)
     v_slots = torch.zeros_like(k_slots)
     p2s = torch.empty((B, H, N), dtype=torch.int32, device=dev)
@@ -548,6 +593,7 @@ def run_gpu_recall(args, world, rank, local):
     host = kvr.kvr_host_kv(k_host.data_ptr(), v_host.data_ptr())
     wset = kvr.kvr_working_set(k_slots.data_ptr(), v_slots.data_ptr(), p2s.data_ptr(), s2p.data_ptr(), S)
     qs = torch.from_numpy(tr.q.view(np.int16).copy()).to(dev)   # [T][B][Hq][D]
+    q_host = torch.from_numpy(tr.q.view(np.int16).copy()).pin_memory()
     T = qs.shape[0]
     main_s = torch.cuda.current_stream()
     side = torch.cuda.Stream()
@@ -555,10 +601,10 @@ def run_gpu_recall(args, world, rank, local):
     ev_s.record()
     ev_r.record()
 
-    def timed(fn, reps):
+    def timed(fn, n):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         best = None
-        for _ in range(reps):
+        for _ in range(n):
             torch.cuda.synchronize()
             a.record()
             fn()
@@ -579,19 +625,14 @@ def run_gpu_recall(args, world, rank, local):
     wsel = torch.zeros(kvr.kvr_workspace_size(d, k, kvr.KVR_OP_SELECT), dtype=torch.uint8, device=dev)
     kvr.kvr_select_pages(d, qs[0], summ, page_table, k, sel0, None, None, wsel, wsel.numel())
     n_copied = torch.zeros(1, dtype=torch.int32, device=dev)
-
-    def cold_recall():
-        kvr.kvr_working_set_reset(d, wset)
-        torch.cuda.synchronize()
-
     recall_times = []
     for _ in range(5):
-        cold_recall()
+        kvr.kvr_working_set_reset(d, wset)
+        torch.cuda.synchronize()
         recall_times.append(timed(lambda: kvr.kvr_recall_pages(d, host, wset, sel0, sel0, None, k, None,
                                                                 n_copied), 1))
     recall_s = min(recall_times)
     recall_bytes = B * H * k * page_bytes
-    recall_gbs = recall_bytes / recall_s / 1e9
 
     # speculative steps with recall, replayed from a CUDA graph of T steps
     q_prev = torch.zeros((B, Hq, D), dtype=torch.int16, device=dev)
@@ -610,7 +651,7 @@ def run_gpu_recall(args, world, rank, local):
                                         ev_r)
 
     kvr.kvr_working_set_reset(d, wset)
-    for i in range(max(args.warmup, 3)):     # step 0 of the trace first (every head corrected)
+    for i in range(max(warmup, 3)):     # step 0 of the trace first (every head corrected)
         step(i)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
@@ -619,14 +660,14 @@ def run_gpu_recall(args, world, rank, local):
             step(i)
     graph.replay()
     torch.cuda.synchronize()
-    reps = max(1, args.steps // T)
-    n0 = int(n_copied.item())
-    props = torch.cuda.get_device_properties(dev)
-    uuid = str(getattr(props, "uuid", "") or "")
-    clocks = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or local))
-    time.sleep(0.3)
+    sampler = _clock_sampler(dev, local) if clocks else None
+    if sampler is not None:
+        time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
+    graph.replay()                      # untimed, right before the timed replays
+    torch.cuda.synchronize()
+    n0 = int(n_copied.item())
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
     for _ in range(reps):
@@ -634,67 +675,169 @@ def run_gpu_recall(args, world, rank, local):
     t1.record()
     torch.cuda.synchronize()
     barrier(world)
-    clk = clocks.stop()
+    clk = sampler.stop() if sampler is not None else None
     elapsed = t0.elapsed_time(t1) / 1e3
     n_steps = reps * T
     pages_per_step = (int(n_copied.item()) - n0) / n_steps
     value, t_max = aggregate(n_steps, elapsed, world)
     status = kvr.kvr_get_status()
 
-    # end to end through the public call: q in from pinned memory, output back, per step
-    q_host = torch.from_numpy(tr.q.view(np.int16).copy()).pin_memory()
+    # end to end through the public call: q in from pinned memory, output
+    # back, per step; untimed warm-up calls on the same buffers first
     out_host = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
     q_dev = torch.empty((B, Hq, D), dtype=torch.int16, device=dev)
-    n_e2e = min(n_steps, 320)
-    barrier(world)
-    torch.cuda.synchronize()
-    w0 = time.perf_counter()
-    for i in range(n_e2e):
+
+    def e2e_step(i):
         q_dev.copy_(q_host[i % T], non_blocking=True)
         step(i, q_dev)
         out_host.copy_(out, non_blocking=True)
         main_s.synchronize()
-    e2e_value, _ = aggregate(n_e2e, time.perf_counter() - w0, world)
-    status |= kvr.kvr_get_status()
 
+    for i in range(16):
+        e2e_step(i)
+    barrier(world)
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for i in range(e2e_calls):
+        e2e_step(i)
+    e2e_value, _ = aggregate(e2e_calls, time.perf_counter() - w0, world)
+    status |= kvr.kvr_get_status()
+    res = dict(wl=wl, tau=wl_trace.tau, S=S, T=T, steps=n_steps, value=value, t_max=t_max,
+               pages_per_step=pages_per_step, page_bytes=page_bytes, recall_s=recall_s,
+               recall_bytes=recall_bytes, link_gbs=link_gbs, e2e_value=e2e_value, e2e_calls=e2e_calls,
+               clk=clk, status=status)
+    del k_slots, v_slots, k_host, v_host, host_pools
+    torch.cuda.empty_cache()
+    return res
+
+
+def recall_roofline(r):
+    gbs = r["recall_bytes"] / r["recall_s"] / 1e9
+    return {"bound": "host_link", "achieved": round(gbs, 1), "peak": round(r["link_gbs"], 1), "unit": "GB/s",
+            "frac": round(gbs / r["link_gbs"], 4), "traffic": None,
+            "peak_kind": "measured in this run: pinned 1 GiB host-to-device copy, best of 3",
+            "kernel": "k_recall", "bytes_per_launch": r["recall_bytes"],
+            "launch_us": round(r["recall_s"] * 1e6, 3),
+            "how": "cold working set: all B*H*k pages of one selection recalled in one launch"}
+
+
+def recall_workload(r):
+    wl = r["wl"]
+    return (f"qwen3-4b-128k-host: {wl.batch} sequences x {wl.n_q_heads}/{wl.n_kv_heads} heads, head_dim "
+            f"{wl.head_dim}, context {wl.context}, page {wl.page_size}, top-k {wl.top_k} pages; K/V in "
+            f"page-locked host memory (head-major), {r['S']}-slot working set per (sequence, KV head) in HBM; "
+            f"speculative, tau {r['tau']}")
+
+
+def recall_summary(r):
+    return {"workload": recall_workload(r), "steps_per_s": round(r["value"], 2), "steps": r["steps"],
+            "ms_per_step": round(r["t_max"] / r["steps"] * 1e3, 5),
+            "recalled_pages_per_step": round(r["pages_per_step"], 2),
+            "recalled_gbs_per_step_rate": round(r["pages_per_step"] * r["page_bytes"] * r["value"] / 1e9, 2),
+            "roofline": recall_roofline(r), "e2e_steps_per_s": round(r["e2e_value"], 2),
+            "clocks": r["clk"], "device_status": r["status"]}
+
+
+def hbm_line(name, r, args, world):
+    """The JSON line of an HBM-resident workload as the headline."""
+    hbm, peak_kind = peaks()
+    achieved = r["attn_bytes"] / r["attn_avg"] / 1e9
+    wl = r["wl"]
+    B, Hq, D = wl.batch, wl.n_q_heads, wl.head_dim
+    cfg = hbm_config(name, r, world)
+    cfg["step"] = f"kvr_speculative_step{'_overlap' if args.step == 'overlap' else ''}"
     return {
         "metric": METRIC,
-        "value": round(value, 2),
+        "value": round(r["value"], 2),
         "unit": "steps/s",
         "n_gpus": world,
-        "steps": n_steps,
+        "steps": r["steps"],
         "warmup": args.warmup,
-        "ms_per_step": round(t_max / n_steps * 1e3, 5),
+        "ms_per_step": round(r["t_max"] / r["steps"] * 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": cfg,
+        "selected_kv_gbs": round(achieved, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": traffic_for("k_sparse_decode", name),
+                     "peak_kind": peak_kind, "kernel": "k_sparse_decode", "bytes_per_launch": r["attn_bytes"],
+                     "launch_us": round(r["attn_avg"] * 1e6, 3), "launches_timed": r["n_attn"]},
+        "kernels": hbm_kernels(r),
+        # k_page_scores, k_topk, k_sparse_decode (+ k_spec_decide and a second attention launch)
+        "gpu_launches": (5 if args.step == "overlap" else 3) * r["steps"],
+        "e2e": {"value": round(r["e2e_value"], 2), "unit": "steps/s",
+                "h2d_bytes_per_step": B * Hq * D * 2, "d2h_bytes_per_step": B * Hq * D * 4,
+                "how": f"{r['e2e_calls']} eager kvr_speculative_step"
+                       f"{'_overlap' if args.step == 'overlap' else ''} calls after 200 untimed ones, q copied in "
+                       f"from pinned host memory and the fp32 output copied back every step, stream synchronised "
+                       f"per step"},
+        "clocks": r["clk"],
+        "device_status": r["status"],
+    }
+
+
+def recall_line(r, args, world):
+    """The JSON line of the host-resident workload as the headline."""
+    wl = r["wl"]
+    B, Hq, D = wl.batch, wl.n_q_heads, wl.head_dim
+    return {
+        "metric": METRIC,
+        "value": round(r["value"], 2),
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": r["steps"],
+        "warmup": args.warmup,
+        "ms_per_step": round(r["t_max"] / r["steps"] * 1e3, 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
         "config": {
-            "workload": f"{args.workload}: {B} sequences x {Hq}/{H} heads, head_dim {D}, context {wl.context}, "
-                        f"page {P}, top-k {k} pages; K/V in page-locked host memory (head-major), "
-                        f"{S}-slot working set per (sequence, KV head) in HBM; speculative, tau {wl_trace.tau}",
-            "batch": B, "n_q_heads": Hq, "n_kv_heads": H, "head_dim": D, "context": wl.context,
-            "page_size": P, "top_k": k, "tau": wl_trace.tau, "storage": "bf16", "accumulate": "f32",
+            "workload": recall_workload(r),
+            "batch": B, "n_q_heads": Hq, "n_kv_heads": wl.n_kv_heads, "head_dim": D, "context": wl.context,
+            "page_size": wl.page_size, "top_k": wl.top_k, "tau": r["tau"], "storage": "bf16",
+            "accumulate": "f32",
             "parallelism": f"{world} independent replica(s)" if world > 1 else "1 GPU",
             "l2": "the host cache (2 GiB) does not fit L2; each recalled page is read from host memory once",
-            "graph": f"steps replayed from a CUDA graph of {T} steps (the {T}-step query trace, repeated)",
+            "graph": f"steps replayed from a CUDA graph of {r['T']} steps (the {r['T']}-step query trace, "
+                     f"repeated)",
         },
-        "recalled_pages_per_step": round(pages_per_step, 2),
-        "roofline": {"bound": "host_link", "achieved": round(recall_gbs, 1), "peak": round(link_gbs, 1),
-                     "unit": "GB/s", "frac": round(recall_gbs / link_gbs, 4), "traffic": None,
-                     "peak_kind": "measured in this run: pinned 1 GiB host-to-device copy, best of 3",
-                     "kernel": "k_recall", "bytes_per_launch": recall_bytes,
-                     "launch_us": round(recall_s * 1e6, 3),
-                     "how": "cold working set: all B*H*k pages of one selection recalled in one launch"},
-        "gpu_launches": 5 * n_steps,  # k_page_scores, k_topk, k_recall, k_sparse_decode x2
-        "e2e": {"value": round(e2e_value, 2), "unit": "steps/s",
+        "recalled_pages_per_step": round(r["pages_per_step"], 2),
+        "roofline": recall_roofline(r),
+        "gpu_launches": 5 * r["steps"],  # k_page_scores, k_topk, k_recall, k_sparse_decode x2
+        "e2e": {"value": round(r["e2e_value"], 2), "unit": "steps/s",
                 "h2d_bytes_per_step": B * Hq * D * 2, "d2h_bytes_per_step": B * Hq * D * 4,
-                "how": f"{n_e2e} eager kvr_speculative_step_recall calls, q copied in from pinned host memory "
-                       f"and the fp32 output copied back every step, stream synchronised per step"},
-        "clocks": clk,
-        "device_status": status,
+                "how": f"{r['e2e_calls']} eager kvr_speculative_step_recall calls after 16 untimed ones, q "
+                       f"copied in from pinned host memory and the fp32 output copied back every step, stream "
+                       f"synchronised per step"},
+        "clocks": r["clk"],
+        "device_status": r["status"],
     }
+
+
+def run_gpu(args, world, rank, local):
+    """The line of --workload, plus (unless --no-extras) compact records of
+    the other HBM-resident workload and of the host-resident one."""
+    e2e_calls = 2000
+    if args.workload.endswith("-host"):
+        r = measure_recall(args, world, local, reps=max(1, -(-args.steps // 32)), warmup=args.warmup,
+                           e2e_calls=e2e_calls)
+        return recall_line(r, args, world)
+    r = measure_hbm(args.workload, args, world, local, args.steps, args.warmup, e2e_calls,
+                    kernel_launches=args.kernel_launches)
+    line = hbm_line(args.workload, r, args, world)
+    if not args.no_extras:
+        other = "llama3.1-8b-32k" if args.workload == "qwen3-4b-128k" else "qwen3-4b-128k"
+        r2 = measure_hbm(other, args, world, local, 640, args.warmup, 1000,
+                         kernel_launches=args.kernel_launches, clocks=True)
+        line["also"] = {other: hbm_summary(other, r2)}
+        rr = measure_recall(args, world, local, reps=8, warmup=args.warmup, e2e_calls=96)
+        line["also"]["qwen3-4b-128k-host"] = recall_summary(rr)
+    return line
 
 
 # ---------------------------------------------------------------- multi-layer pipeline
@@ -863,9 +1006,7 @@ def run_gpu_pipeline(args, world, rank, local):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / 1e3
 
-    props = torch.cuda.get_device_properties(dev)
-    uuid = str(getattr(props, "uuid", "") or "")
-    clocks = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or local))
+    clocks = _clock_sampler(dev, local)
     time.sleep(0.3)
     barrier(world)
     t_pipe = timed(g_pipe)
@@ -960,7 +1101,11 @@ def main():
     ap.add_argument("--steps", type=int, default=64000)
     ap.add_argument("--warmup", type=int, default=128)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llama3.1-8b-32k", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="qwen3-4b-128k", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-extras", action="store_true",
+                    help="only the --workload line (no records of the other workloads under 'also')")
+    ap.add_argument("--kernel-launches", type=int, default=1280,
+                    help="launches timed for each per-kernel figure (selection, attention)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--copies", type=int, default=4, help="rotating cache copies (L2-cold timing needs >= 3)")
     ap.add_argument("--step", default="sequential", choices=["sequential", "overlap", "pipeline"],
@@ -990,7 +1135,7 @@ def main():
     if args.step == "pipeline":
         res = run_gpu_pipeline(args, world, rank, local)
     else:
-        res = (run_gpu_recall if args.workload.endswith("-host") else run_gpu)(args, world, rank, local)
+        res = run_gpu(args, world, rank, local)
     if rank == 0:
         if args.step == "pipeline":
             res["cpu_baseline"] = None

@@ -455,15 +455,21 @@ uint64_t kvr_kv_bytes(int64_t n_layers, int64_t n_kv_heads, int64_t head_dim,
  * the library keeps until the process exits.  The caller still passes all
  * inputs and outputs (q, summ, page_table, sel, sel_phys, scores_opt as in
  * kvr_select_pages).
- *   - Limit: B * H * N * 4 bytes of scores plus 4 bytes per (b, g) must fit in
- *     KVR_NOALLOC_SCRATCH_BYTES (about one million page scores); larger
- *     problems return KVR_ERR_SCRATCH_LIMIT before anything is enqueued.
- *   - The first call on each device looks up the array's device address
- *     (with that device current) and caches it; make that first call before
- *     any stream capture.
- *   - All calls share the one array: calls that overlap on the GPU (on
- *     different streams, or from several threads) race and must be
- *     serialised by the caller.
+ *   - Limit: the scratch is the score rows, B * H * N * 4 bytes, plus one
+ *     4-byte word per (b, g), each part rounded up to a multiple of 256
+ *     bytes: round256(B*H*N*4) + round256(B*H*4) <= KVR_NOALLOC_SCRATCH_BYTES
+ *     (about one million page scores; B*H = 64 allows N up to 16383).
+ *     Larger problems return KVR_ERR_SCRATCH_LIMIT before anything is
+ *     enqueued.
+ *   - Every call looks up the array's device address on the current device
+ *     (a host-side query; it allocates nothing and stays valid across a
+ *     cudaDeviceReset).  The first call on a device may make the driver load
+ *     the library's device code, so make that first call before any stream
+ *     capture.
+ *   - All calls share the one array, which keeps the last call's contents
+ *     (every score is written before it is read, so no call depends on
+ *     them): calls that overlap on the GPU (on different streams, or from
+ *     several threads) race and must be serialised by the caller.
  * It never calls cudaMalloc, cudaFree or any allocating routine. */
 #define KVR_NOALLOC_SCRATCH_BYTES 4194304u /* 4 MiB */
 int kvr_select_pages_noalloc(const kvr_dims *dims, const uint16_t *q,

@@ -19,7 +19,10 @@
 // heads, and every CTA gets every worker's (m, l).  After one cluster
 // barrier each CTA merges its slice from its own shared memory with a
 // log-sum-exp rescale and writes it to `out`; no CTA reads another's shared
-// memory after the barrier, so each leaves as soon as it is done.  Nothing of
+// memory after the barrier, so each leaves as soon as it is done.  Before the
+// first push, a handshake (every thread arrives right after the setup and
+// waits before pushing) makes sure every CTA of the cluster has started, as
+// distributed shared memory requires.  Nothing of
 // the split goes through global memory and no second kernel is needed.
 //
 // Inside a CTA (CPS per SM) the warps share the shared-memory ring:
@@ -276,8 +279,13 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
   // the previous kernel; every global read and write comes after this wait.
   pdl_wait();
   if (tid == 0) pdl_launch_dependents();
-  // the whole cluster holds one unit, so this exit is uniform over it
+  // the whole cluster holds one unit, so this exit is uniform over it (no
+  // thread of the cluster touches another CTA's shared memory)
   if (!attn_unit_active(filter, filter_mode, u)) return;
+  // Start handshake of the cluster: no thread may write another CTA's shared
+  // memory before that CTA has started; every thread arrives here and waits
+  // (cluster_wait) before the first push of the merge.
+  cluster_arrive_relaxed();
 
   if (warp == NC) {
     // ---------------------------------------------------------- producer warp
@@ -361,6 +369,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
       for (int j = max(0, i - R); j < i; ++j)
         mbar_wait(&full[lane * R + j % R], static_cast<uint32_t>((j / R) & 1));
     __syncwarp();
+    cluster_wait();  // the start handshake's second half (see above)
   } else {
     // ---------------------------------------------------------- consumer warps
     const int cw = warp;
@@ -430,6 +439,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
       if (2 * tq + 1 < G) stg_ml[2 * tq + 1] = make_float2(m_run[1], l1);
     }
     __syncwarp();
+    cluster_wait();  // every CTA of the cluster has started: pushes may begin
     const int j = rank * NC + cw;  // this worker's index in the cluster
     const uint32_t rc0 = smem_addr(s_recv), ml0 = smem_addr(s_mlr);
 #pragma unroll

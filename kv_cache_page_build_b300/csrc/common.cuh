@@ -1,8 +1,7 @@
 // common.cuh -- device helpers shared by the libkvr kernels (sm_103a).
 //
 // Inline PTX for the Blackwell async-copy path: mbarrier transaction
-// barriers, the bulk copy engine (cp.async.bulk, 1D) and the tensor copy
-// engine (cp.async.bulk.tensor, tiled 3D).  Every wait on a barrier is
+// barriers and the tensor copy engine (cp.async.bulk.tensor, tiled 2D/3D).  Every wait on a barrier is
 // bounded by the global timer and reports a timeout through the status word
 // instead of spinning forever.
 #pragma once
@@ -188,17 +187,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
 
 // ---------------------------------------------------------------- copy engines
 
-// 1D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
-// both addresses 16-byte aligned).
-__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,
-                                              uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
 // Tiled 2D tensor copy global -> shared (coordinates innermost first).
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int c0, int c1) {
@@ -252,6 +240,11 @@ __device__ __forceinline__ void cluster_sync() {
 // The two halves of cluster_sync, for work between them.
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+// Arrive without memory ordering: only says "this thread has started", for
+// the handshake that must precede any access to another CTA's shared memory.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");

@@ -86,6 +86,35 @@ int ensure_smem(const void *kern, size_t bytes, int *max_set) {
   return KVR_OK;
 }
 
+// Prefer the largest shared-memory carveout for a kernel with little or no
+// shared memory of its own (set once per device and kernel).  An SM's split
+// between L1 and shared memory follows the preferences of the kernels
+// resident on it, and the attention's ring needs most of an SM's shared
+// memory: the kernels that run before or beside it (top-k, the speculative
+// decision, recall, append, the stand-in) take this preference so that an SM
+// holding one of their CTAs can still take an attention CTA at once.
+std::mutex g_carve_mu;
+struct Carved {
+  int dev;
+  const void *kern;
+};
+Carved g_carved[256];
+int g_n_carved = 0;
+
+int prefer_max_shared(const void *kern) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(g_carve_mu);
+  for (int i = 0; i < g_n_carved; ++i)
+    if (g_carved[i].dev == dev && g_carved[i].kern == kern) return KVR_OK;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return cuda_fail(e, "shared memory carveout attribute");
+  if (g_n_carved < 256) g_carved[g_n_carved++] = Carved{dev, kern};
+  return KVR_OK;
+}
+
 // ---------------------------------------------------------------- workspace
 
 struct SelectWs {
@@ -292,23 +321,28 @@ int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
   cudaError_t e;
   if (d->n_pages <= 256 * 4) {
     cfg.blockDim = dim3(256);
+    if (int rc = prefer_max_shared(reinterpret_cast<const void *>(k_topk<G, 256, 4>))) return rc;
     e = cudaLaunchKernelEx(&cfg, k_topk<G, 256, 4>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
                            sel, sel_phys, spec, seq_len, d->page_size);
   } else if (d->n_pages <= 256 * 8) {
     cfg.blockDim = dim3(256);
+    if (int rc = prefer_max_shared(reinterpret_cast<const void *>(k_topk<G, 256, 8>))) return rc;
     e = cudaLaunchKernelEx(&cfg, k_topk<G, 256, 8>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
                            sel, sel_phys, spec, seq_len, d->page_size);
   } else if (d->n_pages <= 512 * 8) {
     cfg.blockDim = dim3(512);
+    if (int rc = prefer_max_shared(reinterpret_cast<const void *>(k_topk<G, 512, 8>))) return rc;
     e = cudaLaunchKernelEx(&cfg, k_topk<G, 512, 8>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
                            sel, sel_phys, spec, seq_len, d->page_size);
   } else if (d->n_pages <= 512 * 16) {
     cfg.blockDim = dim3(512);
+    if (int rc = prefer_max_shared(reinterpret_cast<const void *>(k_topk<G, 512, 16>))) return rc;
     e = cudaLaunchKernelEx(&cfg, k_topk<G, 512, 16>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
                            sel, sel_phys, spec, seq_len, d->page_size);
   } else {
     cfg.blockDim = dim3(1024);
     static_assert(1024 * 16 >= kMaxPages, "the largest top-k launch covers every page count");
+    if (int rc = prefer_max_shared(reinterpret_cast<const void *>(k_topk<G, 1024, 16>))) return rc;
     e = cudaLaunchKernelEx(&cfg, k_topk<G, 1024, 16>, q, ptab, d->n_kv_heads, d->n_pages, k, ws_sc,
                            sel, sel_phys, spec, seq_len, d->page_size);
   }
@@ -494,6 +528,7 @@ int launch_recall(const kvr_dims *d, const kvr_host_kv *host, const kvr_working_
   const size_t smem = (2 * static_cast<size_t>(S) + k) * sizeof(int32_t);
   const dim3 grid(d->n_kv_heads, d->batch);
 #define KVR_RECALL(PP)                                                                          \
+  if (int rc2 = prefer_max_shared(reinterpret_cast<const void *>(k_recall<PP>))) return rc2;   \
   k_recall<PP><<<grid, kRecallThreads, smem, st>>>(                                             \
       static_cast<const uint16_t *>(kh), static_cast<const uint16_t *>(vh), wset->k_slots,      \
       wset->v_slots, wset->page2slot, wset->slot2page, S, sel_new, protect, corrected,          \
@@ -535,6 +570,7 @@ SpecArgs no_spec() {
 template <int G>
 int launch_spec_decide_g(const kvr_dims *d, const uint16_t *q, const int32_t *ptab, int k,
                          const SpecArgs &spec, cudaStream_t st) {
+  if (int rc = prefer_max_shared(reinterpret_cast<const void *>(k_spec_decide<G>))) return rc;
   k_spec_decide<G><<<dim3(d->n_kv_heads, d->batch), 32 * G, 0, st>>>(q, ptab, d->n_kv_heads,
                                                                      d->n_pages, k, spec);
   return check_launch("k_spec_decide");
@@ -622,6 +658,7 @@ int kvr_append_kv(const kvr_dims *dims, const uint16_t *k_new, const uint16_t *v
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const dim3 grid(dims->batch);
 #define KVR_APPEND(PP)                                                                        \
+  if ((rc = prefer_max_shared(reinterpret_cast<const void *>(k_append<PP>)))) return rc;       \
   k_append<PP><<<grid, kAppendThreads, 0, st>>>(k_new, v_new, page_table, seq_len, k_pool,    \
                                                 v_pool, summ, dims->n_kv_heads, dims->n_pages, \
                                                 dims->n_phys_pages)
@@ -933,6 +970,7 @@ static int launch_stand_in(const kvr_stand_in *c, uint64_t offset, uint64_t byte
   const uint64_t cap = static_cast<uint64_t>(sms) * kStandInCPS;
   const unsigned grid = static_cast<unsigned>(std::max<uint64_t>(1, std::min(want, cap)));
   const uint8_t *base = static_cast<const uint8_t *>(c->weights) + offset;
+  if (int rc = prefer_max_shared(reinterpret_cast<const void *>(k_stand_in))) return rc;
   k_stand_in<<<grid, kStandInThreads, 0, st>>>(reinterpret_cast<const uint4 *>(base), n16, c->sink);
   return check_launch("k_stand_in");
 }
@@ -1153,29 +1191,19 @@ uint64_t kvr_kv_bytes(int64_t n_layers, int64_t n_kv_heads, int64_t head_dim, in
 // score rows) in this fixed device array instead of a caller
 // workspace, for callers that may not allocate device memory.  Host code
 // must not pass the array's name to a kernel (on the host it only stands in
-// for the symbol); the device address is looked up once per device below.
+// for the symbol); the device address is looked up on every call below.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[KVR_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up on
-// the first call per device, then cached).
+// Device address of the scratch array on the current device.  Looked up on
+// every call (a host-side query that allocates nothing), so an address from
+// a context that was since destroyed (cudaDeviceReset) is never reused.
 int noalloc_scratch(void **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices) return KVR_ERR_UNSUPPORTED_SHAPE;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "scratch symbol address");
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
+  void *p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "scratch symbol address");
+  *out = p;
   return KVR_OK;
 }
 
