@@ -270,44 +270,53 @@ int make_summ_map(CUtensorMap *map, const void *summ, long long F, int rows) {
 
 int sm_count(int *out);
 
+// Which kernels of the selection a launch_select call enqueues.
+constexpr int kSelScores = 1;  // k_page_scores
+constexpr int kSelTopk = 2;    // k_topk
+constexpr int kSelBoth = kSelScores | kSelTopk;
+
 template <int G>
 int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
                     const int32_t *ptab, int k, SelectWs w, int32_t *sel, int32_t *sel_phys,
                     float *scores, const SpecArgs &spec, cudaStream_t st, bool pdl_first,
-                    const int32_t *seq_len) {
-  // 1. page scores: kScCPS CTAs per SM, each warp a worker over a contiguous
-  //    range of the flat page list
-  auto kern = k_page_scores<G>;
-  static int max_set[kMaxDevices] = {};
-  if (int rc = ensure_smem(reinterpret_cast<const void *>(kern), kScSmem, max_set)) return rc;
-  int sms = 0;
-  if (int rc = sm_count(&sms)) return rc;
-  const long long F = static_cast<long long>(d->batch) * d->n_kv_heads * d->n_pages;
-  const long long per_cta = static_cast<long long>(kScMinPagesPerWorker) * kScNC;
-  long long n_ctas = std::min<long long>(static_cast<long long>(sms) * kScCPS, (F + per_cta - 1) / per_cta);
-  n_ctas = std::max<long long>(1, std::min<long long>(n_ctas, kScMaxCtas));
-  CUtensorMap tsm, tsm8;
-  if (int rc = make_summ_map(&tsm, summ, F, kScPages)) return rc;
-  if (int rc = make_summ_map(&tsm8, summ, F, 8)) return rc;
-  {  // a programmatic dependent launch (unless the stream's last operation is
-     // an event wait): the setup overlaps the kernel before it
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(n_ctas));
-    cfg.blockDim = dim3(kScThreads);
-    cfg.dynamicSmemBytes = kScSmem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl_first ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tsm, tsm8, q, d->n_kv_heads, d->n_pages, F,
-                                             w.scores, scores);
-    if (e != cudaSuccess) return cuda_fail(e, "k_page_scores");
+                    const int32_t *seq_len, int parts) {
+  if (parts & kSelScores) {
+    // 1. page scores: kScCPS CTAs per SM, each warp a worker over a contiguous
+    //    range of the flat page list
+    auto kern = k_page_scores<G>;
+    static int max_set[kMaxDevices] = {};
+    if (int rc = ensure_smem(reinterpret_cast<const void *>(kern), kScSmem, max_set)) return rc;
+    int sms = 0;
+    if (int rc = sm_count(&sms)) return rc;
+    const long long F = static_cast<long long>(d->batch) * d->n_kv_heads * d->n_pages;
+    const long long per_cta = static_cast<long long>(kScMinPagesPerWorker) * kScNC;
+    long long n_ctas = std::min<long long>(static_cast<long long>(sms) * kScCPS, (F + per_cta - 1) / per_cta);
+    n_ctas = std::max<long long>(1, std::min<long long>(n_ctas, kScMaxCtas));
+    CUtensorMap tsm, tsm8;
+    if (int rc = make_summ_map(&tsm, summ, F, kScPages)) return rc;
+    if (int rc = make_summ_map(&tsm8, summ, F, 8)) return rc;
+    {  // a programmatic dependent launch (unless the stream's last operation is
+       // an event wait): the setup overlaps the kernel before it
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(n_ctas));
+      cfg.blockDim = dim3(kScThreads);
+      cfg.dynamicSmemBytes = kScSmem;
+      cfg.stream = st;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = pdl_first ? 1 : 0;
+      const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tsm, tsm8, q, d->n_kv_heads, d->n_pages, F,
+                                               w.scores, scores);
+      if (e != cudaSuccess) return cuda_fail(e, "k_page_scores");
+    }
   }
-  // 2. top-k per unit: a programmatic dependent launch; threads x keys per
-  //    thread by page count (measured: fewer than 8 keys per thread costs more
-  //    in cross-warp steps than it saves)
+  if (!(parts & kSelTopk)) return KVR_OK;
+  // 2. top-k per unit: a programmatic dependent launch right after the
+  //    scores (an ordinary launch when it opens the stream's work after an
+  //    event wait); threads x keys per thread by page count (measured: fewer
+  //    than 8 keys per thread costs more in cross-warp steps than it saves)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d->n_kv_heads, d->batch);
   cfg.dynamicSmemBytes = 0;
@@ -316,7 +325,7 @@ int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = (parts & kSelScores) || pdl_first ? 1 : 0;
   const float *ws_sc = static_cast<const float *>(w.scores);
   cudaError_t e;
   if (d->n_pages <= 256 * 4) {
@@ -356,12 +365,12 @@ int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
 int launch_select(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
                   const int32_t *ptab, int k, SelectWs w, int32_t *sel, int32_t *sel_phys,
                   float *scores, const SpecArgs &spec, cudaStream_t st, bool pdl_first = true,
-                  const int32_t *seq_len = nullptr) {
+                  const int32_t *seq_len = nullptr, int parts = kSelBoth) {
   switch (d->n_q_heads / d->n_kv_heads) {
-    case 1: return launch_select_g<1>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len);
-    case 2: return launch_select_g<2>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len);
-    case 4: return launch_select_g<4>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len);
-    default: return launch_select_g<8>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len);
+    case 1: return launch_select_g<1>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len, parts);
+    case 2: return launch_select_g<2>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len, parts);
+    case 4: return launch_select_g<4>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len, parts);
+    default: return launch_select_g<8>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len, parts);
   }
 }
 
@@ -850,18 +859,24 @@ int kvr_speculative_step_overlap(const kvr_dims *dims, kvr_spec_state *st, const
   cudaStream_t side = static_cast<cudaStream_t>(side_stream);
   cudaEvent_t ed = static_cast<cudaEvent_t>(ev_decide), es = static_cast<cudaEvent_t>(ev_select);
   SpecArgs sa = spec_args(st, tau, corrected, cbar_opt, sel_used, sel_used_phys, nullptr, 0);
-  // 1. the decision per (b, g); reused heads get sel_used from sel_prev
+  const SelectWs sw = carve_select(dims, (uint8_t *)ws);
+  // 1. the decision per (b, g) (reused heads get sel_used from sel_prev),
+  //    then the page scores, both on `stream`
   rc = launch_spec_decide(dims, q_t, page_table, top_k, sa, s);
   if (rc) return rc;
   st->step += 1;
+  sa.decided = 1;
+  rc = launch_select(dims, q_t, summ, page_table, top_k, sw, nullptr, nullptr, nullptr, sa, s, true,
+                     nullptr, kSelScores);
+  if (rc) return rc;
   cudaError_t e = cudaEventRecord(ed, s);
   if (e != cudaSuccess) return cuda_fail(e, "record decide event");
-  // 2. side stream: the new selection (becomes sel_prev; sel_used of the corrected heads)
+  // 2. side stream: the top-k of the new selection (becomes sel_prev; sel_used
+  //    of the corrected heads), beside the reused heads' attention
   e = cudaStreamWaitEvent(side, ed, 0);
   if (e != cudaSuccess) return cuda_fail(e, "side stream wait");
-  sa.decided = 1;
-  rc = launch_select(dims, q_t, summ, page_table, top_k, carve_select(dims, (uint8_t *)ws), nullptr,
-                     nullptr, nullptr, sa, side, false);
+  rc = launch_select(dims, q_t, summ, page_table, top_k, sw, nullptr, nullptr, nullptr, sa, side, false,
+                     nullptr, kSelTopk);
   if (rc) return rc;
   e = cudaEventRecord(es, side);
   if (e != cudaSuccess) return cuda_fail(e, "record select event");
@@ -1058,20 +1073,22 @@ int kvr_pipeline_step(const kvr_dims *dims, int32_t n_layers, kvr_layer *layers,
     KVR_TRY(launch_stand_in(compute, 0, qkv, s));
     KVR_TRY(mark(l, 1, s));
     if (!L.host) {
-      // the decision on the main stream, the selection beside the reused
-      // heads' attention (as kvr_speculative_step_overlap)
+      // the decision and the page scores on the main stream, the top-k
+      // beside the reused heads' attention (as kvr_speculative_step_overlap)
       SpecArgs sa = spec_args(L.st, tau, L.corrected, L.cbar_opt, L.sel_used, L.sel_used_idx,
                               nullptr, 0);
+      const SelectWs sw = carve_select(dims, static_cast<uint8_t *>(L.ws));
       KVR_TRY(launch_spec_decide(dims, L.q, L.page_table, top_k, sa, s));
       L.st->step += 1;
+      sa.decided = 1;
+      KVR_TRY(launch_select(dims, L.q, L.summ, L.page_table, top_k, sw, nullptr, nullptr, nullptr, sa,
+                            s, true, nullptr, kSelScores));
       KVR_TRY(mark(l, 2, s));
       KVR_TRY(record(L.ev[0], s));
       KVR_TRY(wait(side, L.ev[0]));
       KVR_TRY(mark(l, 7, side));
-      sa.decided = 1;
-      KVR_TRY(launch_select(dims, L.q, L.summ, L.page_table, top_k,
-                            carve_select(dims, static_cast<uint8_t *>(L.ws)), nullptr, nullptr,
-                            nullptr, sa, side, false));
+      KVR_TRY(launch_select(dims, L.q, L.summ, L.page_table, top_k, sw, nullptr, nullptr, nullptr, sa,
+                            side, false, nullptr, kSelTopk));
       KVR_TRY(mark(l, 8, side));
       KVR_TRY(mark(l, 9, side));   // before ev[1], which joins them to `stream`
       KVR_TRY(mark(l, 10, side));

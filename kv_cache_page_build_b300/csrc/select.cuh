@@ -377,21 +377,84 @@ __global__ void __launch_bounds__(NT, 1)
   // pages the sequence has started (all N without lengths); only these rank
   const int Nv = seq_len ? min(N, max(0, (seq_len[b] + P - 1) / P)) : N;
 
-  // Inputs of the speculative mode, loaded now and used after the top-k: the
-  // query slices and the previous selection.  Safe before the wait:
-  // k_page_scores, the kernel this one depends on, passed its own wait before
-  // letting this one start, and writes neither.
-  uint2 qa = make_uint2(0u, 0u), qb = make_uint2(0u, 0u);
-  const bool cos_lane = spec.enabled && !spec.decided && spec.step > 0 && warp < G;
-  if (cos_lane) {
-    const size_t qo = (static_cast<size_t>(b) * Hq + g * G + warp) * kD + 4 * lane;
-    qa = *reinterpret_cast<const uint2 *>(q + qo);
-    qb = *reinterpret_cast<const uint2 *>(spec.q_prev + qo);
+  // ---- speculative mode: group similarity and the correction decision,
+  // taken before the wait so that it overlaps the scores kernel.  It reads
+  // q_t, q_prev, sel_prev and the page table (or working-set map) and writes
+  // corrected, cbar, q_prev and the reused heads' sel_used: k_page_scores,
+  // the kernel this one depends on, touches none of them, and it passed its
+  // own wait (so every kernel before it has finished) before letting this
+  // one start.
+  const int32_t *ptab = page_table ? page_table + static_cast<size_t>(b) * N : nullptr;
+  bool corrected = true;
+  if (spec.enabled && !spec.decided) {
+    if (spec.step > 0 && warp < G) {
+      const size_t qo = (static_cast<size_t>(b) * Hq + g * G + warp) * kD + 4 * lane;
+      const uint2 qa = *reinterpret_cast<const uint2 *>(q + qo);
+      const uint2 qb = *reinterpret_cast<const uint2 *>(spec.q_prev + qo);
+      const float x[4] = {bf_lo(qa.x), bf_hi(qa.x), bf_lo(qa.y), bf_hi(qa.y)};
+      const float y[4] = {bf_lo(qb.x), bf_hi(qb.x), bf_lo(qb.y), bf_hi(qb.y)};
+      float dot = 0.f, nx = 0.f, ny = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        dot = fmaf(x[i], y[i], dot);
+        nx = fmaf(x[i], x[i], nx);
+        ny = fmaf(y[i], y[i], ny);
+      }
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) {
+        dot += __shfl_xor_sync(0xffffffffu, dot, m);
+        nx += __shfl_xor_sync(0xffffffffu, nx, m);
+        ny += __shfl_xor_sync(0xffffffffu, ny, m);
+      }
+      if (lane == 0) s_cos[warp] = (nx > 0.f && ny > 0.f) ? dot / (sqrtf(nx) * sqrtf(ny)) : 0.f;
+    }
+    __syncthreads();
+    // every thread takes the same decision from the same values
+    float cb = __int_as_float(0x7fc00000);  // NaN: no previous query at step 0
+    if (spec.step > 0) {
+      float sum = 0.f;
+      for (int h = 0; h < G; ++h) sum += s_cos[h];
+      cb = sum / G;
+      corrected = cb < spec.tau;
+    }
+    if (tid == 0) {
+      spec.corrected[unit] = corrected ? 1 : 0;
+      if (spec.cbar) spec.cbar[unit] = cb;
+    }
+    // q_prev <- q_t for this group's heads (only this CTA reads them; every
+    // read above is done)
+    for (int i = tid; i < G * kD / 8; i += NT) {
+      const size_t off = (static_cast<size_t>(b) * Hq + g * G) * kD + 8 * i;
+      *reinterpret_cast<uint4 *>(spec.q_prev + off) = *reinterpret_cast<const uint4 *>(q + off);
+    }
+    if (!corrected) {  // reuse: sel_used <- previous selection (replaced only after the top-k)
+      for (int i = tid; i < k; i += NT) {
+        const int p = spec.sel_prev[unit * k + i];
+        spec.sel_used[unit * k + i] = p;
+        if (spec.sel_used_phys) {
+          int phys = -1;
+          if (p >= 0 && p < N)
+            phys = spec.page2slot
+                       ? (spec.page2slot[unit * N + p] >= 0
+                              ? b * spec.n_slots + spec.page2slot[unit * N + p]
+                              : -1)
+                       : ptab[p];
+          spec.sel_used_phys[unit * k + i] = phys;
+        }
+      }
+    }
   }
-  const int sp0 = spec.enabled && !spec.decided && tid < k ? spec.sel_prev[unit * k + tid] : -1;
   for (int i = tid; i < 2 * kSelBins; i += NT) (&s_hist[0][0])[i] = 0u;
+  // page-table entries of this thread's pages, for the physical ids of the
+  // selected ones (the page table is an input no kernel of the step writes)
+  const bool want_phys = spec.enabled ? (spec.sel_used_phys && !spec.page2slot && (spec.decided || corrected))
+                                      : sel_phys_out != nullptr;
+  int phys[KPT];
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) phys[j] = want_phys && base + 32 * j < Nv ? __ldg(ptab + base + 32 * j) : -1;
 
   pdl_wait();  // the scores of k_page_scores are complete and visible
+  if (spec.enabled && spec.decided) corrected = spec.corrected[unit] != 0;  // k_spec_decide's decision
 
   // the keys, all loads in flight at once, and their range
   const float *row = ws_scores + unit * N;
@@ -499,67 +562,6 @@ __global__ void __launch_bounds__(NT, 1)
     buf ^= 1;
   }
 
-  // ---- speculative mode: group similarity and the correction decision
-  const int32_t *ptab = page_table ? page_table + static_cast<size_t>(b) * N : nullptr;
-  bool corrected = true;
-  if (spec.enabled && spec.decided) {
-    corrected = spec.corrected[unit] != 0;  // k_spec_decide's decision (complete before the scores)
-    __syncthreads();                        // every read of s_w* is done
-  } else if (spec.enabled) {
-    if (cos_lane) {
-      const float x[4] = {bf_lo(qa.x), bf_hi(qa.x), bf_lo(qa.y), bf_hi(qa.y)};
-      const float y[4] = {bf_lo(qb.x), bf_hi(qb.x), bf_lo(qb.y), bf_hi(qb.y)};
-      float dot = 0.f, nx = 0.f, ny = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        dot = fmaf(x[i], y[i], dot);
-        nx = fmaf(x[i], x[i], nx);
-        ny = fmaf(y[i], y[i], ny);
-      }
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) {
-        dot += __shfl_xor_sync(0xffffffffu, dot, m);
-        nx += __shfl_xor_sync(0xffffffffu, nx, m);
-        ny += __shfl_xor_sync(0xffffffffu, ny, m);
-      }
-      if (lane == 0) s_cos[warp] = (nx > 0.f && ny > 0.f) ? dot / (sqrtf(nx) * sqrtf(ny)) : 0.f;
-    }
-    __syncthreads();
-    // every thread takes the same decision from the same values
-    float cb = __int_as_float(0x7fc00000);  // NaN: no previous query at step 0
-    if (spec.step > 0) {
-      float sum = 0.f;
-      for (int h = 0; h < G; ++h) sum += s_cos[h];
-      cb = sum / G;
-      corrected = cb < spec.tau;
-    }
-    if (tid == 0) {
-      spec.corrected[unit] = corrected ? 1 : 0;
-      if (spec.cbar) spec.cbar[unit] = cb;
-    }
-    // q_prev <- q_t for this group's heads (only this CTA reads them)
-    for (int i = tid; i < G * kD / 8; i += NT) {
-      const size_t off = (static_cast<size_t>(b) * Hq + g * G) * kD + 8 * i;
-      *reinterpret_cast<uint4 *>(spec.q_prev + off) = *reinterpret_cast<const uint4 *>(q + off);
-    }
-    if (!corrected) {  // reuse: sel_used <- previous selection (read before it is replaced)
-      for (int i = tid; i < k; i += NT) {
-        const int p = i == tid ? sp0 : spec.sel_prev[unit * k + i];
-        spec.sel_used[unit * k + i] = p;
-        if (spec.sel_used_phys) {
-          int phys = -1;
-          if (p >= 0 && p < N)
-            phys = spec.page2slot
-                       ? (spec.page2slot[unit * N + p] >= 0
-                              ? b * spec.n_slots + spec.page2slot[unit * N + p]
-                              : -1)
-                       : ptab[p];
-          spec.sel_used_phys[unit * k + i] = phys;
-        }
-      }
-    }
-  }
-
   // ---- ordered compaction (ascending page ids): every key above R, then the
   // first `need` keys of [L, R] by page id (all of them when cnt == need).
   // Per 32-page block: ballots of the two kinds; per warp: running counts;
@@ -606,12 +608,6 @@ __global__ void __launch_bounds__(NT, 1)
     gt_seen += __popc(m_gt);
     eq_seen += __popc(m_eq);
   }
-  // page-table entries of the selected pages: all loads before any store
-  int phys[KPT];
-  const bool want_phys = spec.enabled ? (corrected && spec.sel_used_phys && !spec.page2slot)
-                                      : sel_phys_out != nullptr;
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) phys[j] = want_phys && pos[j] >= 0 ? __ldg(ptab + base + 32 * j) : -1;
   // fewer started pages than k (lengths only): slots n_take .. k-1, which no
   // selected key takes, are -1
   if (!spec.enabled)

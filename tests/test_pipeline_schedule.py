@@ -61,7 +61,8 @@ def _classify(stmt):
     if name == "launch_spec_decide":
         return ("kernel", a[-1], "decide")
     if name == "launch_select":
-        return ("kernel", a[-2], "select")
+        part = {"kSelScores": "scores", "kSelTopk": "topk"}.get(a[-1], "select")
+        return ("kernel", a[a.index("sa") + 1], part)
     if name == "spec_select_impl":
         return ("kernel", a[-2], "spec_select")
     if name == "launch_recall":
@@ -99,6 +100,8 @@ ACCESS = {
     "stand_in": ((), ()),
     "decide": (("q_prev", "sel_prev"), ("corrected", "cbar", "q_prev", "sel_used.r", "idx.r")),
     "select": (("corrected",), ("ws", "sel_prev", "sel_used.c", "idx.c")),
+    "scores": ((), ("ws",)),
+    "topk": (("corrected", "ws"), ("sel_prev", "sel_used.c", "idx.c")),
     "spec_select": (("q_prev", "sel_prev", "maps"),
                     ("ws", "corrected", "cbar", "q_prev", "sel_prev", "sel_used", "idx.r")),
     "recall_corrected": (("sel_prev", "sel_used", "corrected", "maps.c"), ("maps.c", "slots.c", "idx.c")),
@@ -196,7 +199,7 @@ def test_schedule_is_read_from_the_source():
     pro, hbm, host, epi = pipeline_schedule()
     kernels = lambda seq: [d for k, _, d in seq if k == "kernel"]
     assert kernels(pro) == ["stand_in"] and kernels(epi) == ["stand_in"]
-    assert kernels(hbm) == ["decide", "select", "attn_reused", "attn_corrected"]
+    assert kernels(hbm) == ["decide", "scores", "topk", "attn_reused", "attn_corrected"]
     assert kernels(host) == ["spec_select", "recall_corrected", "recall_prefetch", "attn_reused",
                              "attn_corrected"]
     assert sum(k == "mark" for k, _, _ in pro + hbm + epi) == 11
@@ -247,6 +250,7 @@ def _mutated(drop=None, move=None):
     (dict(drop=("host", ("wait", "pf", 1))), ["host"] * 2),                      # prefetch before selection
     (dict(move=("host", ("record", "side", 1), ("kernel", "side", "recall_corrected"))), ["host"] * 2),
     (dict(move=("hbm", ("record", "s", 0), ("kernel", "s", "decide"))), ["hbm"] * 2),
+    (dict(move=("hbm", ("record", "s", 0), ("kernel", "s", "scores"))), ["hbm"] * 2),  # top-k before its scores
 ])
 def test_the_check_catches_a_broken_schedule(mutation, kinds):
     assert races(unroll(_mutated(**mutation), kinds, 3)) != []
