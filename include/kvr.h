@@ -71,6 +71,10 @@ extern "C" {
 #define KVR_ST_NO_TOKENS 0x4u     /* an attention row had no valid token */
 #define KVR_ST_NO_FREE_SLOT 0x8u  /* recall found fewer free slots than misses */
 
+/* output element types of kvr_sparse_decode_attn_multi */
+#define KVR_DTYPE_F32 0  /* fp32 */
+#define KVR_DTYPE_BF16 1 /* bf16, the fp32 result rounded to nearest even once */
+
 /* workspace kinds for kvr_workspace_size */
 #define KVR_OP_SELECT 1 /* kvr_select_pages, kvr_speculative_select */
 #define KVR_OP_ATTN 2   /* kvr_sparse_decode_attn */
@@ -179,6 +183,51 @@ int kvr_sparse_decode_attn_len(const kvr_dims *dims, const uint16_t *q,
                                const int32_t *sel_phys, int32_t top_k,
                                float scale, float *out, void *ws,
                                size_t ws_bytes, void *stream);
+
+/* ---- several query tokens per sequence in one step.  The pages treat one
+ * new token per decode step; a step that decodes several (the T newest
+ * tokens of each sequence, whose K and V are already appended) is this
+ * library's extension of [FreeKV] section 2.1's group-consistent selection:
+ * one selection per (b, g) serves the whole step, scored with the mean of
+ * the page bound over every query row that will read the pages (the G heads
+ * of the group times the T tokens), and each query token attends causally.
+ * qs [B][T][Hq][D] bf16: the queries of the last T tokens of each sequence,
+ * oldest first.  G T must be 1, 2, 4, 8 or 16 (KVR_ERR_UNSUPPORTED_SHAPE
+ * otherwise).  seq_len [B] counts the written tokens including the T new
+ * ones (seq_len[b] >= T). */
+
+/* The step's selection: for each (b, g) the page score is
+ *   S[b][g][p] = (1 / (T G)) * sum_{tau < T} sum_{h in group g} sum_c
+ *                max(qs[b][tau][h][c]*kmin_c, qs[b][tau][h][c]*kmax_c)
+ * over the sequence's started pages, and the top_k pages with the largest S
+ * are selected as in kvr_select_pages_len (ties to the lower page id, ids
+ * ascending, -1 beyond the started pages).  Workspace kind KVR_OP_SELECT. */
+int kvr_select_pages_multi(const kvr_dims *dims, const uint16_t *qs,
+                           int32_t n_query, const uint16_t *summ,
+                           const int32_t *page_table, const int32_t *seq_len,
+                           int32_t top_k, int32_t *sel, int32_t *sel_phys,
+                           float *scores_opt, void *ws, size_t ws_bytes,
+                           void *stream);
+
+/* The step's attention: query token tau of sequence b (0 <= tau < T), head
+ * h, attends over the tokens of its KV head's selected pages at positions
+ * below seq_len[b] - T + tau + 1 (its own token and the ones before it):
+ *   out[b][tau][h] = sum_t softmax_t(scale * qs[b][tau][h] . K_t) * V_t .
+ * sel [B][H][k] holds the logical ids (from kvr_select_pages_multi; needed
+ * for T > 1, may be NULL for T = 1) and sel_phys the physical ones.  out
+ * [B][T][Hq][D] is fp32 (out_dtype KVR_DTYPE_F32) or bf16 (KVR_DTYPE_BF16:
+ * the fp32 result rounded to nearest even once, at the store).  With T = 1
+ * this is kvr_sparse_decode_attn_len with a choice of output type.  A row
+ * that sees no token gets zeros and sets KVR_ST_NO_TOKENS.  Workspace kind
+ * KVR_OP_ATTN. */
+int kvr_sparse_decode_attn_multi(const kvr_dims *dims, const uint16_t *qs,
+                                 int32_t n_query, const uint16_t *k_pool,
+                                 const uint16_t *v_pool,
+                                 const int32_t *page_table,
+                                 const int32_t *seq_len, const int32_t *sel,
+                                 const int32_t *sel_phys, int32_t top_k,
+                                 float scale, void *out, int32_t out_dtype,
+                                 void *ws, size_t ws_bytes, void *stream);
 
 /* State of the speculative mode, owned by the caller.  q_prev [B][Hq][D]
  * bf16 and sel_prev [B][H][k] int32 are device buffers; `step` is a host

@@ -58,21 +58,29 @@ constexpr int kAttnMaxQ = 8;                       // CTAs per cluster (the port
 constexpr int kAttnWarpRing = 48 * 1024;           // ring bytes of one consumer warp
 constexpr int kSmemPerSM = 228 * 1024;             // shared memory of one SM
 
-template <int G, int P>
+// NR: query rows per unit, the G heads of the group times the T query tokens
+// of the step (1, 2, 4, 8 or 16); they are the MMA's column side, in CB
+// blocks of 8 columns.
+template <int NR, int P>
 struct AttnCfg {
+  static constexpr int CB = NR > 8 ? 2 : 1;        // 8-column blocks of the query rows
   static constexpr int C = P < 32 ? P : 32;        // tokens per chunk (one stage)
   static constexpr int CPP = P / C;                // chunks per page
   static constexpr int NB = C / 8;                 // 8-token column blocks of the QK MMA
   static constexpr int KP = C / 16;                // 16-token k-steps of the PV MMA
   static constexpr int kHalf = C * 128;            // 64 channels of C rows (swizzled)
   static constexpr int kStageBytes = 4 * kHalf;    // K lo, K hi, V lo, V hi
-  static constexpr int R = kAttnWarpRing / kStageBytes;  // stages per consumer warp
+  // ring bytes of one consumer warp: 48 KiB, 32 KiB with two column blocks
+  // (whose partials need twice the receive space)
+  static constexpr int kWarpRing = CB == 1 ? kAttnWarpRing : 32 * 1024;
+  static constexpr int R = kWarpRing / kStageBytes;  // stages per consumer warp
   static constexpr int S = kAttnNC * R;            // ring depth
   static constexpr int kSmem = S * kStageBytes + 1024;   // + 1 KiB to align the ring
-  static constexpr int kStatic = kAttnNC * G * kD * 4 + kAttnMaxQ * kAttnNC * G * 8 +
-                                 kAttnNC * kAttnIds * 4 + S * 24 + 64;
+  static constexpr int kStatic = kAttnNC * NR * kD * 4 + kAttnMaxQ * kAttnNC * NR * 8 +
+                                 2 * kAttnNC * kAttnIds * 4 + S * 28 + 64;
   static_assert(kAttnCPS * (kSmem + kStatic + 1024) <= kSmemPerSM, "CTAs per SM must fit");
   static_assert(CPP * C == P && NB * 8 == C && KP * 16 == C && R >= 2, "chunk tiling");
+  static_assert(NR * kD * 4 + NR * 8 <= R * kStageBytes, "a worker's partial fits its stages");
 };
 
 __device__ __forceinline__ bool attn_unit_active(const uint8_t *filter, int filter_mode,
@@ -82,30 +90,36 @@ __device__ __forceinline__ bool attn_unit_active(const uint8_t *filter, int filt
 }
 
 // One chunk of C tokens for a consumer warp.
-//   QK   S^T[t][h] = K_t . q_h with the tokens on the MMA's 16-row side and
-//        the heads as its 8 columns (columns G..7 zero): C/16 row blocks x 8
-//        channel k-steps; K fragments by ldmatrix, q as B fragments held in
-//        registers.  Lane (gq, tq) gets tokens 16 mt + gq (+8) of heads 2tq,
-//        2tq + 1.
+//   QK   S^T[t][j] = K_t . q_j with the tokens on the MMA's 16-row side and
+//        the query rows as its columns (8 per block; rows NR.. are zero):
+//        C/16 row blocks x 8 channel k-steps per column block; K fragments
+//        by ldmatrix, q as B fragments held in registers.  Lane (gq, tq)
+//        gets tokens 16 mt + gq (+8) of columns 8 cb + 2tq, 8 cb + 2tq + 1.
 //   softmax  online, base 2 (logits prescaled by scale * log2 e); the lane's
-//        running (m, l) are those of its heads 2tq, 2tq + 1.
-//   PV   O^T[c][h] += V^T[c][t] P^T[t][h]: V fragments by transposing
+//        running (m, l) are those of its columns.
+//   PV   O^T[c][j] += V^T[c][t] P^T[t][j]: V fragments by transposing
 //        ldmatrix; P^T as B fragments by transposing the accumulator tiles
 //        in registers (movmatrix).  P is split into a bf16 high part and a
-//        bf16 residual, so the weights keep about 16 bits: for G <= 4 the
-//        residual rides in columns h + 4 of the same MMA (the output of head
-//        h is then column h plus column h + 4); for G = 8 it takes a second
+//        bf16 residual, so the weights keep about 16 bits: for NR <= 4 the
+//        residual rides in columns j + 4 of the same MMA (the output of row
+//        j is then column j plus column j + 4); otherwise it takes a second
 //        MMA.
 // nv: tokens of the chunk that exist (C except in the partial last page of
-// a sequence): the scores of the others become -inf and their V rows zero,
-// so stale rows can contribute neither weight nor NaN.
-template <int G, int P>
-__device__ __forceinline__ void attn_chunk(uint32_t kb, const uint32_t (&qb)[8][2],
-                                           float scale_log2, float (&m_run)[2], float (&l_run)[2],
-                                           float (&o)[8][4], int lane, int nv) {
-  using Cfg = AttnCfg<G, P>;
-  constexpr int HALF = Cfg::kHalf, MT = Cfg::C / 16;
-  constexpr bool kPair = G <= 4;
+// a sequence): their V rows beyond nv are zeroed, so stale rows can
+// contribute neither weight nor NaN.  lim[cb][c]: the leading tokens of the
+// chunk that the lane's column 8 cb + 2tq + c may see (at most nv; fewer for
+// an earlier query token of the step, which attends causally); the scores of
+// the others become -inf.  A column that has seen no token yet keeps
+// m = -inf and l = 0.
+template <int NR, int P, bool CAUSAL>
+__device__ __forceinline__ void attn_chunk(uint32_t kb, const uint32_t (&qb)[AttnCfg<NR, P>::CB][8][2],
+                                           float scale_log2, float (&m_run)[AttnCfg<NR, P>::CB][2],
+                                           float (&l_run)[AttnCfg<NR, P>::CB][2],
+                                           float (&o)[AttnCfg<NR, P>::CB][8][4], int lane, int nv,
+                                           const int (&lim)[AttnCfg<NR, P>::CB][2]) {
+  using Cfg = AttnCfg<NR, P>;
+  constexpr int HALF = Cfg::kHalf, MT = Cfg::C / 16, CB = Cfg::CB;
+  constexpr bool kPair = NR <= 4;
   const int gq = lane >> 2, tq = lane & 3, mi = lane >> 3, mr = lane & 7;
   const uint32_t vb = kb + 2 * HALF;
   if (nv < Cfg::C) {  // zero V rows nv .. C-1 of both channel halves (16 bytes a lane-store)
@@ -118,118 +132,140 @@ __device__ __forceinline__ void attn_chunk(uint32_t kb, const uint32_t (&qb)[8][
     __syncwarp();
   }
   // ---- S^T, even and odd channel k-steps in separate accumulators
-  float st[MT][4], su[MT][4];
+  float st[CB][MT][4], su[CB][MT][4];
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
+  for (int cb = 0; cb < CB; ++cb)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) st[mt][e] = su[mt][e] = 0.f;
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) st[cb][mt][e] = su[cb][mt][e] = 0.f;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       uint32_t a[4];
       ldsm_x4(swz<HALF>(kb, 16 * mt + 8 * (mi & 1) + mr, 2 * kk + (mi >> 1)), a);
-      if (kk & 1)
-        mma_bf16_16816(su[mt], a[0], a[1], a[2], a[3], qb[kk][0], qb[kk][1]);
-      else
-        mma_bf16_16816(st[mt], a[0], a[1], a[2], a[3], qb[kk][0], qb[kk][1]);
-    }
-  // ---- online softmax for heads 2tq (e = 0, 2) and 2tq + 1 (e = 1, 3)
-  float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      st[mt][e] = (st[mt][e] + su[mt][e]) * scale_log2;
-      if (16 * mt + gq + 8 * (e >> 1) >= nv) st[mt][e] = -INFINITY;  // no such token
-    }
-    mx0 = fmaxf(mx0, fmaxf(st[mt][0], st[mt][2]));
-    mx1 = fmaxf(mx1, fmaxf(st[mt][1], st[mt][3]));
-  }
-#pragma unroll
-  for (int m = 4; m <= 16; m <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, m));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, m));
-  }
-  const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-  const float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
-  const bool on0 = 2 * tq < G, on1 = 2 * tq + 1 < G;
-  float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    st[mt][0] = on0 ? exp2f(st[mt][0] - mn0) : 0.f;
-    st[mt][2] = on0 ? exp2f(st[mt][2] - mn0) : 0.f;
-    st[mt][1] = on1 ? exp2f(st[mt][1] - mn1) : 0.f;
-    st[mt][3] = on1 ? exp2f(st[mt][3] - mn1) : 0.f;
-    ls0 += st[mt][0] + st[mt][2];
-    ls1 += st[mt][1] + st[mt][3];
-  }
-  l_run[0] = fmaf(l_run[0], al0, ls0);
-  l_run[1] = fmaf(l_run[1], al1, ls1);
-  m_run[0] = mn0;
-  m_run[1] = mn1;
-  // rescale O; with the residual in columns h + 4, lanes tq >= 2 hold the
-  // residual columns of heads 2tq - 4, 2tq - 3 (the lane tq - 2's heads)
-  float a0 = al0, a1 = al1;
-  if (kPair) {
-    const float x0 = __shfl_xor_sync(0xffffffffu, al0, 2);
-    const float x1 = __shfl_xor_sync(0xffffffffu, al1, 2);
-    if (tq >= 2) {
-      a0 = x0;
-      a1 = x1;
-    }
-  }
-#pragma unroll
-  for (int mb = 0; mb < 8; ++mb) {
-    o[mb][0] *= a0;
-    o[mb][1] *= a1;
-    o[mb][2] *= a0;
-    o[mb][3] *= a1;
-  }
-  // ---- P^T as B fragments: 8x8 tiles (tokens 16 mt + 8 r .., heads) transposed
-  uint32_t pb[MT][2], pl[MT][2];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const float x0 = st[mt][2 * r], x1 = st[mt][2 * r + 1];
-      const uint32_t hi = pack_bf16x2(x0, x1);
-      const uint32_t lo = pack_bf16x2(x0 - __uint_as_float(hi << 16),
-                                      x1 - __uint_as_float(hi & 0xffff0000u));
-      if (kPair) {
-        const uint32_t lo_s = __shfl_xor_sync(0xffffffffu, lo, 2);
-        pb[mt][r] = movmatrix_trans(tq < 2 ? hi : lo_s);
-        pl[mt][r] = 0u;
-      } else {
-        pb[mt][r] = movmatrix_trans(hi);
-        pl[mt][r] = movmatrix_trans(lo);
+      for (int cb = 0; cb < CB; ++cb) {
+        if (kk & 1)
+          mma_bf16_16816(su[cb][mt], a[0], a[1], a[2], a[3], qb[cb][kk][0], qb[cb][kk][1]);
+        else
+          mma_bf16_16816(st[cb][mt], a[0], a[1], a[2], a[3], qb[cb][kk][0], qb[cb][kk][1]);
       }
     }
-  // ---- PV: O^T[16 mb ..][heads] += V^T[16 mb ..][16 kp ..] P^T
+  uint32_t pb[CB][MT][2], pl[CB][MT][2];
+#pragma unroll
+  for (int cb = 0; cb < CB; ++cb) {
+    // ---- online softmax for columns 8 cb + 2tq (e = 0, 2) and + 1 (e = 1, 3)
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        st[cb][mt][e] = (st[cb][mt][e] + su[cb][mt][e]) * scale_log2;
+        if (16 * mt + gq + 8 * (e >> 1) >= (CAUSAL ? lim[cb][e & 1] : nv))
+          st[cb][mt][e] = -INFINITY;  // not visible
+      }
+      mx0 = fmaxf(mx0, fmaxf(st[cb][mt][0], st[cb][mt][2]));
+      mx1 = fmaxf(mx1, fmaxf(st[cb][mt][1], st[cb][mt][3]));
+    }
+#pragma unroll
+    for (int m = 4; m <= 16; m <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, m));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, m));
+    }
+    const float mn0 = fmaxf(m_run[cb][0], mx0), mn1 = fmaxf(m_run[cb][1], mx1);
+    // exponent base: 0 while a column has seen no token (everything is -inf;
+    // without the causal limits every column sees the chunk's first token)
+    const float mb0 = CAUSAL && mn0 == -INFINITY ? 0.f : mn0;
+    const float mb1 = CAUSAL && mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = exp2f(m_run[cb][0] - mb0), al1 = exp2f(m_run[cb][1] - mb1);
+    const bool on0 = 8 * cb + 2 * tq < NR, on1 = 8 * cb + 2 * tq + 1 < NR;
+    float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      st[cb][mt][0] = on0 ? exp2f(st[cb][mt][0] - mb0) : 0.f;
+      st[cb][mt][2] = on0 ? exp2f(st[cb][mt][2] - mb0) : 0.f;
+      st[cb][mt][1] = on1 ? exp2f(st[cb][mt][1] - mb1) : 0.f;
+      st[cb][mt][3] = on1 ? exp2f(st[cb][mt][3] - mb1) : 0.f;
+      ls0 += st[cb][mt][0] + st[cb][mt][2];
+      ls1 += st[cb][mt][1] + st[cb][mt][3];
+    }
+    l_run[cb][0] = fmaf(l_run[cb][0], al0, ls0);
+    l_run[cb][1] = fmaf(l_run[cb][1], al1, ls1);
+    m_run[cb][0] = mn0;
+    m_run[cb][1] = mn1;
+    // rescale O; with the residual in columns j + 4, lanes tq >= 2 hold the
+    // residual columns of rows 2tq - 4, 2tq - 3 (the lane tq - 2's rows)
+    float a0 = al0, a1 = al1;
+    if (kPair) {
+      const float x0 = __shfl_xor_sync(0xffffffffu, al0, 2);
+      const float x1 = __shfl_xor_sync(0xffffffffu, al1, 2);
+      if (tq >= 2) {
+        a0 = x0;
+        a1 = x1;
+      }
+    }
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      o[cb][mb][0] *= a0;
+      o[cb][mb][1] *= a1;
+      o[cb][mb][2] *= a0;
+      o[cb][mb][3] *= a1;
+    }
+    // ---- P^T as B fragments: 8x8 tiles (tokens 16 mt + 8 r .., columns) transposed
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float x0 = st[cb][mt][2 * r], x1 = st[cb][mt][2 * r + 1];
+        const uint32_t hi = pack_bf16x2(x0, x1);
+        const uint32_t lo = pack_bf16x2(x0 - __uint_as_float(hi << 16),
+                                        x1 - __uint_as_float(hi & 0xffff0000u));
+        if (kPair) {
+          const uint32_t lo_s = __shfl_xor_sync(0xffffffffu, lo, 2);
+          pb[cb][mt][r] = movmatrix_trans(tq < 2 ? hi : lo_s);
+          pl[cb][mt][r] = 0u;
+        } else {
+          pb[cb][mt][r] = movmatrix_trans(hi);
+          pl[cb][mt][r] = movmatrix_trans(lo);
+        }
+      }
+  }
+  // ---- PV: O^T[16 mb ..][columns] += V^T[16 mb ..][16 kp ..] P^T
 #pragma unroll
   for (int mb = 0; mb < 8; ++mb) {
 #pragma unroll
     for (int kp = 0; kp < MT; ++kp) {
       uint32_t va[4];
       ldsm_x4_trans(swz<HALF>(vb, 16 * kp + 8 * (mi >> 1) + mr, 2 * mb + (mi & 1)), va);
-      mma_bf16_16816(o[mb], va[0], va[1], va[2], va[3], pb[kp][0], pb[kp][1]);
-      if (!kPair) mma_bf16_16816(o[mb], va[0], va[1], va[2], va[3], pl[kp][0], pl[kp][1]);
+#pragma unroll
+      for (int cb = 0; cb < CB; ++cb) {
+        mma_bf16_16816(o[cb][mb], va[0], va[1], va[2], va[3], pb[cb][kp][0], pb[cb][kp][1]);
+        if (!kPair) mma_bf16_16816(o[cb][mb], va[0], va[1], va[2], va[3], pl[cb][kp][0], pl[cb][kp][1]);
+      }
     }
   }
 }
 
 // filter_mode: 0 every unit; 1 only units with filter[unit] == 0; 2 only != 0.
 // Grid: units x Q CTAs in clusters of Q (cluster c = unit c).
-template <int G, int P>
+// T query tokens per sequence and G query heads per KV head (NR = T G): q and
+// out are [B][T][Hq][D]; with T > 1 seq_len and sel_log (the logical ids of
+// sel_phys) are given and query token tau sees the positions below
+// seq_len - T + tau + 1 (CAUSAL instances; T = 1 takes the others).  out is
+// fp32, or bf16 (rounded to nearest even) when out_bf16 != 0.
+template <int NR, int P, bool CAUSAL>
 __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
     k_sparse_decode(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const uint16_t *__restrict__ q,
-                    const int32_t *__restrict__ sel_phys, int H, int k, int n_phys, int Q,
-                    float scale_log2, const uint8_t *__restrict__ filter, int filter_mode,
-                    float *__restrict__ out, const int32_t *__restrict__ seq_len,
+                    const int32_t *__restrict__ sel_phys, const int32_t *__restrict__ sel_log,
+                    int H, int k, int n_phys, int Q, int T, int G, float scale_log2,
+                    const uint8_t *__restrict__ filter, int filter_mode, void *__restrict__ out,
+                    int out_bf16, const int32_t *__restrict__ seq_len,
                     const int32_t *__restrict__ page_table, int N) {
-  using Cfg = AttnCfg<G, P>;
-  constexpr int NC = kAttnNC, CPP = Cfg::CPP, HALF = Cfg::kHalf, R = Cfg::R, S = Cfg::S;
+  using Cfg = AttnCfg<NR, P>;
+  constexpr int NC = kAttnNC, CPP = Cfg::CPP, HALF = Cfg::kHalf, R = Cfg::R, S = Cfg::S, CB = Cfg::CB;
   constexpr int kIdRounds = kAttnIds / 32;
   extern __shared__ uint8_t smem_raw[];
   // the swizzle pattern repeats every 1024 bytes: align the ring to it
@@ -237,12 +273,14 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
   const uint32_t ring = smem_addr(smem);
   __shared__ __align__(8) uint64_t full[S], empty[S];
   __shared__ int s_ok[S];
-  __shared__ int s_nv[S];  // tokens of the stage's chunk that exist
-  __shared__ int s_ids[NC][kAttnIds];  // page ids of the first kAttnIds chunks of each worker
+  __shared__ int s_nv[S];    // tokens of the stage's chunk that exist
+  __shared__ int s_pos0[S];  // position of the chunk's first token in its sequence (T > 1)
+  __shared__ int s_ids[NC][kAttnIds];   // page ids of the first kAttnIds chunks of each worker
+  __shared__ int s_lids[NC][kAttnIds];  // their logical ids (T > 1)
   // partials of the cluster's workers for this CTA's channel slice:
-  // [worker][head][channel of the slice], and (m, l) per worker and head
-  __shared__ __align__(16) float s_recv[NC * G * kD];
-  __shared__ __align__(8) float2 s_mlr[kAttnMaxQ * NC * G];
+  // [worker][query row][channel of the slice], and (m, l) per worker and row
+  __shared__ __align__(16) float s_recv[NC * NR * kD];
+  __shared__ __align__(8) float2 s_mlr[kAttnMaxQ * NC * NR];
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -256,6 +294,10 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
   const int per = kD / Q;                                 // channels merged by each CTA
   const int kc = k * CPP;                                 // chunks of the unit
   const int32_t *sel_u = sel_phys + static_cast<size_t>(u) * k;  // the unit's page ids
+  constexpr bool causal = CAUSAL;  // T > 1: seq_len and sel_log are given
+  // heads per KV head: NR itself for one query token (a compile-time constant)
+  const int Gc = CAUSAL ? G : NR;
+  const int32_t *sel_lu = causal ? sel_log + static_cast<size_t>(u) * k : nullptr;
   // range of this CTA's worker w: chunks [a, a + n) of the unit
   auto worker_range = [&](int w, int &a, int &n) {
     const uint32_t v = static_cast<uint32_t>(rank * NC + w);
@@ -307,13 +349,29 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
       for (int w = 0; w < NC; ++w)
 #pragma unroll
         for (int r = 0; r < kIdRounds; ++r) s_ids[w][lane + 32 * r] = idv[w][r];
+      if (causal) {
+#pragma unroll
+        for (int w = 0; w < NC; ++w) {
+          int a, n;
+          worker_range(w, a, n);
+#pragma unroll
+          for (int r = 0; r < kIdRounds; ++r) {
+            const int j = lane + 32 * r;
+            idv[w][r] = j < n ? __ldg(sel_lu + (a + j) / CPP) : -1;
+          }
+        }
+#pragma unroll
+        for (int w = 0; w < NC; ++w)
+#pragma unroll
+          for (int r = 0; r < kIdRounds; ++r) s_lids[w][lane + 32 * r] = idv[w][r];
+      }
     }
     __syncwarp();
     // with lengths, only the sequence's last page can be partial: its
     // physical id and written tokens (-1 ids are padding, skipped silently)
-    int last_phys = -2, last_nt = P;
+    int last_phys = -2, last_nt = P, L = 0;
     if (seq_len) {
-      const int L = seq_len[b];
+      L = seq_len[b];
       if (L > 0) {
         const int pl = (L - 1) / P;
         last_phys = pl < N ? __ldg(page_table + static_cast<size_t>(b) * N + pl) : -2;
@@ -337,11 +395,18 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
         if (i < R || mbar_test_wait(&empty[s], static_cast<uint32_t>((i / R - 1) & 1))) {
           const int pos = a + i;
           const int id = i < kAttnIds ? s_ids[lane][i] : __ldg(sel_u + pos / CPP);
-          const int nv = id == last_phys ? min(Cfg::C, max(0, last_nt - (pos % CPP) * Cfg::C))
-                                         : Cfg::C;
+          int nv, pos0 = 0;
+          if (causal) {  // tokens below the sequence's length, from the logical position
+            const int lid = i < kAttnIds ? s_lids[lane][i] : __ldg(sel_lu + pos / CPP);
+            pos0 = lid * P + (pos % CPP) * Cfg::C;
+            nv = lid >= 0 ? min(Cfg::C, max(0, L - pos0)) : 0;
+          } else {
+            nv = id == last_phys ? min(Cfg::C, max(0, last_nt - (pos % CPP) * Cfg::C)) : Cfg::C;
+          }
           const bool ok = id >= 0 && id < n_phys && nv > 0;
           s_ok[s] = ok ? 1 : 0;
           s_nv[s] = nv;
+          if (causal) s_pos0[s] = pos0;
           if (ok) {
             uint8_t *dst = smem + s * Cfg::kStageBytes;
             const int row = id * P + (pos % CPP) * Cfg::C;
@@ -374,23 +439,31 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
     // ---------------------------------------------------------- consumer warps
     const int cw = warp;
     const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group and column pair
-    const int Hq = H * G;
+    const int Hq = H * Gc;
     int a, n;
     worker_range(cw, a, n);
+    const int L = causal ? seq_len[b] : 0;
 
-    uint32_t qb[8][2];  // q of head gq as B fragments (k-step kk: channels 16kk + 2tq, +8)
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};  // heads 2tq, 2tq + 1
-    float o[8][4];  // O^T[16 mb + gq (+8)][2 tq (+1)]
+    // query row j = 8 cb + gq (token j / G, head j % G of the group) as B
+    // fragments (k-step kk: channels 16kk + 2tq, +8); rows NR.. are zero
+    uint32_t qb[CB][8][2];
+    float m_run[CB][2], l_run[CB][2];  // columns 8 cb + 2tq, + 1
+    float o[CB][8][4];                 // O^T[16 mb + gq (+8)][8 cb + 2 tq (+1)]
 #pragma unroll
-    for (int mb = 0; mb < 8; ++mb) o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
-    {
+    for (int cb = 0; cb < CB; ++cb) {
+      m_run[cb][0] = m_run[cb][1] = -INFINITY;
+      l_run[cb][0] = l_run[cb][1] = 0.f;
+#pragma unroll
+      for (int mb = 0; mb < 8; ++mb) o[cb][mb][0] = o[cb][mb][1] = o[cb][mb][2] = o[cb][mb][3] = 0.f;
+      const int jr = min(8 * cb + gq, NR - 1);
+      const int tau = CAUSAL ? jr / Gc : 0;  // one query token: row jr is head jr
       const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-          q + (static_cast<size_t>(b) * Hq + g * G + min(gq, G - 1)) * kD);
-      const bool on = gq < G;
+          q + ((static_cast<size_t>(b) * T + tau) * Hq + g * Gc + jr - tau * Gc) * kD);
+      const bool on = 8 * cb + gq < NR;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        qb[kk][0] = on ? __ldg(qrow + 8 * kk + tq) : 0u;
-        qb[kk][1] = on ? __ldg(qrow + 8 * kk + 4 + tq) : 0u;
+        qb[cb][kk][0] = on ? __ldg(qrow + 8 * kk + tq) : 0u;
+        qb[cb][kk][1] = on ? __ldg(qrow + 8 * kk + 4 + tq) : 0u;
       }
     }
 #pragma unroll 1
@@ -405,54 +478,76 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
           s_abort = 1;
         }
       }
-      if (have)
-        attn_chunk<G, P>(ring + s * Cfg::kStageBytes, qb, scale_log2, m_run, l_run, o, lane, s_nv[s]);
+      if (have) {
+        const int nv = s_nv[s];
+        int lim[CB][2];
+#pragma unroll
+        for (int cb = 0; cb < CB; ++cb)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            lim[cb][c] = nv;
+            if (causal) {  // query token tau sees positions below L - T + tau + 1
+              const int tau = min(8 * cb + 2 * tq + c, NR - 1) / Gc;
+              lim[cb][c] = min(nv, max(0, L - T + tau + 1 - s_pos0[s]));
+            }
+          }
+        attn_chunk<NR, P, CAUSAL>(ring + s * Cfg::kStageBytes, qb, scale_log2, m_run, l_run, o, lane, nv, lim);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
     // ---- this worker's partial, pushed to the CTAs that merge it
-    float l0 = l_run[0], l1 = l_run[1];
+    float lr[CB][2];
 #pragma unroll
-    for (int m = 4; m <= 16; m <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, m);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, m);
-    }
-    if (G <= 4) {  // add the residual columns h + 4 into columns h
+    for (int cb = 0; cb < CB; ++cb)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float x = l_run[cb][c];
+#pragma unroll
+        for (int m = 4; m <= 16; m <<= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+        lr[cb][c] = x;
+      }
+    if (NR <= 4) {  // add the residual columns j + 4 into columns j
 #pragma unroll
       for (int mb = 0; mb < 8; ++mb)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o[mb][e] += __shfl_xor_sync(0xffffffffu, o[mb][e], 2);
+        for (int e = 0; e < 4; ++e) o[0][mb][e] += __shfl_xor_sync(0xffffffffu, o[0][mb][e], 2);
     }
-    // stage O [head][channel] and (m, l) [head] in this warp's first stage,
+    // stage O [row][channel] and (m, l) [row] in this warp's first stages,
     // free now that its last chunk is consumed
     float *stg = reinterpret_cast<float *>(smem + cw * R * Cfg::kStageBytes);
-    float2 *stg_ml = reinterpret_cast<float2 *>(stg + G * kD);
+    float2 *stg_ml = reinterpret_cast<float2 *>(stg + NR * kD);
 #pragma unroll
-    for (int mb = 0; mb < 8; ++mb)
+    for (int cb = 0; cb < CB; ++cb)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int h = 2 * tq + (e & 1);
-        if (h < G) stg[h * kD + 16 * mb + gq + 8 * (e >> 1)] = o[mb][e];
-      }
+      for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int jr = 8 * cb + 2 * tq + (e & 1);
+          if (jr < NR) stg[jr * kD + 16 * mb + gq + 8 * (e >> 1)] = o[cb][mb][e];
+        }
     if (gq == 0) {
-      if (2 * tq < G) stg_ml[2 * tq] = make_float2(m_run[0], l0);
-      if (2 * tq + 1 < G) stg_ml[2 * tq + 1] = make_float2(m_run[1], l1);
+#pragma unroll
+      for (int cb = 0; cb < CB; ++cb) {
+        if (8 * cb + 2 * tq < NR) stg_ml[8 * cb + 2 * tq] = make_float2(m_run[cb][0], lr[cb][0]);
+        if (8 * cb + 2 * tq + 1 < NR) stg_ml[8 * cb + 2 * tq + 1] = make_float2(m_run[cb][1], lr[cb][1]);
+      }
     }
     __syncwarp();
     cluster_wait();  // every CTA of the cluster has started: pushes may begin
     const int j = rank * NC + cw;  // this worker's index in the cluster
     const uint32_t rc0 = smem_addr(s_recv), ml0 = smem_addr(s_mlr);
 #pragma unroll
-    for (int x = lane; x < G * kD / 4; x += 32) {  // 4 channels of one head per store
-      const int h = x / (kD / 4), c = 4 * (x - h * (kD / 4));
+    for (int x = lane; x < NR * kD / 4; x += 32) {  // 4 channels of one row per store
+      const int jr = x / (kD / 4), c = 4 * (x - jr * (kD / 4));
       const int owner = c / per, cl = c - owner * per;
-      st_cluster_f32x4(cluster_map(rc0 + ((j * G + h) * per + cl) * 4, owner),
-                       *reinterpret_cast<const float4 *>(stg + h * kD + c));
+      st_cluster_f32x4(cluster_map(rc0 + ((j * NR + jr) * per + cl) * 4, owner),
+                       *reinterpret_cast<const float4 *>(stg + jr * kD + c));
     }
-    if (lane < G) {
+    if (lane < NR) {
       const float2 ml = stg_ml[lane];
 #pragma unroll 1
-      for (int qr = 0; qr < Q; ++qr) st_cluster_f32x2(cluster_map(ml0 + (j * G + lane) * 8, qr), ml);
+      for (int qr = 0; qr < Q; ++qr) st_cluster_f32x2(cluster_map(ml0 + (j * NR + lane) * 8, qr), ml);
     }
     __syncwarp();
   }
@@ -462,34 +557,40 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
   // barrier no CTA touches another's shared memory
   cluster_sync();
   {
-    // CTA `rank` merges channels [rank per, (rank + 1) per) of the G heads,
-    // one thread per 4 channels of a head, from its own shared memory
+    // CTA `rank` merges channels [rank per, (rank + 1) per) of the NR rows,
+    // one thread per 4 channels of a row, from its own shared memory
     const int n4 = per / 4;
-    const int Hq = H * G;
+    const int Hq = H * Gc;
 #pragma unroll 1
-    for (int e = tid; e < G * n4; e += kAttnThreads) {
-      const int h = e / n4, cl = 4 * (e - h * n4);
+    for (int e = tid; e < NR * n4; e += kAttnThreads) {
+      const int jr = e / n4, cl = 4 * (e - jr * n4);
       float M = -INFINITY;
 #pragma unroll 4
-      for (int jj = 0; jj < nw; ++jj) M = fmaxf(M, s_mlr[jj * G + h].x);
-      float L = 0.f;
+      for (int jj = 0; jj < nw; ++jj) M = fmaxf(M, s_mlr[jj * NR + jr].x);
+      float Ls = 0.f;
       float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
       for (int jj = 0; jj < nw; ++jj) {
-        const float2 ml = s_mlr[jj * G + h];
+        const float2 ml = s_mlr[jj * NR + jr];
         const float sc = ml.x != -INFINITY ? exp2f(ml.x - M) : 0.f;
-        const float4 ov = *reinterpret_cast<const float4 *>(&s_recv[(jj * G + h) * per + cl]);
-        L = fmaf(sc, ml.y, L);
+        const float4 ov = *reinterpret_cast<const float4 *>(&s_recv[(jj * NR + jr) * per + cl]);
+        Ls = fmaf(sc, ml.y, Ls);
         A.x = fmaf(sc, ov.x, A.x);
         A.y = fmaf(sc, ov.y, A.y);
         A.z = fmaf(sc, ov.z, A.z);
         A.w = fmaf(sc, ov.w, A.w);
       }
       const int c = rank * per + cl;
-      if (L <= 0.f && c == 0) set_status(KVR_ST_NO_TOKENS);
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      *reinterpret_cast<float4 *>(out + (static_cast<size_t>(b) * Hq + g * G + h) * kD + c) =
-          make_float4(A.x * inv, A.y * inv, A.z * inv, A.w * inv);
+      if (Ls <= 0.f && c == 0) set_status(KVR_ST_NO_TOKENS);
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+      const int tau = CAUSAL ? jr / Gc : 0;
+      const size_t row = (static_cast<size_t>(b) * T + tau) * Hq + g * Gc + jr - tau * Gc;
+      const float4 r = make_float4(A.x * inv, A.y * inv, A.z * inv, A.w * inv);
+      if (out_bf16)
+        *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + row * kD + c) =
+            make_uint2(pack_bf16x2(r.x, r.y), pack_bf16x2(r.z, r.w));
+      else
+        *reinterpret_cast<float4 *>(static_cast<float *>(out) + row * kD + c) = r;
     }
   }
 }

@@ -125,10 +125,15 @@ struct AttnWs {
   uint32_t *reserved;  // the attention keeps its split partials on chip
 };
 
-// Per-sequence lengths for the attention (seq_len null: every page full).
+// Per-sequence lengths for the attention (seq_len null: every page full),
+// and the several-query form: T query tokens per sequence (sel_log holds the
+// logical ids of sel_phys, for the causal limits), bf16 output.
 struct AttnLen {
   const int32_t *seq_len = nullptr;
   const int32_t *page_table = nullptr;
+  int T = 1;
+  const int32_t *sel_log = nullptr;
+  int out_bf16 = 0;
 };
 
 size_t select_ws_bytes(const kvr_dims *d) {
@@ -275,42 +280,59 @@ constexpr int kSelScores = 1;  // k_page_scores
 constexpr int kSelTopk = 2;    // k_topk
 constexpr int kSelBoth = kSelScores | kSelTopk;
 
+// k_page_scores for NR = G T query rows per unit (q [B][T][Hq][D]): kScCPS
+// CTAs per SM, each warp a worker over a contiguous range of the flat page
+// list; a programmatic dependent launch unless pdl_first is false (right
+// after an event wait): the setup overlaps the kernel before it.
+template <int NR>
+int launch_scores(const kvr_dims *d, const uint16_t *q, const uint16_t *summ, int T, SelectWs w,
+                  float *scores, cudaStream_t st, bool pdl_first) {
+  auto kern = k_page_scores<NR>;
+  static int max_set[kMaxDevices] = {};
+  if (int rc = ensure_smem(reinterpret_cast<const void *>(kern), kScSmem, max_set)) return rc;
+  int sms = 0;
+  if (int rc = sm_count(&sms)) return rc;
+  const long long F = static_cast<long long>(d->batch) * d->n_kv_heads * d->n_pages;
+  const long long per_cta = static_cast<long long>(kScMinPagesPerWorker) * kScNC;
+  long long n_ctas = std::min<long long>(static_cast<long long>(sms) * kScCPS, (F + per_cta - 1) / per_cta);
+  n_ctas = std::max<long long>(1, std::min<long long>(n_ctas, kScMaxCtas));
+  CUtensorMap tsm, tsm8;
+  if (int rc = make_summ_map(&tsm, summ, F, kScPages)) return rc;
+  if (int rc = make_summ_map(&tsm8, summ, F, 8)) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(n_ctas));
+  cfg.blockDim = dim3(kScThreads);
+  cfg.dynamicSmemBytes = kScSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_first ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tsm, tsm8, q, d->n_kv_heads, d->n_pages, F, T,
+                                           d->n_q_heads / d->n_kv_heads, w.scores, scores);
+  if (e != cudaSuccess) return cuda_fail(e, "k_page_scores");
+  return KVR_OK;
+}
+
+// T: query tokens per sequence (q [B][T][Hq][D]); more than one only
+// without the speculative mode (the query rows per unit, G T, are 1, 2, 4,
+// 8 or 16, checked by the callers).
 template <int G>
 int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
                     const int32_t *ptab, int k, SelectWs w, int32_t *sel, int32_t *sel_phys,
                     float *scores, const SpecArgs &spec, cudaStream_t st, bool pdl_first,
-                    const int32_t *seq_len, int parts) {
+                    const int32_t *seq_len, int parts, int T) {
   if (parts & kSelScores) {
-    // 1. page scores: kScCPS CTAs per SM, each warp a worker over a contiguous
-    //    range of the flat page list
-    auto kern = k_page_scores<G>;
-    static int max_set[kMaxDevices] = {};
-    if (int rc = ensure_smem(reinterpret_cast<const void *>(kern), kScSmem, max_set)) return rc;
-    int sms = 0;
-    if (int rc = sm_count(&sms)) return rc;
-    const long long F = static_cast<long long>(d->batch) * d->n_kv_heads * d->n_pages;
-    const long long per_cta = static_cast<long long>(kScMinPagesPerWorker) * kScNC;
-    long long n_ctas = std::min<long long>(static_cast<long long>(sms) * kScCPS, (F + per_cta - 1) / per_cta);
-    n_ctas = std::max<long long>(1, std::min<long long>(n_ctas, kScMaxCtas));
-    CUtensorMap tsm, tsm8;
-    if (int rc = make_summ_map(&tsm, summ, F, kScPages)) return rc;
-    if (int rc = make_summ_map(&tsm8, summ, F, 8)) return rc;
-    {  // a programmatic dependent launch (unless the stream's last operation is
-       // an event wait): the setup overlaps the kernel before it
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(static_cast<unsigned>(n_ctas));
-      cfg.blockDim = dim3(kScThreads);
-      cfg.dynamicSmemBytes = kScSmem;
-      cfg.stream = st;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr[0].val.programmaticStreamSerializationAllowed = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = pdl_first ? 1 : 0;
-      const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tsm, tsm8, q, d->n_kv_heads, d->n_pages, F,
-                                               w.scores, scores);
-      if (e != cudaSuccess) return cuda_fail(e, "k_page_scores");
+    int rc;
+    switch (G * T) {
+      case 1: rc = launch_scores<1>(d, q, summ, T, w, scores, st, pdl_first); break;
+      case 2: rc = launch_scores<2>(d, q, summ, T, w, scores, st, pdl_first); break;
+      case 4: rc = launch_scores<4>(d, q, summ, T, w, scores, st, pdl_first); break;
+      case 8: rc = launch_scores<8>(d, q, summ, T, w, scores, st, pdl_first); break;
+      default: rc = launch_scores<16>(d, q, summ, T, w, scores, st, pdl_first); break;
     }
+    if (rc) return rc;
   }
   if (!(parts & kSelTopk)) return KVR_OK;
   // 2. top-k per unit: a programmatic dependent launch right after the
@@ -365,12 +387,12 @@ int launch_select_g(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
 int launch_select(const kvr_dims *d, const uint16_t *q, const uint16_t *summ,
                   const int32_t *ptab, int k, SelectWs w, int32_t *sel, int32_t *sel_phys,
                   float *scores, const SpecArgs &spec, cudaStream_t st, bool pdl_first = true,
-                  const int32_t *seq_len = nullptr, int parts = kSelBoth) {
+                  const int32_t *seq_len = nullptr, int parts = kSelBoth, int T = 1) {
   switch (d->n_q_heads / d->n_kv_heads) {
-    case 1: return launch_select_g<1>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len, parts);
-    case 2: return launch_select_g<2>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len, parts);
-    case 4: return launch_select_g<4>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len, parts);
-    default: return launch_select_g<8>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len, parts);
+    case 1: return launch_select_g<1>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len, parts, T);
+    case 2: return launch_select_g<2>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len, parts, T);
+    case 4: return launch_select_g<4>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len, parts, T);
+    default: return launch_select_g<8>(d, q, summ, ptab, k, w, sel, sel_phys, scores, spec, st, pdl_first, seq_len, parts, T);
   }
 }
 
@@ -394,7 +416,7 @@ int sm_count(int *out) {
 // CTAs per cluster of the attention kernel: the largest Q in {8, 4, 2} whose
 // clusters for all units are resident at once (and that leaves every worker
 // at least one chunk), else 1.  Occupancy per Q is cached per device.
-template <int G, int P>
+template <int NR, int P>
 int attn_cluster_size(const void *kern, size_t smem, long long units, long long kc, int *q_out) {
   static int cap[kMaxDevices][4] = {};  // resident clusters for Q = 1, 2, 4, 8 (0: not yet asked)
   int dev = 0;
@@ -431,21 +453,21 @@ int attn_cluster_size(const void *kern, size_t smem, long long units, long long 
   return KVR_OK;
 }
 
-template <int G, int P>
+template <int NR, int P, bool CAUSAL>
 int launch_attn_gp(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &tv,
                    const uint16_t *q, const int32_t *sel_phys, int k, int n_phys, float scale,
-                   const uint8_t *filter, int filter_mode, AttnWs w, float *out, cudaStream_t st,
+                   const uint8_t *filter, int filter_mode, AttnWs w, void *out, cudaStream_t st,
                    bool pdl_ok, AttnLen len) {
   (void)w;
-  using Cfg = AttnCfg<G, P>;
+  using Cfg = AttnCfg<NR, P>;
   const long long units = static_cast<long long>(d->batch) * d->n_kv_heads;
   const long long kc = static_cast<long long>(k) * Cfg::CPP;
   const size_t smem = Cfg::kSmem;
-  auto kern = k_sparse_decode<G, P>;
+  auto kern = k_sparse_decode<NR, P, CAUSAL>;
   static int max_set[kMaxDevices] = {};
   if (int rc = ensure_smem(reinterpret_cast<const void *>(kern), smem, max_set)) return rc;
   int Q = 1;
-  if (int rc = attn_cluster_size<G, P>(reinterpret_cast<const void *>(kern), smem, units, kc, &Q))
+  if (int rc = attn_cluster_size<NR, P>(reinterpret_cast<const void *>(kern), smem, units, kc, &Q))
     return rc;
   if (units * Q > 0x7fffffffLL) return KVR_ERR_UNSUPPORTED_SHAPE;
   const float scale_log2 = scale * 1.4426950408889634f;
@@ -466,36 +488,38 @@ int launch_attn_gp(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_ok ? 2 : 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tk, tv, q, sel_phys, d->n_kv_heads, k,
-                                           n_phys, Q, scale_log2, filter, filter_mode, out,
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tk, tv, q, sel_phys, len.sel_log, d->n_kv_heads,
+                                           k, n_phys, Q, len.T, d->n_q_heads / d->n_kv_heads,
+                                           scale_log2, filter, filter_mode, out, len.out_bf16,
                                            len.seq_len, len.page_table, d->n_pages);
   if (e != cudaSuccess) return cuda_fail(e, "k_sparse_decode");
   return KVR_OK;
 }
 
-template <int G>
+template <int NR, bool CAUSAL>
 int launch_attn_g(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &tv,
                   const uint16_t *q, const int32_t *sel_phys, int k, int n_phys, float scale,
-                  const uint8_t *filter, int filter_mode, AttnWs w, float *out, cudaStream_t st,
+                  const uint8_t *filter, int filter_mode, AttnWs w, void *out, cudaStream_t st,
                   bool pdl_ok, AttnLen len) {
   switch (d->page_size) {
     case 16:
-      return launch_attn_gp<G, 16>(d, tk, tv, q, sel_phys, k, n_phys, scale, filter, filter_mode,
-                                   w, out, st, pdl_ok, len);
+      return launch_attn_gp<NR, 16, CAUSAL>(d, tk, tv, q, sel_phys, k, n_phys, scale, filter,
+                                            filter_mode, w, out, st, pdl_ok, len);
     case 32:
-      return launch_attn_gp<G, 32>(d, tk, tv, q, sel_phys, k, n_phys, scale, filter, filter_mode,
-                                   w, out, st, pdl_ok, len);
+      return launch_attn_gp<NR, 32, CAUSAL>(d, tk, tv, q, sel_phys, k, n_phys, scale, filter,
+                                            filter_mode, w, out, st, pdl_ok, len);
     default:
-      return launch_attn_gp<G, 64>(d, tk, tv, q, sel_phys, k, n_phys, scale, filter, filter_mode,
-                                   w, out, st, pdl_ok, len);
+      return launch_attn_gp<NR, 64, CAUSAL>(d, tk, tv, q, sel_phys, k, n_phys, scale, filter,
+                                            filter_mode, w, out, st, pdl_ok, len);
   }
 }
 
 // pdl_ok: launch as a programmatic dependent launch (false right after an
-// event wait on the stream, whose dependency must stay a full one)
+// event wait on the stream, whose dependency must stay a full one).  The
+// query rows per unit, G len.T, are 1, 2, 4, 8 or 16 (checked by the callers).
 int launch_attn(const kvr_dims *d, const uint16_t *q, const uint16_t *k_pool,
                 const uint16_t *v_pool, int64_t n_phys, const int32_t *sel_phys, int k,
-                float scale, const uint8_t *filter, int filter_mode, AttnWs w, float *out,
+                float scale, const uint8_t *filter, int filter_mode, AttnWs w, void *out,
                 cudaStream_t st, bool pdl_ok = true, AttnLen len = AttnLen()) {
   CUtensorMap tk, tv;
   int rc = make_pool_map(&tk, k_pool, d, n_phys);
@@ -504,11 +528,19 @@ int launch_attn(const kvr_dims *d, const uint16_t *q, const uint16_t *k_pool,
   if (rc) return rc;
   if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(kD));
   const int np = static_cast<int>(n_phys);
-  switch (d->n_q_heads / d->n_kv_heads) {
-    case 1: return launch_attn_g<1>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
-    case 2: return launch_attn_g<2>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
-    case 4: return launch_attn_g<4>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
-    default: return launch_attn_g<8>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
+  if (len.T == 1) {  // one query token: no causal limits (G <= 8 rows)
+    switch (d->n_q_heads / d->n_kv_heads) {
+      case 1: return launch_attn_g<1, false>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
+      case 2: return launch_attn_g<2, false>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
+      case 4: return launch_attn_g<4, false>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
+      default: return launch_attn_g<8, false>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
+    }
+  }
+  switch (d->n_q_heads / d->n_kv_heads * len.T) {
+    case 2: return launch_attn_g<2, true>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
+    case 4: return launch_attn_g<4, true>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
+    case 8: return launch_attn_g<8, true>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
+    default: return launch_attn_g<16, true>(d, tk, tv, q, sel_phys, k, np, scale, filter, filter_mode, w, out, st, pdl_ok, len);
   }
 }
 
@@ -749,6 +781,61 @@ int kvr_sparse_decode_attn_len(const kvr_dims *dims, const uint16_t *q, const ui
   len.seq_len = seq_len;
   len.page_table = page_table;
   return launch_attn(dims, q, k_pool, v_pool, dims->n_phys_pages, sel_phys, top_k, scale, nullptr,
+                     0, carve_attn(dims, top_k, (uint8_t *)ws), out,
+                     static_cast<cudaStream_t>(stream), true, len);
+}
+
+// Query rows per unit of a several-queries call: G T in {1, 2, 4, 8, 16}.
+static int check_rows(const kvr_dims *dims, int32_t n_query) {
+  if (n_query <= 0) return KVR_ERR_INVALID_ARG;
+  const int64_t nr = static_cast<int64_t>(dims->n_q_heads / dims->n_kv_heads) * n_query;
+  if (nr != 1 && nr != 2 && nr != 4 && nr != 8 && nr != 16) return KVR_ERR_UNSUPPORTED_SHAPE;
+  return KVR_OK;
+}
+
+int kvr_select_pages_multi(const kvr_dims *dims, const uint16_t *qs, int32_t n_query,
+                           const uint16_t *summ, const int32_t *page_table, const int32_t *seq_len,
+                           int32_t top_k, int32_t *sel, int32_t *sel_phys, float *scores_opt,
+                           void *ws, size_t ws_bytes, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_topk(dims, top_k))) return rc;
+  if ((rc = check_rows(dims, n_query))) return rc;
+  if (!qs || !summ || !page_table || !seq_len || !sel) return KVR_ERR_INVALID_ARG;
+  if (!aligned16(qs) || !aligned16(summ) || !aligned16(page_table) || !aligned16(seq_len) ||
+      !aligned16(sel) || (sel_phys && !aligned16(sel_phys)) || (scores_opt && !aligned16(scores_opt)))
+    return KVR_ERR_ALIGN;
+  if ((rc = check_ws(ws, ws_bytes, select_ws_bytes(dims)))) return rc;
+  return launch_select(dims, qs, summ, page_table, top_k, carve_select(dims, (uint8_t *)ws), sel,
+                       sel_phys, scores_opt, no_spec(), static_cast<cudaStream_t>(stream), true,
+                       seq_len, kSelBoth, n_query);
+}
+
+int kvr_sparse_decode_attn_multi(const kvr_dims *dims, const uint16_t *qs, int32_t n_query,
+                                 const uint16_t *k_pool, const uint16_t *v_pool,
+                                 const int32_t *page_table, const int32_t *seq_len,
+                                 const int32_t *sel, const int32_t *sel_phys, int32_t top_k,
+                                 float scale, void *out, int32_t out_dtype, void *ws,
+                                 size_t ws_bytes, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_topk(dims, top_k))) return rc;
+  if ((rc = check_rows(dims, n_query))) return rc;
+  if (out_dtype != KVR_DTYPE_F32 && out_dtype != KVR_DTYPE_BF16) return KVR_ERR_INVALID_ARG;
+  if (!qs || !k_pool || !v_pool || !page_table || !seq_len || !sel_phys || !out) return KVR_ERR_INVALID_ARG;
+  if (n_query > 1 && !sel) return KVR_ERR_INVALID_ARG;
+  if (!aligned16(qs) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(page_table) ||
+      !aligned16(seq_len) || !aligned16(sel_phys) || (sel && !aligned16(sel)) || !aligned16(out))
+    return KVR_ERR_ALIGN;
+  if (std::isnan(scale)) return KVR_ERR_INVALID_ARG;
+  if ((rc = check_ws(ws, ws_bytes, attn_ws_bytes(dims, top_k)))) return rc;
+  AttnLen len;
+  len.seq_len = seq_len;
+  len.page_table = page_table;
+  len.T = n_query;
+  len.sel_log = n_query > 1 ? sel : nullptr;
+  len.out_bf16 = out_dtype == KVR_DTYPE_BF16 ? 1 : 0;
+  return launch_attn(dims, qs, k_pool, v_pool, dims->n_phys_pages, sel_phys, top_k, scale, nullptr,
                      0, carve_attn(dims, top_k, (uint8_t *)ws), out,
                      static_cast<cudaStream_t>(stream), true, len);
 }

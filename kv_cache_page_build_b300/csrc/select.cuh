@@ -106,11 +106,15 @@ __device__ __forceinline__ int sc_chunk(long long f, int pos, int N, long long e
   return static_cast<int>(min(static_cast<long long>(min(kScPages, N - pos)), e - f));
 }
 
-template <int G>
+// NR query rows per unit: the G heads of the group times the T query tokens
+// of the step (q [B][T][Hq][D]); the score is the mean over the NR rows.
+// Rows take the MMA's 8 columns, in CB blocks.
+template <int NR>
 __global__ void __launch_bounds__(kScThreads, kScCPS)
     k_page_scores(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_s8,
-                  const uint16_t *__restrict__ q, int H, int N, long long F,
+                  const uint16_t *__restrict__ q, int H, int N, long long F, int T, int G,
                   float *__restrict__ ws_scores, float *__restrict__ scores_out) {
+  constexpr int CB = NR > 8 ? 2 : 1;
   constexpr int HALF = kScPages * 128;  // one 64-channel box of a stage
   extern __shared__ uint8_t smem_raw[];
   // the swizzle pattern repeats every 1024 bytes: align the ring to it
@@ -201,9 +205,10 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
   int pos;
   flat_divmod(f, N, u, pos);
   const int gq = lane >> 2, tq = lane & 3, mi = lane >> 3, mr = lane & 7;
-  // [q- | q+] of head gq as B fragments: k-step kk < 8 meets kmin channels
-  // 16kk.., kk >= 8 meets kmax channels 16(kk - 8)..; words hold bf16 pairs
-  uint32_t qa[16][2];
+  // [q- | q+] of row 8 cb + gq (token j / G, head j % G) as B fragments:
+  // k-step kk < 8 meets kmin channels 16kk.., kk >= 8 meets kmax channels
+  // 16(kk - 8)..; words hold bf16 pairs
+  uint32_t qa[CB][16][2];
   long long q_unit = -1;
 #pragma unroll 1
   for (int use = 0; f < e; ++use) {
@@ -211,18 +216,22 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
     if (q_unit != u) {
       const int ui = static_cast<int>(u);  // < B H
       const int b = ui / H, g = ui - b * H;
-      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-          q + (static_cast<size_t>(b) * Hq + g * G + min(gq, G - 1)) * kD);
-      const bool on = gq < G;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int cb = 0; cb < CB; ++cb) {
+        const int jr = min(8 * cb + gq, NR - 1);
+        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+            q + ((static_cast<size_t>(b) * T + jr / G) * Hq + g * G + jr % G) * kD);
+        const bool on = 8 * cb + gq < NR;
 #pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
-          const uint32_t w = on ? __ldg(qrow + 8 * kk + 4 * hlf + tq) : 0u;
-          // per bf16 half: all ones where the sign bit is set
-          const uint32_t neg = ((w >> 15) & 0x00010001u) * 0xffffu;
-          qa[kk][hlf] = w & neg;        // q- with kmin
-          qa[8 + kk][hlf] = w & ~neg;   // q+ with kmax
+        for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+          for (int hlf = 0; hlf < 2; ++hlf) {
+            const uint32_t w = on ? __ldg(qrow + 8 * kk + 4 * hlf + tq) : 0u;
+            // per bf16 half: all ones where the sign bit is set
+            const uint32_t neg = ((w >> 15) & 0x00010001u) * 0xffffu;
+            qa[cb][kk][hlf] = w & neg;        // q- with kmin
+            qa[cb][8 + kk][hlf] = w & ~neg;   // q+ with kmax
+          }
         }
       }
       q_unit = u;
@@ -243,32 +252,42 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
       // odd k-steps in separate accumulators.  Rows past cnt hold stale
       // shared memory; their results are never stored.
       const uint32_t sb = ring + s * kScStageBytes;
-      float c[2][4], d[2][4];
+      float c[CB][2][4], d[CB][2][4];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
+      for (int cb = 0; cb < CB; ++cb)
 #pragma unroll
-        for (int x = 0; x < 4; ++x) c[mt][x] = d[mt][x] = 0.f;
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int x = 0; x < 4; ++x) c[cb][mt][x] = d[cb][mt][x] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < 16; ++kk)
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
           uint32_t a[4];
           ldsm_x4(swz<HALF>(sb, 16 * mt + 8 * (mi & 1) + mr, 2 * kk + (mi >> 1)), a);
-          if (kk & 1)
-            mma_bf16_16816(d[mt], a[0], a[1], a[2], a[3], qa[kk][0], qa[kk][1]);
-          else
-            mma_bf16_16816(c[mt], a[0], a[1], a[2], a[3], qa[kk][0], qa[kk][1]);
+#pragma unroll
+          for (int cb = 0; cb < CB; ++cb) {
+            if (kk & 1)
+              mma_bf16_16816(d[cb][mt], a[0], a[1], a[2], a[3], qa[cb][kk][0], qa[cb][kk][1]);
+            else
+              mma_bf16_16816(c[cb][mt], a[0], a[1], a[2], a[3], qa[cb][kk][0], qa[cb][kk][1]);
+          }
         }
-      // sum over the heads in a fixed order: the lane's two heads, then the
-      // four column pairs (heads G.. are zero columns)
+      // sum over the rows in a fixed order: the lane's two columns, then the
+      // four column pairs (rows NR.. are zero columns), then the blocks
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          float t = (c[mt][2 * r] + d[mt][2 * r]) + (c[mt][2 * r + 1] + d[mt][2 * r + 1]);
-          t += __shfl_xor_sync(0xffffffffu, t, 1);
-          t += __shfl_xor_sync(0xffffffffu, t, 2);
-          t *= (1.0f / G);
+          float t = 0.f;
+#pragma unroll
+          for (int cb = 0; cb < CB; ++cb) {
+            float x = (c[cb][mt][2 * r] + d[cb][mt][2 * r]) + (c[cb][mt][2 * r + 1] + d[cb][mt][2 * r + 1]);
+            x += __shfl_xor_sync(0xffffffffu, x, 1);
+            x += __shfl_xor_sync(0xffffffffu, x, 2);
+            t = cb == 0 ? x : t + x;
+          }
+          t *= (1.0f / NR);
           const int p = 16 * mt + gq + 8 * r;
           if (tq == 0 && p < cnt) {
             ws_scores[f + p] = t;

@@ -103,6 +103,8 @@ _SIGS = {
     "kvr_get_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "kvr_stream_wait": (_I, [_P, ctypes.c_uint64]),
     "kvr_select_pages_noalloc": (_I, [_D, _P, _P, _P, _I, _P, _P, _P, _P]),
+    "kvr_select_pages_multi": (_I, [_D, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _S, _P]),
+    "kvr_sparse_decode_attn_multi": (_I, [_D, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P, _I, _P, _S, _P]),
     "kvr_error_string": (ctypes.c_char_p, [_I]),
     "kvr_kv_bytes": (ctypes.c_uint64, [ctypes.c_int64] * 5),
 }
@@ -317,6 +319,27 @@ def kvr_select_pages_noalloc(d, q, summ, page_table, top_k, sel, sel_phys, score
     return _check(_lib.kvr_select_pages_noalloc(_d(d), _ptr(q), _ptr(summ), _ptr(page_table), int(top_k),
                                                 _ptr(sel), _ptr(sel_phys), _ptr(scores_opt), _stream(stream)),
                   "kvr_select_pages_noalloc")
+
+
+def kvr_select_pages_multi(d, qs, n_query, summ, page_table, seq_len, top_k, sel, sel_phys, scores_opt, ws,
+                           ws_bytes, stream=None):
+    """Selection for a step of n_query query tokens per sequence (qs
+    [B][T][Hq][D]; see include/kvr.h)."""
+    return _check(_lib.kvr_select_pages_multi(_d(d), _ptr(qs), int(n_query), _ptr(summ), _ptr(page_table),
+                                              _ptr(seq_len), int(top_k), _ptr(sel), _ptr(sel_phys),
+                                              _ptr(scores_opt), _ptr(ws), int(ws_bytes), _stream(stream)),
+                  "kvr_select_pages_multi")
+
+
+def kvr_sparse_decode_attn_multi(d, qs, n_query, k_pool, v_pool, page_table, seq_len, sel, sel_phys, top_k,
+                                 scale, out, out_dtype, ws, ws_bytes, stream=None):
+    """Causal attention of n_query query tokens per sequence over the step's
+    selection; out_dtype KVR_DTYPE_F32 or KVR_DTYPE_BF16."""
+    return _check(_lib.kvr_sparse_decode_attn_multi(_d(d), _ptr(qs), int(n_query), _ptr(k_pool), _ptr(v_pool),
+                                                    _ptr(page_table), _ptr(seq_len), _ptr(sel), _ptr(sel_phys),
+                                                    int(top_k), float(scale), _ptr(out), int(out_dtype), _ptr(ws),
+                                                    int(ws_bytes), _stream(stream)),
+                  "kvr_sparse_decode_attn_multi")
 
 
 def kvr_get_status(stream=None) -> int:

@@ -252,3 +252,34 @@ def test_pipeline_binding_checks_the_marks_length():
     with pytest.raises(kvr.KvrError):
         kvr.kvr_pipeline_step(D(), [], None, 64, 0.8, 0.0, 0, 0, 0)
     assert st.step == 0
+
+
+def test_several_queries_arguments_rejected_before_launch():
+    """kvr_select_pages_multi and kvr_sparse_decode_attn_multi: the query
+    rows per unit (G T) must be 1, 2, 4, 8 or 16; the lengths are required,
+    the logical ids too when T > 1; the output type is one of the two."""
+    lib = kvr.raw()
+    d = D()                                          # G = 4
+    big = 1 << 40
+    sel = lambda T, **kw: lib.kvr_select_pages_multi(
+        ctypes.byref(kw.get("d", d)), kw.get("qs", FAKE), T, FAKE, FAKE, kw.get("lens", FAKE), 8, FAKE, FAKE, None,
+        FAKE, big, None)
+    assert sel(0) == kvr.KVR_ERR_INVALID_ARG
+    assert sel(3) == kvr.KVR_ERR_UNSUPPORTED_SHAPE   # 12 rows
+    assert sel(8) == kvr.KVR_ERR_UNSUPPORTED_SHAPE   # 32 rows
+    assert sel(2, lens=None) == kvr.KVR_ERR_INVALID_ARG
+    assert sel(2, qs=FAKE + 8) == kvr.KVR_ERR_ALIGN
+    need = kvr.kvr_workspace_size(d, 64, kvr.KVR_OP_ATTN)
+
+    def attn(T, sel_log=FAKE, lens=FAKE, dtype=kvr.KVR_DTYPE_F32, ws_bytes=need, dd=d):
+        return lib.kvr_sparse_decode_attn_multi(ctypes.byref(dd), FAKE, T, FAKE, FAKE, FAKE, lens, sel_log, FAKE, 64,
+                                                0.0, FAKE, dtype, FAKE, ws_bytes, None)
+    assert attn(0) == kvr.KVR_ERR_INVALID_ARG
+    assert attn(5) == kvr.KVR_ERR_UNSUPPORTED_SHAPE
+    assert attn(2, sel_log=None) == kvr.KVR_ERR_INVALID_ARG       # causal limits need the logical ids
+    assert attn(2, lens=None) == kvr.KVR_ERR_INVALID_ARG
+    assert attn(2, dtype=2) == kvr.KVR_ERR_INVALID_ARG
+    assert attn(2, sel_log=FAKE + 4) == kvr.KVR_ERR_ALIGN
+    assert attn(2, ws_bytes=need - 1) == kvr.KVR_ERR_WORKSPACE
+    assert attn(4, dd=D(n_q_heads=16, n_kv_heads=8), ws_bytes=need - 1) == kvr.KVR_ERR_WORKSPACE  # G 2, T 4: 8 rows
+    assert attn(16, dd=D(n_q_heads=16, n_kv_heads=8)) == kvr.KVR_ERR_UNSUPPORTED_SHAPE            # 32 rows
