@@ -434,6 +434,28 @@ def measure_hbm(wl_name, args, world, local, steps, warmup, e2e_calls, kernel_la
     sel_avg, n_sel = _graph_time(torch, graph_sel, LK, kernel_launches)
     status |= kvr.kvr_get_status()
 
+    # several query tokens per step (kvr_sparse_decode_attn_multi): the T
+    # newest tokens of every (full) sequence query the same selected pages,
+    # so the bytes stay those of one query; T = 1 also with the bf16 store
+    seq_full = torch.full((B,), N * P, dtype=torch.int32, device=dev)
+    multi = {}
+    for T, dt in ((1, kvr.KVR_DTYPE_F32), (1, kvr.KVR_DTYPE_BF16), (2, kvr.KVR_DTYPE_F32), (4, kvr.KVR_DTYPE_F32)):
+        qm = qs[:T].permute(1, 0, 2, 3).contiguous()           # [B][T][Hq][D]
+        selm = torch.empty((B, H, k), dtype=torch.int32, device=dev)
+        selpm = torch.empty_like(selm)
+        kvr.kvr_select_pages_multi(d, qm, T, summs[0], page_table, seq_full, k, selm, selpm, None, ws, ws_n)
+        out_m = torch.empty((B, T, Hq, D), dtype=torch.float32 if dt == kvr.KVR_DTYPE_F32 else torch.int16,
+                            device=dev)
+        gm = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gm):
+            for i in range(LK):
+                c = i % COPIES
+                kvr.kvr_sparse_decode_attn_multi(d, qm, T, k_pools[c], v_pools[c], page_table, seq_full, selm, selpm,
+                                                 k, 0.0, out_m, dt, wa, wa_n)
+        t_m, _ = _graph_time(torch, gm, LK, kernel_launches)
+        multi[f"T={T}" + (" bf16" if dt == kvr.KVR_DTYPE_BF16 else "")] = t_m
+    status |= kvr.kvr_get_status()
+
     # end to end through the public entry point with host buffers: q copied
     # in from pinned memory and the output copied back every step, the
     # stream synchronised per step; untimed warm-up calls on the same buffers
@@ -481,6 +503,7 @@ def measure_hbm(wl_name, args, world, local, steps, warmup, e2e_calls, kernel_la
     status |= kvr.kvr_get_status()
     res = dict(wl=wl, tau=wl_trace.tau, copies=COPIES, steps=steps, L=L, value=value, t_max=t_max,
                attn_avg=attn_avg, n_attn=n_attn, sel_avg=sel_avg, n_sel=n_sel, app_avg=app_avg, summ_s=summ_s,
+               multi=multi,
                e2e_value=e2e_value, e2e_calls=e2e_calls, clk=clk, status=status,
                attn_bytes=B * H * k * P * 2 * D * 2,          # selected K and V rows read per launch
                summ_bytes=B * H * N * 2 * D * 2,               # summaries read by the selection
@@ -512,6 +535,11 @@ def hbm_kernels(r):
         "k_build_summaries": {"us": round(r["summ_s"] * 1e6, 3), "bytes": build_bytes,
                               "gbs": round(build_bytes / r["summ_s"] / 1e9, 1),
                               "note": "once per cache (prefill), not in the step"},
+        "several queries per step (k_sparse_decode, kvr_sparse_decode_attn_multi)": {
+            name: {"us": round(t * 1e6, 3), "gbs": round(r["attn_bytes"] / t / 1e9, 1),
+                   "frac": round(r["attn_bytes"] / t / 1e9 / hbm, 4),
+                   "vs_one_query": round(t / r["multi"]["T=1"], 3)}
+            for name, t in r["multi"].items()},
     }
 
 

@@ -472,6 +472,18 @@ int kvr_pipeline_step(const kvr_dims *dims, int32_t n_layers, kvr_layer *layers,
  * exact reading, let every stream that runs library kernels finish first. */
 int kvr_get_status(void *stream, uint32_t *status_out);
 
+/* Bound, in ns, of the kernels' waits for progress: a copy landing in
+ * shared memory, a ring stage being released (0 restores the default, 2 s).
+ * When such a wait runs out the kernel sets KVR_ST_WAIT_TIMEOUT, stops
+ * issuing copies, waits for the copies it already issued (always with the
+ * 2 s bound, so no copy is left in flight) and returns; the outputs of that
+ * call are then unspecified and the context stays usable.  For tests of that
+ * path, and for callers that want a hung copy engine reported sooner.  The
+ * bound is a process-wide host setting passed to every launch enqueued
+ * after the call (a captured graph keeps the bound of its capture).
+ * Returns KVR_OK. */
+int kvr_set_wait_limit(uint64_t ns);
+
 /* Bounded host-side wait: return once all work enqueued on `stream` has
  * finished, or after timeout_us microseconds of host time, whichever comes
  * first (polling cudaStreamQuery; the thread yields between polls).

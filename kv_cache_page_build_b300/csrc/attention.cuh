@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
     k_sparse_decode(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const uint16_t *__restrict__ q,
                     const int32_t *__restrict__ sel_phys, const int32_t *__restrict__ sel_log,
-                    int H, int k, int n_phys, int Q, int T, int G, float scale_log2,
+                    int H, int k, int n_phys, int Q, int T, int G, float scale_log2, uint64_t wait_ns,
                     const uint8_t *__restrict__ filter, int filter_mode, void *__restrict__ out,
                     int out_bf16, const int32_t *__restrict__ seq_len,
                     const int32_t *__restrict__ page_table, int N) {
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
           }
           ++i;
           t_prog = global_timer_ns();
-        } else if (global_timer_ns() - t_prog > kWaitNs) {
+        } else if (global_timer_ns() - t_prog > wait_ns) {
           set_status(KVR_ST_WAIT_TIMEOUT);
           s_abort = 1;
         }
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
     // this lane's last issued chunks
     if (feeder && abort)
       for (int j = max(0, i - R); j < i; ++j)
-        mbar_wait(&full[lane * R + j % R], static_cast<uint32_t>((j / R) & 1));
+        mbar_wait(&full[lane * R + j % R], static_cast<uint32_t>((j / R) & 1), kWaitNs);
     __syncwarp();
     cluster_wait();  // the start handshake's second half (see above)
   } else {
@@ -469,10 +469,11 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
 #pragma unroll 1
     for (int i = 0; i < n; ++i) {
       const int s = cw * R + i % R;  // this warp's stages in turn
-      bool have = false;
+      bool have = false, landed = false;
       if (__shfl_sync(0xffffffffu, s_abort, 0) == 0) {  // warp-uniform
-        const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((i / R) & 1));
+        const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((i / R) & 1), wait_ns);
         if (__all_sync(0xffffffffu, ok)) {
+          landed = true;
           have = s_ok[s] != 0;
         } else if (lane == 0) {
           s_abort = 1;
@@ -494,7 +495,10 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
         attn_chunk<NR, P, CAUSAL>(ring + s * Cfg::kStageBytes, qb, scale_log2, m_run, l_run, o, lane, nv, lim);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      // a stage is released only once its copy has landed: after an abort
+      // the producer may not refill a stage whose copy is still in flight
+      // (it drains those before the CTA leaves)
+      if (lane == 0 && landed) mbar_arrive(&empty[s]);
     }
     // ---- this worker's partial, pushed to the CTAs that merge it
     float lr[CB][2];

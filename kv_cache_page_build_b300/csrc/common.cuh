@@ -17,7 +17,11 @@ namespace kvr {
 
 constexpr int kD = 128;                 // head_dim supported by the kernels
 constexpr int kMaxPages = 16384;        // logical pages per sequence
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s bound on any barrier wait
+// 2 s: the default bound of a kernel's wait for progress (a copy to land, a
+// stage to be released; the launch passes the bound in force, which
+// kvr_set_wait_limit changes), and always the bound of the drain of copies
+// already issued.
+constexpr uint64_t kWaitNs = 2000000000ull;
 
 // Device status word (one per device that loads the library): bits KVR_ST_*.
 __device__ uint32_t g_status;
@@ -169,16 +173,16 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait until the barrier's phase `parity` completes, for at most kWaitNs.
-// Returns false (and sets KVR_ST_WAIT_TIMEOUT) when the bound is hit.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Wait until the barrier's phase `parity` completes, for at most `limit`
+// ns.  Returns false (and sets KVR_ST_WAIT_TIMEOUT) when the bound is hit.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitNs) {
+    if (global_timer_ns() - t0 > limit) {
       set_status(KVR_ST_WAIT_TIMEOUT);
       return false;
     }

@@ -8,6 +8,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <chrono>
 #include <cmath>
 #include <cstdio>
@@ -27,6 +28,9 @@ namespace {
 using namespace kvr;
 
 thread_local char g_err_text[512];
+
+// Bound of the kernels' waits for progress, passed to every streaming launch.
+std::atomic<uint64_t> g_wait_limit{kWaitNs};
 
 int cuda_fail(cudaError_t e, const char *where) {
   std::snprintf(g_err_text, sizeof g_err_text, "CUDA error in %s: %s", where,
@@ -310,7 +314,8 @@ int launch_scores(const kvr_dims *d, const uint16_t *q, const uint16_t *summ, in
   cfg.attrs = attr;
   cfg.numAttrs = pdl_first ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tsm, tsm8, q, d->n_kv_heads, d->n_pages, F, T,
-                                           d->n_q_heads / d->n_kv_heads, w.scores, scores);
+                                           d->n_q_heads / d->n_kv_heads,
+                                           g_wait_limit.load(std::memory_order_relaxed), w.scores, scores);
   if (e != cudaSuccess) return cuda_fail(e, "k_page_scores");
   return KVR_OK;
 }
@@ -490,7 +495,8 @@ int launch_attn_gp(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &
   cfg.numAttrs = pdl_ok ? 2 : 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tk, tv, q, sel_phys, len.sel_log, d->n_kv_heads,
                                            k, n_phys, Q, len.T, d->n_q_heads / d->n_kv_heads,
-                                           scale_log2, filter, filter_mode, out, len.out_bf16,
+                                           scale_log2, g_wait_limit.load(std::memory_order_relaxed),
+                                           filter, filter_mode, out, len.out_bf16,
                                            len.seq_len, len.page_table, d->n_pages);
   if (e != cudaSuccess) return cuda_fail(e, "k_sparse_decode");
   return KVR_OK;
@@ -1241,6 +1247,11 @@ int kvr_get_status(void *stream, uint32_t *status_out) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "status clear");
   *status_out = v;
+  return KVR_OK;
+}
+
+int kvr_set_wait_limit(uint64_t ns) {
+  g_wait_limit.store(ns ? ns : kWaitNs, std::memory_order_relaxed);
   return KVR_OK;
 }
 

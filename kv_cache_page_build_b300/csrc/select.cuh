@@ -113,7 +113,7 @@ template <int NR>
 __global__ void __launch_bounds__(kScThreads, kScCPS)
     k_page_scores(const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_s8,
                   const uint16_t *__restrict__ q, int H, int N, long long F, int T, int G,
-                  float *__restrict__ ws_scores, float *__restrict__ scores_out) {
+                  uint64_t wait_ns, float *__restrict__ ws_scores, float *__restrict__ scores_out) {
   constexpr int CB = NR > 8 ? 2 : 1;
   constexpr int HALF = kScPages * 128;  // one 64-channel box of a stage
   extern __shared__ uint8_t smem_raw[];
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
           if (pos == N) pos = 0;
           ++use;
           t_prog = global_timer_ns();
-        } else if (global_timer_ns() - t_prog > kWaitNs) {
+        } else if (global_timer_ns() - t_prog > wait_ns) {
           set_status(KVR_ST_WAIT_TIMEOUT);
           s_abort = 1;
         }
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
     }
     if (feeder && abort)  // never leave with copies in flight
       for (int j = max(0, use - kScR); j < use; ++j)
-        mbar_wait(&full[lane * kScR + j % kScR], static_cast<uint32_t>((j / kScR) & 1));
+        mbar_wait(&full[lane * kScR + j % kScR], static_cast<uint32_t>((j / kScR) & 1), kWaitNs);
     return;
   }
 
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
     const int s = warp * kScR + use % kScR;
     bool have = false;
     if (__shfl_sync(0xffffffffu, s_abort, 0) == 0) {  // warp-uniform
-      const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((use / kScR) & 1));
+      const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((use / kScR) & 1), wait_ns);
       if (__all_sync(0xffffffffu, ok)) {
         have = true;
       } else if (lane == 0) {
@@ -296,7 +296,10 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
         }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    // a stage is released only once its copy has landed: after an abort the
+    // producer may not refill a stage whose copy is still in flight (it
+    // drains those before the CTA leaves)
+    if (lane == 0 && have) mbar_arrive(&empty[s]);
     f += cnt;
     pos += cnt;
     if (pos == N) {

@@ -102,6 +102,7 @@ _SIGS = {
     "kvr_stand_in_read": (_I, [ctypes.POINTER(kvr_stand_in), ctypes.c_uint64, ctypes.c_uint64, _P]),
     "kvr_get_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "kvr_stream_wait": (_I, [_P, ctypes.c_uint64]),
+    "kvr_set_wait_limit": (_I, [ctypes.c_uint64]),
     "kvr_select_pages_noalloc": (_I, [_D, _P, _P, _P, _I, _P, _P, _P, _P]),
     "kvr_select_pages_multi": (_I, [_D, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _S, _P]),
     "kvr_sparse_decode_attn_multi": (_I, [_D, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P, _I, _P, _S, _P]),
@@ -356,6 +357,11 @@ def kvr_stream_wait(stream=None, timeout_us: int = 0) -> bool:
         return False
     _check(rc, "kvr_stream_wait")
     return True
+
+
+def kvr_set_wait_limit(ns: int):
+    """Bound of the kernels' waits for progress, in ns (0: the default 2 s)."""
+    return _check(_lib.kvr_set_wait_limit(int(ns)), "kvr_set_wait_limit")
 
 
 def kvr_error_string(code: int) -> str:

@@ -56,9 +56,9 @@ def protocol_of(kernel):
     m = re.search(r"if \((\w+) < (\w+) \|\| mbar_test_wait\(&empty\[s\], "
                   r"static_cast<uint32_t>\((.+?)\)\)\) \{", code)
     counter, ring, prod = m.groups()
-    cons = re.search(r"mbar_wait\(&full\[s\], static_cast<uint32_t>\((.+?)\)\)", code).group(1)
+    cons = re.search(r"mbar_wait\(&full\[s\], static_cast<uint32_t>\((.+?)\)(?:, \w+)?\)", code).group(1)
     dm = re.search(r"for \(int j = max\(0, (\w+) - (\w+)\); j < \1; \+\+j\) "
-                   r"mbar_wait\(&full\[lane \* \2 \+ j % \2\], static_cast<uint32_t>\((.+?)\)\)", code)
+                   r"mbar_wait\(&full\[lane \* \2 \+ j % \2\], static_cast<uint32_t>\((.+?)\)(?:, \w+)?\)", code)
     assert dm and dm.group(1) == counter and dm.group(2) == ring
     drain = dm.group(3)
     st = re.search(r"const int s = lane \* %s \+ %s %% %s;" % (ring, counter, ring), code)
@@ -154,6 +154,77 @@ def test_drain_after_an_abort_ends(kernel, R):
         reads, drain_ok = run(p, R, 40, seed, abort_at=seed % 37)
         assert [c for _, c in reads] == list(range(len(reads)))
         assert drain_ok, (kernel, R, seed)
+
+
+def release_is_guarded(kernel):
+    """Whether the consumer arrives on `empty` only for a stage whose wait
+    succeeded (`if (lane == 0 && <flag>) mbar_arrive(&empty[s]);`)."""
+    code = _code(open(os.path.join(ROOT, "kv_cache_page_build_b300", "csrc", SOURCES[kernel])).read())
+    m = re.search(r"if \(lane == 0( && \w+)?\) mbar_arrive\(&empty\[s\]\);", code)
+    assert m, "consumer release"
+    return m.group(1) is not None
+
+
+def run_abort(proto, R, n_chunks, seed, abort_at, guarded):
+    """The abort as the kernels run it: after abort_at reads the consumer
+    stops waiting but goes on over its remaining chunks, releasing a stage
+    only when `guarded` is false; the producer notices the abort a random
+    number of steps later.  Returns (a copy was issued into a stage whose
+    previous copy was still in flight, the drain's waits all pass)."""
+    rng = random.Random(seed)
+    full = [Barrier() for _ in range(R)]
+    empty = [Barrier() for _ in range(R)]
+    in_flight = []
+    t, issued, consumed, aborted, notice, overlap = 0, 0, 0, False, rng.randint(0, 8), False
+    while True:
+        t += 1
+        for item in sorted(in_flight):
+            if item[0] <= t:
+                in_flight.remove(item)
+                full[item[1]].complete()
+        producing = issued < n_chunks and (not aborted or notice > 0)
+        if rng.random() < 0.5 and producing:
+            if aborted:
+                notice -= 1
+            i = issued
+            s = proto.stage(i, R)
+            if i < R or empty[s].passes(proto.producer(i, R)):
+                overlap |= any(x[1] == s for x in in_flight)
+                in_flight.append((t + rng.randint(1, 12), s, i))
+                issued += 1
+        elif not aborted:
+            if consumed == abort_at:
+                aborted = True
+            elif consumed < issued and full[proto.stage(consumed, R)].passes(proto.consumer(consumed, R)):
+                empty[proto.stage(consumed, R)].complete()
+                consumed += 1
+        elif consumed < n_chunks:                           # skipped without a wait
+            if not guarded:
+                empty[proto.stage(consumed, R)].complete()
+            consumed += 1
+        if aborted and consumed == n_chunks and not producing:
+            break
+        if t > 20000:
+            raise RuntimeError("no progress")
+    for _, s, _ in sorted(in_flight):
+        full[s].complete()
+    drain_ok = all(full[proto.stage(j, R)].passes(proto.drain(j, R)) for j in range(max(0, issued - R), issued))
+    return overlap, drain_ok
+
+
+@pytest.mark.parametrize("kernel", sorted(SOURCES))
+@pytest.mark.parametrize("R", [2, 3])
+def test_abort_never_refills_a_stage_with_a_copy_in_flight(kernel, R):
+    """The kernels release a stage only after its copy landed, so after an
+    abort no second copy enters a stage whose copy is still in flight, and
+    the drain covers every copy; releasing skipped stages (the planted
+    mistake) lets the producer refill them."""
+    p = protocol_of(kernel)
+    assert release_is_guarded(kernel)
+    for seed in range(300):
+        overlap, drain_ok = run_abort(p, R, 40, seed, abort_at=seed % 23, guarded=True)
+        assert not overlap and drain_ok, (kernel, R, seed)
+    assert any(run_abort(p, R, 40, seed, abort_at=seed % 23, guarded=False)[0] for seed in range(300))
 
 
 def _broken(p, **repl):
