@@ -95,8 +95,10 @@ int ensure_smem(const void *kern, size_t bytes, int *max_set) {
 // between L1 and shared memory follows the preferences of the kernels
 // resident on it, and the attention's ring needs most of an SM's shared
 // memory: the kernels that run before or beside it (top-k, the speculative
-// decision, recall, append, the stand-in) take this preference so that an SM
-// holding one of their CTAs can still take an attention CTA at once.
+// decision, recall, append) take this preference so that an SM
+// holding one of their CTAs can still take an attention CTA at once.  (Not
+// the stand-in projection read: a streaming kernel of plain loads, which
+// measured slower with the smaller L1.)
 std::mutex g_carve_mu;
 struct Carved {
   int dev;
@@ -1078,7 +1080,6 @@ static int launch_stand_in(const kvr_stand_in *c, uint64_t offset, uint64_t byte
   const uint64_t cap = static_cast<uint64_t>(sms) * kStandInCPS;
   const unsigned grid = static_cast<unsigned>(std::max<uint64_t>(1, std::min(want, cap)));
   const uint8_t *base = static_cast<const uint8_t *>(c->weights) + offset;
-  if (int rc = prefer_max_shared(reinterpret_cast<const void *>(k_stand_in))) return rc;
   k_stand_in<<<grid, kStandInThreads, 0, st>>>(reinterpret_cast<const uint4 *>(base), n16, c->sink);
   return check_launch("k_stand_in");
 }
