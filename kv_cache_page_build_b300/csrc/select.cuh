@@ -467,14 +467,6 @@ __global__ void __launch_bounds__(NT, 1)
     }
   }
   for (int i = tid; i < 2 * kSelBins; i += NT) (&s_hist[0][0])[i] = 0u;
-  // page-table entries of this thread's pages, for the physical ids of the
-  // selected ones (the page table is an input no kernel of the step writes)
-  const bool want_phys = spec.enabled ? (spec.sel_used_phys && !spec.page2slot && (spec.decided || corrected))
-                                      : sel_phys_out != nullptr;
-  int phys[KPT];
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) phys[j] = want_phys && base + 32 * j < Nv ? __ldg(ptab + base + 32 * j) : -1;
-
   pdl_wait();  // the scores of k_page_scores are complete and visible
   if (spec.enabled && spec.decided) corrected = spec.corrected[unit] != 0;  // k_spec_decide's decision
 
@@ -502,6 +494,14 @@ __global__ void __launch_bounds__(NT, 1)
     s_w1[warp] = kmn;
     s_w2[warp] = kmx;
   }
+  // page-table entries of this thread's pages, for the physical ids of the
+  // selected ones, in flight during the histogram rounds (issued after the
+  // scores, which are on the critical path)
+  const bool want_phys = spec.enabled ? (spec.sel_used_phys && !spec.page2slot && (spec.decided || corrected))
+                                      : sel_phys_out != nullptr;
+  int phys[KPT];
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) phys[j] = want_phys && base + 32 * j < Nv ? __ldg(ptab + base + 32 * j) : -1;
   __syncthreads();
   uint32_t L = 0xffffffffu, R = 0u;
 #pragma unroll
