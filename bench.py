@@ -103,6 +103,67 @@ def aggregate(units_per_rank: int, seconds_per_rank: float, world: int):
     return units_per_rank * world / t, t
 
 
+def e2e_rates(torch, stream, world, calls, warm, enqueue, out_shape):
+    """End to end through a public call with host buffers, two ways, each
+    after `warm` untimed steps: (pipelined, synchronised) steps/s.
+
+    enqueue(i, out_host) enqueues step i, which takes its q from pinned host
+    memory and leaves its fp32 output in the pinned buffer out_host.
+    Synchronised: the host waits for each step before the next.  Pipelined:
+    the host enqueues step i, then waits for step i - 1 (an event) and reads
+    a value of its output, so one step is in flight while the host prepares
+    the next (two pinned output buffers alternate)."""
+    outs = [torch.empty(out_shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    views = [o.numpy() for o in outs]
+    evs = [torch.cuda.Event() for _ in range(2)]
+
+    def sync_step(i):
+        enqueue(i, outs[0])
+        stream.synchronize()
+        return float(views[0].flat[0])
+
+    def piped(n):
+        acc = 0.0
+        for i in range(n):
+            enqueue(i, outs[i & 1])
+            evs[i & 1].record(stream)
+            if i > 0:
+                evs[(i - 1) & 1].synchronize()
+                acc += float(views[(i - 1) & 1].flat[0])
+        evs[(n - 1) & 1].synchronize()
+        return acc + float(views[(n - 1) & 1].flat[0])
+
+    rates = []
+    for mode in ("pipelined", "sync"):
+        if mode == "sync":
+            for i in range(warm):
+                sync_step(i)
+        else:
+            piped(warm)
+        barrier(world)
+        torch.cuda.synchronize()
+        w0 = time.perf_counter()
+        if mode == "sync":
+            for i in range(calls):
+                sync_step(i)
+        else:
+            piped(calls)
+        rates.append(aggregate(calls, time.perf_counter() - w0, world)[0])
+    return rates[0], rates[1]
+
+
+def copy_enqueue(q_host, q_dev, step, out):
+    """enqueue() for a step without a host-buffer form: q copied in from
+    pinned memory and the output copied back by the copy engines."""
+    n_q = q_host.shape[0]
+
+    def enqueue(i, out_host):
+        q_dev.copy_(q_host[i % n_q], non_blocking=True)
+        step(i, q_dev)
+        out_host.copy_(out, non_blocking=True)
+    return enqueue
+
+
 # ---------------------------------------------------------------- clocks
 
 
@@ -456,28 +517,21 @@ def measure_hbm(wl_name, args, world, local, steps, warmup, e2e_calls, kernel_la
         multi[f"T={T}" + (" bf16" if dt == kvr.KVR_DTYPE_BF16 else "")] = t_m
     status |= kvr.kvr_get_status()
 
-    # end to end through the public entry point with host buffers: q copied
-    # in from pinned memory and the output copied back every step, the
-    # stream synchronised per step; untimed warm-up calls on the same buffers
-    out_host = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
-    q_dev = torch.empty((B, Hq, D), dtype=torch.int16, device=dev)
-    stream = torch.cuda.current_stream()
+    # end to end through the public entry point with host buffers: every
+    # step takes its q from pinned host memory and leaves its output there
+    if args.step == "overlap":  # no host-buffer form: copy-engine transfers
+        q_dev = torch.empty((B, Hq, D), dtype=torch.int16, device=dev)
+        enqueue = copy_enqueue(q_host[:TRACE_LEN], q_dev, step, out)
+    else:
+        w_host = torch.zeros(kvr.kvr_workspace_size(d, k, kvr.KVR_OP_STEP_HOST), dtype=torch.uint8, device=dev)
 
-    def e2e_step(i):
-        q_dev.copy_(q_host[i % TRACE_LEN], non_blocking=True)
-        step(i, q_dev)
-        out_host.copy_(out, non_blocking=True)
-        stream.synchronize()
-
-    for i in range(200):
-        e2e_step(i)
-    barrier(world)
-    torch.cuda.synchronize()
-    w0 = time.perf_counter()
-    for i in range(e2e_calls):
-        e2e_step(i)
-    e2e_s = time.perf_counter() - w0
-    e2e_value, _ = aggregate(e2e_calls, e2e_s, world)
+        def enqueue(i, out_host):
+            c = i % COPIES
+            kvr.kvr_speculative_step_host(d, st, q_host[i % TRACE_LEN], summs[c], page_table, k_pools[c],
+                                          v_pools[c], k, wl_trace.tau, 0.0, out_host, corrected, None, sel_used,
+                                          sel_used_phys, w_host, w_host.numel())
+    e2e_value, e2e_sync = e2e_rates(torch, torch.cuda.current_stream(), world, e2e_calls, 200, enqueue,
+                                    (B, Hq, D))
     status |= kvr.kvr_get_status()
 
     # decode-time append (kvr_append_kv), timed last: a graph of LK appends
@@ -504,7 +558,7 @@ def measure_hbm(wl_name, args, world, local, steps, warmup, e2e_calls, kernel_la
     res = dict(wl=wl, tau=wl_trace.tau, copies=COPIES, steps=steps, L=L, value=value, t_max=t_max,
                attn_avg=attn_avg, n_attn=n_attn, sel_avg=sel_avg, n_sel=n_sel, app_avg=app_avg, summ_s=summ_s,
                multi=multi,
-               e2e_value=e2e_value, e2e_calls=e2e_calls, clk=clk, status=status,
+               e2e_value=e2e_value, e2e_sync=e2e_sync, e2e_calls=e2e_calls, clk=clk, status=status,
                attn_bytes=B * H * k * P * 2 * D * 2,          # selected K and V rows read per launch
                summ_bytes=B * H * N * 2 * D * 2,               # summaries read by the selection
                k_bytes=B * N * P * H * D * 2)
@@ -711,28 +765,15 @@ def measure_recall(args, world, local, reps, warmup, e2e_calls, clocks=True):
     status = kvr.kvr_get_status()
 
     # end to end through the public call: q in from pinned memory, output
-    # back, per step; untimed warm-up calls on the same buffers first
-    out_host = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
+    # back, every step
     q_dev = torch.empty((B, Hq, D), dtype=torch.int16, device=dev)
-
-    def e2e_step(i):
-        q_dev.copy_(q_host[i % T], non_blocking=True)
-        step(i, q_dev)
-        out_host.copy_(out, non_blocking=True)
-        main_s.synchronize()
-
-    for i in range(16):
-        e2e_step(i)
-    barrier(world)
-    torch.cuda.synchronize()
-    w0 = time.perf_counter()
-    for i in range(e2e_calls):
-        e2e_step(i)
-    e2e_value, _ = aggregate(e2e_calls, time.perf_counter() - w0, world)
+    e2e_value, e2e_sync = e2e_rates(torch, main_s, world, e2e_calls, 16, copy_enqueue(q_host[:T], q_dev, step, out),
+                                    (B, Hq, D))
     status |= kvr.kvr_get_status()
     res = dict(wl=wl, tau=wl_trace.tau, S=S, T=T, steps=n_steps, value=value, t_max=t_max,
                pages_per_step=pages_per_step, page_bytes=page_bytes, recall_s=recall_s,
-               recall_bytes=recall_bytes, link_gbs=link_gbs, e2e_value=e2e_value, e2e_calls=e2e_calls,
+               recall_bytes=recall_bytes, link_gbs=link_gbs, e2e_value=e2e_value, e2e_sync=e2e_sync,
+               e2e_calls=e2e_calls,
                clk=clk, status=status)
     del k_slots, v_slots, k_host, v_host, host_pools
     torch.cuda.empty_cache()
@@ -798,10 +839,16 @@ def hbm_line(name, r, args, world):
         "gpu_launches": (5 if args.step == "overlap" else 3) * r["steps"],
         "e2e": {"value": round(r["e2e_value"], 2), "unit": "steps/s",
                 "h2d_bytes_per_step": B * Hq * D * 2, "d2h_bytes_per_step": B * Hq * D * 4,
-                "how": f"{r['e2e_calls']} eager kvr_speculative_step"
-                       f"{'_overlap' if args.step == 'overlap' else ''} calls after 200 untimed ones, q copied in "
-                       f"from pinned host memory and the fp32 output copied back every step, stream synchronised "
-                       f"per step"},
+                "synchronised_per_step": round(r["e2e_sync"], 2),
+                "how": (f"{r['e2e_calls']} eager kvr_speculative_step_overlap calls after 200 untimed ones, q "
+                        f"copied in from pinned host memory and the fp32 output copied back by the copy engines "
+                        f"every step"
+                        if args.step == "overlap" else
+                        f"{r['e2e_calls']} eager kvr_speculative_step_host calls after 200 untimed ones: every "
+                        f"step reads its q from pinned host memory (staged by its first kernel) and the "
+                        f"attention writes the fp32 output into pinned host memory")
+                       + "; pipelined: the host enqueues step i, then waits for step i-1 and reads its output "
+                         "(one step in flight); synchronised_per_step: the host waits for each step"},
         "clocks": r["clk"],
         "device_status": r["status"],
     }
@@ -839,9 +886,11 @@ def recall_line(r, args, world):
         "gpu_launches": 5 * r["steps"],  # k_page_scores, k_topk, k_recall, k_sparse_decode x2
         "e2e": {"value": round(r["e2e_value"], 2), "unit": "steps/s",
                 "h2d_bytes_per_step": B * Hq * D * 2, "d2h_bytes_per_step": B * Hq * D * 4,
+                "synchronised_per_step": round(r["e2e_sync"], 2),
                 "how": f"{r['e2e_calls']} eager kvr_speculative_step_recall calls after 16 untimed ones, q "
-                       f"copied in from pinned host memory and the fp32 output copied back every step, stream "
-                       f"synchronised per step"},
+                       f"copied in from pinned host memory and the fp32 output copied back every step; "
+                       f"pipelined: one step in flight while the host reads the previous step's output; "
+                       f"synchronised_per_step: the host waits for each step"},
         "clocks": r["clk"],
         "device_status": r["status"],
     }

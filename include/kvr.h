@@ -79,6 +79,7 @@ extern "C" {
 #define KVR_OP_SELECT 1 /* kvr_select_pages, kvr_speculative_select */
 #define KVR_OP_ATTN 2   /* kvr_sparse_decode_attn */
 #define KVR_OP_STEP 3   /* kvr_speculative_step(_overlap), kvr_speculative_step_recall */
+#define KVR_OP_STEP_HOST 4 /* kvr_speculative_step_host */
 
 typedef struct kvr_dims {
   int32_t batch;        /* B */
@@ -268,6 +269,31 @@ int kvr_speculative_step(const kvr_dims *dims, kvr_spec_state *st,
                          float *cbar_opt, int32_t *sel_used,
                          int32_t *sel_used_phys, void *ws, size_t ws_bytes,
                          void *stream);
+
+/* kvr_speculative_step with the query and the output in host memory
+ * ([FreeKV] section 2.2: the step's data movement stays off the critical
+ * path).  q_host [B][Hq][D] bf16 and out_host [B][Hq][D] fp32 are
+ * page-locked, mapped host memory (cudaHostAlloc, or cudaHostRegister with
+ * mapping), 16-byte aligned; anything else returns KVR_ERR_INVALID_ARG
+ * before any launch.  The call's first kernel copies q_host into the
+ * workspace through the host mapping, and the attention stores the output
+ * straight into out_host: no copy-engine transfer, so the step has no
+ * hand-off between a copy and a kernel.  The first kernel may read q_host
+ * before the kernel that precedes the call on `stream` has finished, so
+ * q_host must hold the query when the call is made (written by the host, or
+ * by device work already complete); the caller must not change q_host until
+ * the call's work on `stream` has run, nor read out_host before then (an
+ * event recorded after the call).  Results are bit-identical to
+ * kvr_speculative_step on device copies of q and out.  Workspace kind
+ * KVR_OP_STEP_HOST.  Increments st->step on success. */
+int kvr_speculative_step_host(const kvr_dims *dims, kvr_spec_state *st,
+                              const uint16_t *q_host, const uint16_t *summ,
+                              const int32_t *page_table, const uint16_t *k_pool,
+                              const uint16_t *v_pool, int32_t top_k, float tau,
+                              float scale, float *out_host, uint8_t *corrected,
+                              float *cbar_opt, int32_t *sel_used,
+                              int32_t *sel_used_phys, void *ws, size_t ws_bytes,
+                              void *stream);
 
 /* The same speculative decode step with the selection taken off the
  * attention's critical path ([FreeKV] section 2.1: speculative retrieval

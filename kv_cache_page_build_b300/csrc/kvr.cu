@@ -18,6 +18,7 @@
 
 #include "attention.cuh"
 #include "common.cuh"
+#include "io.cuh"
 #include "pipeline.cuh"
 #include "recall.cuh"
 #include "select.cuh"
@@ -151,6 +152,11 @@ size_t attn_ws_bytes(const kvr_dims *d, int top_k) {
   (void)top_k;
   const size_t units = static_cast<size_t>(d->batch) * d->n_kv_heads;
   return align_up(units * sizeof(uint32_t));
+}
+
+// The query staged in device memory by the host-buffer step.
+size_t stage_ws_bytes(const kvr_dims *d) {
+  return align_up(static_cast<size_t>(d->batch) * d->n_q_heads * d->head_dim * sizeof(uint16_t));
 }
 
 SelectWs carve_select(const kvr_dims *d, uint8_t *p) {
@@ -552,13 +558,14 @@ int launch_attn(const kvr_dims *d, const uint16_t *q, const uint16_t *k_pool,
   }
 }
 
-// Device address of page-locked host memory (the kernels read it directly).
-int mapped_host_pointer(const void *host, void **dev) {
+// Device address of page-locked host memory (the kernels read or write it
+// directly); `what` names the buffer in the error text.
+int mapped_host_pointer(const void *host, void **dev, const char *what = "host cache") {
   cudaPointerAttributes a;
   const cudaError_t e = cudaPointerGetAttributes(&a, host);
-  if (e != cudaSuccess) return cuda_fail(e, "host cache pointer attributes");
+  if (e != cudaSuccess) return cuda_fail(e, what);
   if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) {
-    std::snprintf(g_err_text, sizeof g_err_text, "host cache is not page-locked, mapped host memory");
+    std::snprintf(g_err_text, sizeof g_err_text, "%s is not page-locked, mapped host memory", what);
     return KVR_ERR_INVALID_ARG;
   }
   *dev = a.devicePointer;
@@ -645,6 +652,8 @@ size_t kvr_workspace_size(const kvr_dims *dims, int32_t top_k, int32_t op) {
     case KVR_OP_SELECT: return select_ws_bytes(dims);
     case KVR_OP_ATTN: return attn_ws_bytes(dims, top_k);
     case KVR_OP_STEP: return select_ws_bytes(dims) + attn_ws_bytes(dims, top_k);
+    case KVR_OP_STEP_HOST:
+      return select_ws_bytes(dims) + attn_ws_bytes(dims, top_k) + stage_ws_bytes(dims);
     default: return 0;
   }
 }
@@ -930,6 +939,52 @@ int kvr_speculative_step(const kvr_dims *dims, kvr_spec_state *st, const uint16_
   return launch_attn(dims, q_t, k_pool, v_pool, dims->n_phys_pages, sel_used_phys, top_k, scale,
                      nullptr, 0, carve_attn(dims, top_k, (uint8_t *)ws + select_ws_bytes(dims)),
                      out, s);
+}
+
+int kvr_speculative_step_host(const kvr_dims *dims, kvr_spec_state *st, const uint16_t *q_host,
+                              const uint16_t *summ, const int32_t *page_table, const uint16_t *k_pool,
+                              const uint16_t *v_pool, int32_t top_k, float tau, float scale,
+                              float *out_host, uint8_t *corrected, float *cbar_opt, int32_t *sel_used,
+                              int32_t *sel_used_phys, void *ws, size_t ws_bytes, void *stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_topk(dims, top_k))) return rc;
+  if (!q_host || !out_host) return KVR_ERR_INVALID_ARG;
+  const size_t sel_b = select_ws_bytes(dims), attn_b = attn_ws_bytes(dims, top_k);
+  if ((rc = check_ws(ws, ws_bytes, sel_b + attn_b + stage_ws_bytes(dims)))) return rc;
+  uint16_t *q_stage = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + sel_b + attn_b);
+  if ((rc = check_spec(dims, st, q_stage, summ, corrected, cbar_opt, sel_used, tau))) return rc;
+  if (!page_table || !k_pool || !v_pool || !sel_used_phys) return KVR_ERR_INVALID_ARG;
+  if (!aligned16(page_table) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(sel_used_phys))
+    return KVR_ERR_ALIGN;
+  if (std::isnan(scale)) return KVR_ERR_INVALID_ARG;
+  void *q_dev = nullptr, *out_dev = nullptr;
+  if ((rc = mapped_host_pointer(q_host, &q_dev, "q_host"))) return rc;
+  if ((rc = mapped_host_pointer(out_host, &out_dev, "out_host"))) return rc;
+  if (!aligned16(q_dev) || !aligned16(out_dev)) return KVR_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint64_t n16 = static_cast<uint64_t>(dims->batch) * dims->n_q_heads * dims->head_dim * 2 / 16;
+  int sms = 0;
+  if ((rc = sm_count(&sms))) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(
+      std::max<uint64_t>(1, std::min<uint64_t>((n16 + kStageThreads - 1) / kStageThreads, 4ull * sms))));
+  cfg.blockDim = dim3(kStageThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_stage_in, static_cast<const uint4 *>(q_dev),
+                                           reinterpret_cast<uint4 *>(q_stage), n16);
+  if (e != cudaSuccess) return cuda_fail(e, "k_stage_in");
+  rc = spec_select_impl(dims, st, q_stage, summ, page_table, top_k, tau, corrected, cbar_opt, sel_used,
+                        sel_used_phys, nullptr, 0, ws, s);
+  if (rc) return rc;
+  st->step += 1;
+  return launch_attn(dims, q_stage, k_pool, v_pool, dims->n_phys_pages, sel_used_phys, top_k, scale,
+                     nullptr, 0, carve_attn(dims, top_k, static_cast<uint8_t *>(ws) + sel_b), out_dev, s);
 }
 
 int kvr_speculative_step_overlap(const kvr_dims *dims, kvr_spec_state *st, const uint16_t *q_t,

@@ -85,6 +85,8 @@ _SIGS = {
                                     _P, _P, _P, _P, _P, _S, _P]),
     "kvr_speculative_step": (_I, [_D, ctypes.POINTER(kvr_spec_state), _P, _P, _P, _P, _P, _I, _F,
                                   _F, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "kvr_speculative_step_host": (_I, [_D, ctypes.POINTER(kvr_spec_state), _P, _P, _P, _P, _P, _I, _F,
+                                       _F, _P, _P, _P, _P, _P, _P, _S, _P]),
     "kvr_speculative_step_overlap": (_I, [_D, ctypes.POINTER(kvr_spec_state), _P, _P, _P, _P, _P, _I,
                                           _F, _F, _P, _P, _P, _P, _P, _P, _S, _P, _P, _P, _P]),
     "kvr_append_kv": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -198,6 +200,16 @@ def kvr_speculative_step(d, st, q_t, summ, page_table, k_pool, v_pool, top_k, ta
                                             _ptr(out), _ptr(corrected), _ptr(cbar_opt), _ptr(sel_used),
                                             _ptr(sel_used_phys), _ptr(ws), int(ws_bytes), _stream(stream)),
                   "kvr_speculative_step")
+
+
+def kvr_speculative_step_host(d, st, q_host, summ, page_table, k_pool, v_pool, top_k, tau, scale, out_host,
+                              corrected, cbar_opt, sel_used, sel_used_phys, ws, ws_bytes, stream=None):
+    return _check(_lib.kvr_speculative_step_host(_d(d), ctypes.byref(st), _ptr(q_host), _ptr(summ),
+                                                 _ptr(page_table), _ptr(k_pool), _ptr(v_pool), int(top_k),
+                                                 float(tau), float(scale), _ptr(out_host), _ptr(corrected),
+                                                 _ptr(cbar_opt), _ptr(sel_used), _ptr(sel_used_phys), _ptr(ws),
+                                                 int(ws_bytes), _stream(stream)),
+                  "kvr_speculative_step_host")
 
 
 def kvr_working_set_reset(d, wset, stream=None):

@@ -254,6 +254,31 @@ def test_pipeline_binding_checks_the_marks_length():
     assert st.step == 0
 
 
+def test_host_buffer_step_arguments_rejected_before_launch():
+    """kvr_speculative_step_host: its workspace holds the step's and the
+    staged query's (B Hq D bf16, rounded up to 256 bytes); missing host
+    buffers, state or workspace are refused before any CUDA call."""
+    lib = kvr.raw()
+    d = D()
+    step_b = kvr.kvr_workspace_size(d, 64, kvr.KVR_OP_STEP)
+    need = kvr.kvr_workspace_size(d, 64, kvr.KVR_OP_STEP_HOST)
+    q_b = d.batch * d.n_q_heads * d.head_dim * 2
+    assert need == step_b + (q_b + 255) // 256 * 256
+    q_prev, sel_prev = FAKE, FAKE
+    st = kvr.kvr_spec_state(q_prev, sel_prev, 0)
+
+    def call(q=FAKE, out=FAKE, ws=FAKE, ws_bytes=need, state=st):
+        return lib.kvr_speculative_step_host(ctypes.byref(d), ctypes.byref(state) if state else None, q, FAKE,
+                                             FAKE, FAKE, FAKE, 64, 0.8, 0.0, out, FAKE, None, FAKE, FAKE, ws,
+                                             ws_bytes, None)
+    assert call(q=None) == kvr.KVR_ERR_INVALID_ARG
+    assert call(out=None) == kvr.KVR_ERR_INVALID_ARG
+    assert call(ws_bytes=need - 1) == kvr.KVR_ERR_WORKSPACE
+    assert call(ws=None) == kvr.KVR_ERR_WORKSPACE
+    assert call(state=None) == kvr.KVR_ERR_INVALID_ARG
+    assert st.step == 0
+
+
 def test_several_queries_arguments_rejected_before_launch():
     """kvr_select_pages_multi and kvr_sparse_decode_attn_multi: the query
     rows per unit (G T) must be 1, 2, 4, 8 or 16; the lengths are required,

@@ -194,6 +194,74 @@ def test_overlapped_step_replays_from_a_cuda_graph():
     np.testing.assert_array_equal(eager.sel_used.cpu().numpy(), ref["sel_used"][15])
 
 
+def test_host_buffer_step_is_bit_identical_to_the_device_step():
+    """kvr_speculative_step_host over the 64-step trace, each query read from
+    a row of one page-locked host array (an interior pointer) and the output
+    written into alternating page-locked host buffers, with no
+    synchronisation between steps: the same bits as kvr_speculative_step on
+    device copies, and the oracle's decisions and selections."""
+    wl, case, dc, tr, ref = accepted_trace(4)
+    qs = gh.t16(tr.q)
+    q_host = torch.from_numpy(np.ascontiguousarray(tr.q).view(np.int16)).pin_memory()
+    B, Hq, D = wl.batch, wl.n_q_heads, wl.head_dim
+    outs = [torch.full((B, Hq, D), float("nan"), dtype=torch.float32).pin_memory() for _ in range(2)]
+    host, dev = SpecRun(wl, dc), SpecRun(wl, dc)
+    host.ws = gh.workspace(dc.dims, wl.top_k, kvr.KVR_OP_STEP_HOST)
+    assert host.ws.numel() > kvr.kvr_workspace_size(dc.dims, wl.top_k, kvr.KVR_OP_STEP)
+    outs_dev = torch.empty((wl.steps, B, Hq, D), dtype=torch.float32, device="cuda")
+    used_host = torch.empty((wl.steps, B, wl.n_kv_heads, wl.top_k), dtype=torch.int32, device="cuda")
+    evs = [torch.cuda.Event() for _ in range(2)]
+    got = []
+    for t in range(wl.steps):
+        kvr.kvr_speculative_step_host(dc.dims, host.st, q_host[t], dc.summaries(), dc.page_table, dc.k_pool,
+                                      dc.v_pool, wl.top_k, wl.tau, 0.0, outs[t & 1], host.corrected, host.cbar,
+                                      host.sel_used, host.sel_used_phys, host.ws, host.ws.numel())
+        used_host[t].copy_(host.sel_used)
+        evs[t & 1].record()
+        dev.step(qs[t])
+        outs_dev[t].copy_(dev.out)
+        if t > 0:  # the previous step's output, once its event has passed
+            evs[(t - 1) & 1].synchronize()
+            got.append(outs[(t - 1) & 1].clone())
+            outs[(t - 1) & 1].fill_(float("nan"))
+    torch.cuda.synchronize()
+    got.append(outs[(wl.steps - 1) & 1].clone())
+    assert host.st.step == wl.steps
+    for t in range(wl.steps):
+        assert torch.equal(got[t], outs_dev[t].cpu()), f"step {t}"
+        np.testing.assert_array_equal(used_host[t].cpu().numpy(), ref["sel_used"][t], err_msg=f"step {t}")
+    for a, b in ((host.q_prev, dev.q_prev), (host.sel_prev, dev.sel_prev), (host.corrected, dev.corrected),
+                 (host.sel_used_phys, dev.sel_used_phys)):
+        assert torch.equal(a, b)
+
+
+def test_host_buffer_step_rejects_memory_that_is_not_page_locked():
+    """Pageable host memory and device memory for q_host or out_host are
+    refused before any launch: the state does not advance."""
+    wl, case, dc, tr, ref = accepted_trace(4)
+    B, Hq, D = wl.batch, wl.n_q_heads, wl.head_dim
+    run = SpecRun(wl, dc)
+    ws = gh.workspace(dc.dims, wl.top_k, kvr.KVR_OP_STEP_HOST)
+    q_ok = torch.from_numpy(np.ascontiguousarray(tr.q[0]).view(np.int16)).pin_memory()
+    out_ok = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
+    q_pageable = torch.from_numpy(np.ascontiguousarray(tr.q[0]).view(np.int16).copy())
+    out_pageable = torch.empty((B, Hq, D), dtype=torch.float32)
+    q_device = gh.t16(tr.q[0])
+    for q, out in ((q_pageable, out_ok), (q_ok, out_pageable), (q_device, out_ok), (q_ok, run.out)):
+        with pytest.raises(kvr.KvrError) as e:
+            kvr.kvr_speculative_step_host(dc.dims, run.st, q, dc.summaries(), dc.page_table, dc.k_pool, dc.v_pool,
+                                          wl.top_k, wl.tau, 0.0, out, run.corrected, run.cbar, run.sel_used,
+                                          run.sel_used_phys, ws, ws.numel())
+        assert e.value.code == kvr.KVR_ERR_INVALID_ARG
+        assert run.st.step == 0
+    kvr.kvr_speculative_step_host(dc.dims, run.st, q_ok, dc.summaries(), dc.page_table, dc.k_pool, dc.v_pool,
+                                  wl.top_k, wl.tau, 0.0, out_ok, run.corrected, run.cbar, run.sel_used,
+                                  run.sel_used_phys, ws, ws.numel())
+    torch.cuda.synchronize()
+    assert run.st.step == 1
+    assert np.isfinite(out_ok.numpy()).all()
+
+
 # ---------------------------------------------------------------- host-resident cache
 
 def test_recall_trace_matches_oracle_and_hbm_path():
