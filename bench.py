@@ -899,7 +899,7 @@ def recall_line(r, args, world):
 def run_gpu(args, world, rank, local):
     """The line of --workload, plus (unless --no-extras) compact records of
     the other HBM-resident workload and of the host-resident one."""
-    e2e_calls = 2000
+    e2e_calls = max(1, args.e2e_calls)
     if args.workload.endswith("-host"):
         r = measure_recall(args, world, local, reps=max(1, -(-args.steps // 32)), warmup=args.warmup,
                            e2e_calls=e2e_calls)
@@ -1184,6 +1184,8 @@ def main():
     ap.add_argument("--kernel-launches", type=int, default=1280,
                     help="launches timed for each per-kernel figure (selection, attention)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-calls", type=int, default=2000,
+                    help="timed eager calls of each e2e measurement (after 200 untimed ones)")
     ap.add_argument("--copies", type=int, default=4, help="rotating cache copies (L2-cold timing needs >= 3)")
     ap.add_argument("--step", default="sequential", choices=["sequential", "overlap", "pipeline"],
                     help="kvr_speculative_step, kvr_speculative_step_overlap (selection on a side stream), or "

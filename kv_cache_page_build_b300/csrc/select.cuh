@@ -393,6 +393,10 @@ __global__ void __launch_bounds__(NT, 1)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = blockIdx.x, b = blockIdx.y;
+  // The kernel after this one (the attention, or the next selection) may be
+  // scheduled now: its launch and setup overlap this one, and its own
+  // dependency wait still covers all of this kernel's writes.
+  if (tid == 0) pdl_launch_dependents();
   const int Hq = H * G;
   const size_t unit = static_cast<size_t>(b) * H + g;
   const int base = warp * KPT * 32 + lane;  // page of key j: base + 32 j
