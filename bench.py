@@ -228,17 +228,30 @@ def cpu_baseline(wl_name: str, seconds: float = 12.0):
     tr = synth.make_trace(synth.WORKLOADS[tid], case)
     summ = oracle.summaries(case.k_pool, case.page_table)
     wl = case.wl
-    n, t0 = 0, time.perf_counter()
-    while True:
-        oracle.decode_step(tr.q[n % tr.q.shape[0]], case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads,
-                           wl.top_k, summ=summ)
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": n / el, "unit": "steps/s", "cores": oracle.max_threads(), "kind": "oracle",
+    cores = oracle.max_threads()
+
+    def run(budget):
+        n, t0 = 0, time.perf_counter()
+        while True:
+            oracle.decode_step(tr.q[n % tr.q.shape[0]], case.k_pool, case.v_pool, case.page_table,
+                               wl.n_kv_heads, wl.top_k, summ=summ)
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= budget:
+                return n, el
+
+    n, el = run(seconds)
+    # the same oracle on one thread, for a third of the budget
+    oracle.set_threads(1)
+    try:
+        n1, el1 = run(seconds / 3)
+    finally:
+        oracle.set_threads(cores)
+    return {"value": n / el, "unit": "steps/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} full decode steps (batch {wl.batch}, selection + attention, fp64) of the same "
-                      f"workload in {el:.1f} s; summaries built beforehand"}
+                      f"workload in {el:.1f} s; summaries built beforehand",
+            "single_thread": {"value": round(n1 / el1, 3), "unit": "steps/s", "cores": 1,
+                              "sample": f"{n1} steps in {el1:.1f} s"}}
 
 
 # ---------------------------------------------------------------- GPU leg
