@@ -43,8 +43,14 @@
  *     wait that timed out) set bits of the status word instead.
  *   - A workspace (`ws`, `ws_bytes`) must be at least kvr_workspace_size()
  *     bytes.  Its contents need no initialisation: a call writes every
- *     scratch value before reading it (a reserved word per (b, g) is left
- *     as found).  Calls that share a workspace must not overlap on the GPU.
+ *     scratch value before reading it, except the speculative step's one
+ *     8-byte early-start word per (b, g) (kvr_speculative_step and
+ *     kvr_speculative_step_host; other calls leave it as found).  The step's
+ *     top-k sets a reused head's word to a 64-bit tag of the call (a fixed
+ *     32-bit pattern above a per-process call count), the attention reads it
+ *     and clears it: any other prior value is ignored, so only a stale word
+ *     that happened to hold that exact tag could mislead a call.  Calls that
+ *     share a workspace must not overlap on the GPU.
  */
 #ifndef KVR_H
 #define KVR_H
@@ -260,7 +266,12 @@ int kvr_speculative_select(const kvr_dims *dims, kvr_spec_state *st,
 
 /* One speculative decode step: kvr_speculative_select followed by
  * kvr_sparse_decode_attn over sel_used_phys (which must be non-NULL), both on
- * `stream`.  Workspace kind KVR_OP_STEP. */
+ * `stream`.  The attention of a head that reuses its previous selection
+ * starts as soon as the selection kernel has announced that head's page ids
+ * (taken before the new selection is computed), without waiting for the
+ * rest of the selection ([FreeKV] section 2.1: speculative retrieval takes
+ * the selection off the critical path); results are unchanged.  Workspace
+ * kind KVR_OP_STEP. */
 int kvr_speculative_step(const kvr_dims *dims, kvr_spec_state *st,
                          const uint16_t *q_t, const uint16_t *summ,
                          const int32_t *page_table, const uint16_t *k_pool,

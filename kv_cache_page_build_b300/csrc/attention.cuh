@@ -255,6 +255,13 @@ __device__ __forceinline__ void attn_chunk(uint32_t kb, const uint32_t (&qb)[Att
 // sel_phys) are given and query token tau sees the positions below
 // seq_len - T + tau + 1 (CAUSAL instances; T = 1 takes the others).  out is
 // fp32, or bf16 (rounded to nearest even) when out_bf16 != 0.
+// ready (may be null; speculative step, every unit active): a unit whose
+// word holds ready_tag when its CTA starts had its page ids written and
+// announced by the top-k kernel before that kernel finished (a reused
+// selection): the CTA starts at once and waits for the kernel it depends on
+// only before it leaves.  The ids are read at L2 (never through the
+// read-only path, as they may have been written during this kernel's
+// lifetime).  CTA 0 of the cluster clears the word at the end.
 template <int NR, int P, bool CAUSAL>
 __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
     k_sparse_decode(const __grid_constant__ CUtensorMap tmap_k,
@@ -263,7 +270,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
                     int H, int k, int n_phys, int Q, int T, int G, float scale_log2, uint64_t wait_ns,
                     const uint8_t *__restrict__ filter, int filter_mode, void *__restrict__ out,
                     int out_bf16, const int32_t *__restrict__ seq_len,
-                    const int32_t *__restrict__ page_table, int N) {
+                    const int32_t *__restrict__ page_table, int N,
+                    unsigned long long *__restrict__ ready, unsigned long long ready_tag) {
   using Cfg = AttnCfg<NR, P>;
   constexpr int NC = kAttnNC, CPP = Cfg::CPP, HALF = Cfg::kHalf, R = Cfg::R, S = Cfg::S, CB = Cfg::CB;
   constexpr int kIdRounds = kAttnIds / 32;
@@ -282,6 +290,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
   __shared__ __align__(16) float s_recv[NC * NR * kD];
   __shared__ __align__(8) float2 s_mlr[kAttnMaxQ * NC * NR];
   __shared__ volatile int s_abort;
+  __shared__ int s_early;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rank = cluster_ctarank();
@@ -314,16 +323,22 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
       mbar_init(&empty[s], 1);
     }
     s_abort = 0;
+    s_early = ready != nullptr && ld_acquire_gpu_u64(ready + u) == ready_tag;
     fence_barrier_init();
   }
   __syncthreads();
   // Launched as a programmatic dependent launch, the setup above overlaps
-  // the previous kernel; every global read and write comes after this wait.
-  pdl_wait();
+  // the previous kernel; every global read and write comes after this wait,
+  // except in an early unit (its inputs were announced; it waits at the end)
+  const bool early = s_early != 0;
+  if (!early) pdl_wait();
   if (tid == 0) pdl_launch_dependents();
   // the whole cluster holds one unit, so this exit is uniform over it (no
   // thread of the cluster touches another CTA's shared memory)
-  if (!attn_unit_active(filter, filter_mode, u)) return;
+  if (!attn_unit_active(filter, filter_mode, u)) {
+    if (early) pdl_wait();
+    return;
+  }
   // Start handshake of the cluster: no thread may write another CTA's shared
   // memory before that CTA has started; every thread arrives here and waits
   // (cluster_wait) before the first push of the merge.
@@ -342,7 +357,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
 #pragma unroll
         for (int r = 0; r < kIdRounds; ++r) {
           const int j = lane + 32 * r;
-          idv[w][r] = j < n ? __ldg(sel_u + (a + j) / CPP) : -1;
+          idv[w][r] = j < n ? __ldcg(sel_u + (a + j) / CPP) : -1;
         }
       }
 #pragma unroll
@@ -394,7 +409,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
         const int s = lane * R + i % R;
         if (i < R || mbar_test_wait(&empty[s], static_cast<uint32_t>((i / R - 1) & 1))) {
           const int pos = a + i;
-          const int id = i < kAttnIds ? s_ids[lane][i] : __ldg(sel_u + pos / CPP);
+          const int id = i < kAttnIds ? s_ids[lane][i] : __ldcg(sel_u + pos / CPP);
           int nv, pos0 = 0;
           if (causal) {  // tokens below the sequence's length, from the logical position
             const int lid = i < kAttnIds ? s_lids[lane][i] : __ldg(sel_lu + pos / CPP);
@@ -597,6 +612,11 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
         *reinterpret_cast<float4 *>(static_cast<float *>(out) + row * kD + c) = r;
     }
   }
+  if (early) pdl_wait();  // this grid completes after the kernel it depends on
+  // every CTA of the cluster read the word at its start (all passed the
+  // cluster barrier above); once the top-k has finished (the wait), nothing
+  // sets it again in this call
+  if (ready != nullptr && rank == 0 && tid == 0) ready[u] = 0ull;
 }
 
 }  // namespace kvr

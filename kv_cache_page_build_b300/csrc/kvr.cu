@@ -33,6 +33,15 @@ thread_local char g_err_text[512];
 // Bound of the kernels' waits for progress, passed to every streaming launch.
 std::atomic<uint64_t> g_wait_limit{kWaitNs};
 
+// Tag of one speculative step's early-start words: a per-process call count
+// in the low half and a fixed pattern in the high half, so that no zeroed
+// word and no earlier call's word carries it.  A CUDA graph keeps the tag of
+// its capture; each replay's attention clears the words it used.
+unsigned long long next_ready_tag() {
+  static std::atomic<uint32_t> calls{0};
+  return (0x9E3779B9ull << 32) | (calls.fetch_add(1, std::memory_order_relaxed) + 1u);
+}
+
 int cuda_fail(cudaError_t e, const char *where) {
   std::snprintf(g_err_text, sizeof g_err_text, "CUDA error in %s: %s", where,
                 cudaGetErrorString(e));
@@ -129,7 +138,9 @@ struct SelectWs {
   uint32_t *count;    // one word per unit, kept zero (reserved in the layout; unused)
 };
 struct AttnWs {
-  uint32_t *reserved;  // the attention keeps its split partials on chip
+  // [B][H] words of the speculative step's early start (the attention keeps
+  // its split partials on chip)
+  unsigned long long *ready;
 };
 
 // Per-sequence lengths for the attention (seq_len null: every page full),
@@ -141,6 +152,8 @@ struct AttnLen {
   int T = 1;
   const int32_t *sel_log = nullptr;
   int out_bf16 = 0;
+  unsigned long long *ready = nullptr;  // early start of reused units (speculative step)
+  unsigned long long ready_tag = 0;
 };
 
 size_t select_ws_bytes(const kvr_dims *d) {
@@ -151,7 +164,7 @@ size_t select_ws_bytes(const kvr_dims *d) {
 size_t attn_ws_bytes(const kvr_dims *d, int top_k) {
   (void)top_k;
   const size_t units = static_cast<size_t>(d->batch) * d->n_kv_heads;
-  return align_up(units * sizeof(uint32_t));
+  return align_up(units * sizeof(unsigned long long));
 }
 
 // The query staged in device memory by the host-buffer step.
@@ -171,7 +184,7 @@ AttnWs carve_attn(const kvr_dims *d, int top_k, uint8_t *p) {
   (void)d;
   (void)top_k;
   AttnWs w;
-  w.reserved = reinterpret_cast<uint32_t *>(p);
+  w.ready = reinterpret_cast<unsigned long long *>(p);
   return w;
 }
 
@@ -505,7 +518,8 @@ int launch_attn_gp(const kvr_dims *d, const CUtensorMap &tk, const CUtensorMap &
                                            k, n_phys, Q, len.T, d->n_q_heads / d->n_kv_heads,
                                            scale_log2, g_wait_limit.load(std::memory_order_relaxed),
                                            filter, filter_mode, out, len.out_bf16,
-                                           len.seq_len, len.page_table, d->n_pages);
+                                           len.seq_len, len.page_table, d->n_pages, len.ready,
+                                           len.ready_tag);
   if (e != cudaSuccess) return cuda_fail(e, "k_sparse_decode");
   return KVR_OK;
 }
@@ -879,9 +893,11 @@ static int spec_select_impl(const kvr_dims *dims, kvr_spec_state *st, const uint
                             const uint16_t *summ, const int32_t *page_table, int32_t top_k,
                             float tau, uint8_t *corrected, float *cbar_opt, int32_t *sel_used,
                             int32_t *sel_used_phys, const int32_t *page2slot, int n_slots,
-                            void *ws, cudaStream_t stream, bool pdl_first = true) {
-  const SpecArgs s =
-      spec_args(st, tau, corrected, cbar_opt, sel_used, sel_used_phys, page2slot, n_slots);
+                            void *ws, cudaStream_t stream, bool pdl_first = true,
+                            unsigned long long *ready = nullptr, unsigned long long ready_tag = 0) {
+  SpecArgs s = spec_args(st, tau, corrected, cbar_opt, sel_used, sel_used_phys, page2slot, n_slots);
+  s.ready = ready;
+  s.ready_tag = ready_tag;
   return launch_select(dims, q_t, summ, page_table, top_k, carve_select(dims, (uint8_t *)ws),
                        nullptr, nullptr, nullptr, s, stream, pdl_first);
 }
@@ -932,13 +948,18 @@ int kvr_speculative_step(const kvr_dims *dims, kvr_spec_state *st, const uint16_
   if (std::isnan(scale)) return KVR_ERR_INVALID_ARG;
   if ((rc = check_ws(ws, ws_bytes, select_ws_bytes(dims) + attn_ws_bytes(dims, top_k)))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the attention of a reused unit starts as soon as the top-k's prologue
+  // has announced its page ids
+  const AttnWs aw = carve_attn(dims, top_k, (uint8_t *)ws + select_ws_bytes(dims));
+  AttnLen early;
+  early.ready = aw.ready;
+  early.ready_tag = next_ready_tag();
   rc = spec_select_impl(dims, st, q_t, summ, page_table, top_k, tau, corrected, cbar_opt, sel_used,
-                        sel_used_phys, nullptr, 0, ws, s);
+                        sel_used_phys, nullptr, 0, ws, s, true, early.ready, early.ready_tag);
   if (rc) return rc;
   st->step += 1;
   return launch_attn(dims, q_t, k_pool, v_pool, dims->n_phys_pages, sel_used_phys, top_k, scale,
-                     nullptr, 0, carve_attn(dims, top_k, (uint8_t *)ws + select_ws_bytes(dims)),
-                     out, s);
+                     nullptr, 0, aw, out, s, true, early);
 }
 
 int kvr_speculative_step_host(const kvr_dims *dims, kvr_spec_state *st, const uint16_t *q_host,
@@ -979,12 +1000,16 @@ int kvr_speculative_step_host(const kvr_dims *dims, kvr_spec_state *st, const ui
   const cudaError_t e = cudaLaunchKernelEx(&cfg, k_stage_in, static_cast<const uint4 *>(q_dev),
                                            reinterpret_cast<uint4 *>(q_stage), n16);
   if (e != cudaSuccess) return cuda_fail(e, "k_stage_in");
+  const AttnWs aw = carve_attn(dims, top_k, static_cast<uint8_t *>(ws) + sel_b);
+  AttnLen early;
+  early.ready = aw.ready;
+  early.ready_tag = next_ready_tag();
   rc = spec_select_impl(dims, st, q_stage, summ, page_table, top_k, tau, corrected, cbar_opt, sel_used,
-                        sel_used_phys, nullptr, 0, ws, s);
+                        sel_used_phys, nullptr, 0, ws, s, true, early.ready, early.ready_tag);
   if (rc) return rc;
   st->step += 1;
   return launch_attn(dims, q_stage, k_pool, v_pool, dims->n_phys_pages, sel_used_phys, top_k, scale,
-                     nullptr, 0, carve_attn(dims, top_k, static_cast<uint8_t *>(ws) + sel_b), out_dev, s);
+                     nullptr, 0, aw, out_dev, s, true, early);
 }
 
 int kvr_speculative_step_overlap(const kvr_dims *dims, kvr_spec_state *st, const uint16_t *q_t,

@@ -74,6 +74,10 @@ struct SpecArgs {
   int32_t *sel_used_phys;      // [B][H][k] or null
   const int32_t *page2slot;    // [B][H][N] working-set map, or null (use page_table)
   int n_slots;                 // slots per sequence when page2slot is set
+  unsigned long long *ready;   // [B][H] or null: a reused unit's word is set to ready_tag
+                               //    (release) once its sel_used and sel_used_phys are
+                               //    written, so the attention may start it early
+  unsigned long long ready_tag;
 };
 
 __device__ __forceinline__ uint32_t score_key(float s) {
@@ -379,7 +383,12 @@ __global__ void __launch_bounds__(32 * G)
 // exchange of warp totals), and the ordered compaction works on ballots of
 // the 32-page blocks, so no pass walks keys through shared memory.
 template <int G, int NT, int KPT>
-__global__ void __launch_bounds__(NT, 1)
+// The 512-thread, 8-key instance at 64 registers (it needs no more): its CTA
+// then fits on an SM beside two scoring CTAs (30 K registers) or an
+// attention CTA (24 K), so that the speculative prologue runs while the
+// scores stream and a reused unit's attention starts as soon as the scoring
+// ends.  (The 256-thread ones fit as they are; 16 keys would spill.)
+__global__ void __launch_bounds__(NT, NT == 512 && KPT <= 8 ? 2 : 1)
     k_topk(const uint16_t *__restrict__ q, const int32_t *__restrict__ page_table, int H, int N,
            int k, const float *__restrict__ ws_scores, int32_t *__restrict__ sel_out,
            int32_t *__restrict__ sel_phys_out, SpecArgs spec,
@@ -468,6 +477,12 @@ __global__ void __launch_bounds__(NT, 1)
           spec.sel_used_phys[unit * k + i] = phys;
         }
       }
+    }
+    // a reused unit's page ids are final now: announce them (after every
+    // thread's writes) so that its attention need not wait for this kernel
+    if (spec.ready != nullptr && !corrected) {  // uniform over the CTA
+      __syncthreads();
+      if (tid == 0) st_release_gpu_u64(spec.ready + unit, spec.ready_tag);
     }
   }
   for (int i = tid; i < 2 * kSelBins; i += NT) (&s_hist[0][0])[i] = 0u;

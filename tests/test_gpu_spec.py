@@ -194,6 +194,60 @@ def test_overlapped_step_replays_from_a_cuda_graph():
     np.testing.assert_array_equal(eager.sel_used.cpu().numpy(), ref["sel_used"][15])
 
 
+def test_sequential_step_replays_from_a_cuda_graph():
+    """Steps 8..15 of kvr_speculative_step captured into a CUDA graph and
+    replayed twice give the bits of an eager run fed the same queries twice:
+    a reused unit's attention may start before the top-k ends (its early-start
+    word carries the capture's tag), and each replay clears the words it
+    used, so the second replay starts as clean as the first."""
+    wl, case, dc, tr, ref = accepted_trace(4)
+    qs = gh.t16(tr.q)
+    eager, graph_run = SpecRun(wl, dc), SpecRun(wl, dc)
+    for t in range(8):
+        eager.step(qs[t])
+        graph_run.step(qs[t])
+    torch.cuda.synchronize()
+    snap = (graph_run.q_prev.clone(), graph_run.sel_prev.clone())
+
+    def plain(run, q):
+        kvr.kvr_speculative_step(dc.dims, run.st, q, dc.summaries(), dc.page_table, dc.k_pool, dc.v_pool,
+                                 wl.top_k, wl.tau, 0.0, run.out, run.corrected, run.cbar, run.sel_used,
+                                 run.sel_used_phys, run.ws, run.ws.numel())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for t in range(8, 16):
+            plain(graph_run, qs[t])
+    graph_run.q_prev.copy_(snap[0])  # capture ran nothing
+    graph_run.sel_prev.copy_(snap[1])
+    for rep in range(2):
+        g.replay()
+        for t in range(8, 16):
+            plain(eager, qs[t])
+        torch.cuda.synchronize()
+        for a, b in ((eager.out, graph_run.out), (eager.sel_used, graph_run.sel_used),
+                     (eager.sel_used_phys, graph_run.sel_used_phys), (eager.corrected, graph_run.corrected),
+                     (eager.sel_prev, graph_run.sel_prev), (eager.q_prev, graph_run.q_prev)):
+            assert torch.equal(a, b), f"replay {rep}"
+        if rep == 0:
+            np.testing.assert_array_equal(graph_run.sel_used.cpu().numpy(), ref["sel_used"][15])
+
+
+@pytest.mark.parametrize("fill", [0xA5, 0xFF])
+def test_speculative_trace_does_not_depend_on_workspace_contents(fill):
+    """The 64-step trace with the step's workspace refilled with junk bytes
+    before every step gives the bits of a run on a zeroed one."""
+    wl, case, dc, tr, ref = accepted_trace(4)
+    qs = gh.t16(tr.q)
+    clean, junk = SpecRun(wl, dc), SpecRun(wl, dc)
+    for t in range(wl.steps):
+        clean.step(qs[t])
+        junk.ws.fill_(fill)
+        junk.step(qs[t])
+        for a, b in ((clean.out, junk.out), (clean.sel_used, junk.sel_used), (clean.corrected, junk.corrected),
+                     (clean.sel_prev, junk.sel_prev)):
+            assert torch.equal(a, b), f"step {t}"
+
+
 def test_host_buffer_step_is_bit_identical_to_the_device_step():
     """kvr_speculative_step_host over the 64-step trace, each query read from
     a row of one page-locked host array (an interior pointer) and the output
