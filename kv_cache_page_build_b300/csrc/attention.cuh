@@ -262,8 +262,15 @@ __device__ __forceinline__ void attn_chunk(uint32_t kb, const uint32_t (&qb)[Att
 // only before it leaves.  The ids are read at L2 (never through the
 // read-only path, as they may have been written during this kernel's
 // lifetime).  CTA 0 of the cluster clears the word at the end.
+// Register cap: at most 128 per thread for up to 8 query rows (they need
+// 127 and do not spill), so that an attention CTA (5 warps) fits on an SM
+// beside a 512-thread top-k CTA: each SM sub-partition's 16 K registers then
+// hold its four top-k warps (4 x 2048) and up to two attention warps
+// (2 x 4096); at 146 registers they did not, and the attention CTAs of a
+// speculative step that land there could not start before the top-k ended.
+// 16 rows keep their registers (they would spill).  kAttnCPS CTAs per SM.
 template <int NR, int P, bool CAUSAL>
-__global__ void __launch_bounds__(kAttnThreads, kAttnCPS)
+__global__ void __maxnreg__(NR <= 8 ? 128 : 255)
     k_sparse_decode(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const uint16_t *__restrict__ q,
                     const int32_t *__restrict__ sel_phys, const int32_t *__restrict__ sel_log,
