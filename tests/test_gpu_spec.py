@@ -84,6 +84,38 @@ def test_speculative_trace_matches_oracle():
         assert ref["corrected"][t].all()
 
 
+def test_speculative_step_with_mixed_decisions_matches_oracle():
+    """Steps that hold both reused units, whose attention may start before
+    the top-k ends, and corrected ones, which wait for it: at each step some
+    sequences jump to the trace's query of a distant step (cosine near 0,
+    all their KV heads corrected) while the others follow the trace (their
+    heads reused).  Every query fed is one the trace accepted (top-k margins
+    hold) and every C is far from tau; decisions, selections and outputs
+    against the oracle's speculative run of the same sequence."""
+    wl, case, dc, tr, _ = accepted_trace(4)
+    _, _, summ = accepted_case(wl.cache_of)
+    steps = 24
+    qs_np = tr.q[:steps].copy()
+    for t in range(2, steps):
+        for b in range(wl.batch):
+            if (t + b) % 3 == 0:
+                qs_np[t, b] = tr.q[(t + wl.steps // 2) % wl.steps, b]
+    ref = oracle.speculative_trace(qs_np, case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads,
+                                   wl.top_k, wl.tau, summ=summ)
+    mixed = [t for t in range(1, steps) if 0 < ref["corrected"][t].sum() < ref["corrected"][t].size]
+    assert len(mixed) >= steps // 2, "the sequence should mix reused and corrected units in most steps"
+    assert np.all(np.abs(ref["cbar"][1:] - wl.tau) > 1e-3)
+    qs = gh.t16(qs_np)
+    run = SpecRun(wl, dc)
+    for t in range(steps):
+        run.step(qs[t])
+        np.testing.assert_array_equal(run.corrected.cpu().numpy().astype(bool), ref["corrected"][t],
+                                      err_msg=f"step {t}")
+        np.testing.assert_array_equal(run.sel_used.cpu().numpy(), ref["sel_used"][t], err_msg=f"step {t}")
+        np.testing.assert_array_equal(run.sel_prev.cpu().numpy(), ref["sel_new"][t], err_msg=f"step {t}")
+        gh.assert_attn_close(run.out.cpu().numpy(), ref["out"][t])
+
+
 def test_speculative_state_checkpoint_resume():
     """Saving (q_prev, sel_prev, step) at step 31 and resuming from it
     reproduces steps 32..63 bit for bit."""
