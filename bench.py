@@ -1136,7 +1136,8 @@ def run_gpu_pipeline(args, world, rank, local):
                 sums[name] += m[a].elapsed_time(m[b]) * 1e3
     breakdown = {name: round(v / (M * nL), 2) for name, v in sums.items()}
     status = kvr.kvr_get_status()
-    per_layer = 2 + (6 if host_mode else 5)       # stand-ins; decide or 2 selection kernels, recalls, attentions
+    # two stand-ins; host: 2 selection kernels, 2 recalls, 2 attentions; HBM: scores, top-k, attention
+    per_layer = 2 + (6 if host_mode else 3)
     return {
         "metric": METRIC + "; here whole multi-layer steps",
         "value": round(value, 2),
@@ -1172,9 +1173,10 @@ def run_gpu_pipeline(args, world, rank, local):
         "step_us_with_marks": round(t_mark / (M * G) * 1e6, 2),
         "breakdown_how": f"a CUDA graph of {G} steps that records the pipeline's timing marks, replayed {M} times; "
                          f"the last step of each replay, mean over {M} x {nL} layers (step_us_with_marks: the "
-                         "whole multi-layer step with the marks recorded); side_stream = selection (HBM) or the corrected "
-                         "heads' recall (host), prefetch_stream = the recall of the other heads' pages for the "
-                         "next step (host)",
+                         "whole multi-layer step with the marks recorded); HBM layers run their selection and "
+                         "attention as one chain of dependent launches (selection_main spans both, the other "
+                         "attention spans and both side spans are 0); host layers: side_stream = the corrected "
+                         "heads' recall, prefetch_stream = the recall of the other heads' pages for the next step",
         "roofline": None,
         "gpu_launches": per_layer * nL * n_steps,
         "clocks": clk,

@@ -407,11 +407,11 @@ int kvr_speculative_step_recall(const kvr_dims *dims, kvr_spec_state *st,
  * sel_used_phys of kvr_speculative_step_overlap); with host != NULL it is in
  * host memory (host, wset; sel_used_idx receives working-set slots, as
  * sel_used_slot of kvr_speculative_step_recall).  q is this step's query of
- * the layer.  ev are caller-created cudaEvent_t passed as void*: ev[0] and
- * ev[1] always, ev[2] for a host-resident layer; they carry the layer's
- * dependencies from one pipeline step to the next, so a layer keeps its
- * events for the whole run (layers may share them).  Workspace kind
- * KVR_OP_STEP; layers may share one workspace. */
+ * the layer.  ev are caller-created cudaEvent_t passed as void*, for a
+ * host-resident layer (an HBM-resident one uses none; they may be NULL);
+ * they carry the layer's dependencies from one pipeline step to the next,
+ * so a layer keeps its events for the whole run (layers may share them).
+ * Workspace kind KVR_OP_STEP; layers may share one workspace. */
 typedef struct kvr_layer {
   kvr_spec_state *st;
   const uint16_t *q;
@@ -458,24 +458,27 @@ int kvr_stand_in_read(const kvr_stand_in *compute, uint64_t offset,
  * layer * KVR_PIPE_MARKS + m), for a latency breakdown by
  * cudaEventElapsedTime:
  *   0 main, layer start           1 main, after the QKV stand-in
- *   2 main, after the selection (HBM) or speculative selection (host)
- *   3 main, after the reused heads' attention
- *   4 main, once the side stream's work this layer waits for is done
- *   5 main, after the corrected heads' attention
+ *   2 main, after the speculative selection (host)
+ *   3 main, after the reused heads' attention (host)
+ *   4 main, once the side stream's work this layer waits for is done (host)
+ *   5 main, after the corrected heads' attention (host) or the layer's
+ *        attention (HBM)
  *   6 main, after the output/FFN stand-in
- *   7, 8 side stream: start and end of the selection (HBM) or of the recall
- *        of the corrected heads' pages (host)
+ *   7, 8 side stream: start and end of the recall of the corrected heads'
+ *        pages (host)
  *   9, 10 prefetch stream: start and end of the recall of the other heads'
- *        pages for the next step (host; an HBM layer records both right after
- *        8 on the side stream) */
+ *        pages for the next step (host)
+ * An HBM layer runs its selection and attention as one chain of dependent
+ * launches, which a mark between them would cut: it records 7 to 10 on the
+ * main stream right after 1, and 2 to 4 right before 5 (its selection and
+ * attention span 1 to 5). */
 #define KVR_PIPE_MARKS 11
 
 /* One decode step through n_layers attention layers, in layer order.  Per
  * layer, on `stream`: the QKV stand-in (if compute != NULL), then
- *   HBM-resident: the correction decision (kvr_speculative_step_overlap's
- *     first part), the selection on `side_stream`, the reused heads'
- *     attention beside it, a wait for the selection, the corrected heads'
- *     attention;
+ *   HBM-resident: kvr_speculative_step (the selection, whose speculative
+ *     prologue lets the reused heads' attention start before it ends, then
+ *     the attention), on `stream` alone;
  *   host-resident: a wait for this layer's prefetch of the previous step,
  *     the speculative selection, then on `side_stream` the recall of the
  *     corrected heads' pages and on `prefetch_stream` (after it) the recall
@@ -483,8 +486,8 @@ int kvr_stand_in_read(const kvr_stand_in *compute, uint64_t offset,
  *     attention beside them, a wait for the first recall only, the corrected
  *     heads' attention;
  * then the output/FFN stand-in.  Every layer's results are bit-identical to
- * kvr_speculative_step_overlap (HBM) or kvr_speculative_step_recall (host)
- * called layer by layer.  Every argument of every layer is checked before
+ * kvr_speculative_step (HBM; also to kvr_speculative_step_overlap) or
+ * kvr_speculative_step_recall (host) called layer by layer.  Every argument of every layer is checked before
  * anything is enqueued; a CUDA error part-way returns KVR_ERR_CUDA with the
  * work before it enqueued (st->step has advanced for every layer whose
  * selection was enqueued).  marks: NULL or

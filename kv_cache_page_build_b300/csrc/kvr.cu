@@ -1183,11 +1183,12 @@ int kvr_stand_in_read(const kvr_stand_in *compute, uint64_t offset, uint64_t byt
 static int check_layer(const kvr_dims *dims, const kvr_layer &L, int32_t top_k, float tau) {
   int rc = check_spec(dims, L.st, L.q, L.summ, L.corrected, L.cbar_opt, L.sel_used, tau);
   if (rc) return rc;
-  if (!L.out || !L.sel_used_idx || !L.ev[0] || !L.ev[1]) return KVR_ERR_INVALID_ARG;
+  if (!L.out || !L.sel_used_idx) return KVR_ERR_INVALID_ARG;
   if (!aligned16(L.out) || !aligned16(L.sel_used_idx)) return KVR_ERR_ALIGN;
   if (L.host) {
     if ((rc = check_wset(dims, L.wset, top_k))) return rc;
-    if (!L.host->k_host || !L.host->v_host || !L.ev[2]) return KVR_ERR_INVALID_ARG;
+    if (!L.host->k_host || !L.host->v_host || !L.ev[0] || !L.ev[1] || !L.ev[2])
+      return KVR_ERR_INVALID_ARG;
     if (!aligned16(L.host->k_host) || !aligned16(L.host->v_host)) return KVR_ERR_ALIGN;
   } else {
     if (!L.page_table || !L.k_pool || !L.v_pool) return KVR_ERR_INVALID_ARG;
@@ -1247,33 +1248,29 @@ int kvr_pipeline_step(const kvr_dims *dims, int32_t n_layers, kvr_layer *layers,
     KVR_TRY(launch_stand_in(compute, 0, qkv, s));
     KVR_TRY(mark(l, 1, s));
     if (!L.host) {
-      // the decision and the page scores on the main stream, the top-k
-      // beside the reused heads' attention (as kvr_speculative_step_overlap)
-      SpecArgs sa = spec_args(L.st, tau, L.corrected, L.cbar_opt, L.sel_used, L.sel_used_idx,
-                              nullptr, 0);
-      const SelectWs sw = carve_select(dims, static_cast<uint8_t *>(L.ws));
-      KVR_TRY(launch_spec_decide(dims, L.q, L.page_table, top_k, sa, s));
+      // kvr_speculative_step: the selection, whose speculative prologue
+      // announces the reused heads' page ids, then the attention, whose
+      // reused units start before the selection ends.  One chain of
+      // dependent launches on `stream`; a mark between its kernels would
+      // cut it, so this layer's side marks come first and marks 2-4 after
+      // the attention.
+      KVR_TRY(mark(l, 7, s));
+      KVR_TRY(mark(l, 8, s));
+      KVR_TRY(mark(l, 9, s));
+      KVR_TRY(mark(l, 10, s));
+      const unsigned long long tag = next_ready_tag();
+      KVR_TRY(spec_select_impl(dims, L.st, L.q, L.summ, L.page_table, top_k, tau, L.corrected,
+                               L.cbar_opt, L.sel_used, L.sel_used_idx, nullptr, 0, L.ws, s, true,
+                               aw.ready, tag));
       L.st->step += 1;
-      sa.decided = 1;
-      KVR_TRY(launch_select(dims, L.q, L.summ, L.page_table, top_k, sw, nullptr, nullptr, nullptr, sa,
-                            s, true, nullptr, kSelScores));
+      AttnLen early;
+      early.ready = aw.ready;
+      early.ready_tag = tag;
+      KVR_TRY(launch_attn(dims, L.q, L.k_pool, L.v_pool, dims->n_phys_pages, L.sel_used_idx, top_k,
+                          scale, nullptr, 0, aw, L.out, s, true, early));
       KVR_TRY(mark(l, 2, s));
-      KVR_TRY(record(L.ev[0], s));
-      KVR_TRY(wait(side, L.ev[0]));
-      KVR_TRY(mark(l, 7, side));
-      KVR_TRY(launch_select(dims, L.q, L.summ, L.page_table, top_k, sw, nullptr, nullptr, nullptr, sa,
-                            side, false, nullptr, kSelTopk));
-      KVR_TRY(mark(l, 8, side));
-      KVR_TRY(mark(l, 9, side));   // before ev[1], which joins them to `stream`
-      KVR_TRY(mark(l, 10, side));
-      KVR_TRY(record(L.ev[1], side));
-      KVR_TRY(launch_attn(dims, L.q, L.k_pool, L.v_pool, dims->n_phys_pages, L.sel_used_idx, top_k,
-                          scale, L.corrected, 1, aw, L.out, s));
       KVR_TRY(mark(l, 3, s));
-      KVR_TRY(wait(s, L.ev[1]));
       KVR_TRY(mark(l, 4, s));
-      KVR_TRY(launch_attn(dims, L.q, L.k_pool, L.v_pool, dims->n_phys_pages, L.sel_used_idx, top_k,
-                          scale, L.corrected, 2, aw, L.out, s, false));
     } else {
       // this layer's maps and slots as the previous step's prefetch left them
       KVR_TRY(wait(s, L.ev[2]));

@@ -207,7 +207,6 @@ def test_pipeline_arguments_rejected_before_launch():
     good = hbm_layer(st0)
     assert call([good], n=0) == kvr.KVR_ERR_INVALID_ARG
     assert call([good], top_k=0) == kvr.KVR_ERR_INVALID_ARG
-    assert call([good, hbm_layer(st1, events=[FAKE])]) == kvr.KVR_ERR_INVALID_ARG      # ev[1] missing
     assert call([good, hbm_layer(st1, k_pool=None)]) == kvr.KVR_ERR_INVALID_ARG
     assert call([good, hbm_layer(st1, out=FAKE + 4)]) == kvr.KVR_ERR_ALIGN
     assert call([good, hbm_layer(st1, ws_bytes=16)]) == kvr.KVR_ERR_WORKSPACE
@@ -216,6 +215,7 @@ def test_pipeline_arguments_rejected_before_launch():
     host = kvr.kvr_host_kv(FAKE, FAKE)
     wset = kvr.kvr_working_set(FAKE, FAKE, FAKE, FAKE, 128)
     assert call([good, hbm_layer(st1, host=host, wset=wset)]) == kvr.KVR_ERR_INVALID_ARG
+    assert call([good, hbm_layer(st1, host=host, wset=wset, events=[FAKE, None, FAKE])]) == kvr.KVR_ERR_INVALID_ARG
     small = kvr.kvr_working_set(FAKE, FAKE, FAKE, FAKE, 127)
     assert call([good, hbm_layer(st1, host=host, wset=small, events=[FAKE] * 3)]) == kvr.KVR_ERR_UNSUPPORTED_SHAPE
     # the stand-in: byte counts in 16-byte words, aligned weights, a sink

@@ -1,7 +1,8 @@
 """Multi-layer decode pipeline (kvr_pipeline_step) through the C ABI.  Each
-layer's results equal, bit for bit, the single-layer step it generalises (the
-overlapped step for an HBM-resident layer, the recall step for a
-host-resident one) and the oracle's speculative trace of that layer; the
+layer's results equal, bit for bit, the single-layer step it generalises
+(kvr_speculative_step, and so the overlapped step too, for an HBM-resident
+layer; the recall step for a host-resident one) and the oracle's
+speculative trace of that layer; the
 working sets end every step in the same state; the stand-in reads exactly
 the bytes it is given; the timing marks and a CUDA-graph replay change no
 result."""
@@ -246,9 +247,12 @@ def test_mixed_layers_with_marks_and_graph_replay():
         torch.cuda.synchronize()
         for L, M in zip(plain.layers, marked.layers):
             _assert_same(L.state(), M.state(), f"marks, step {t}")
-        for l in range(len(specs)):
+        for l, (_, host) in enumerate(specs):
             m = marks[l * kvr.KVR_PIPE_MARKS:(l + 1) * kvr.KVR_PIPE_MARKS]
-            for a, b in ((0, 1), (1, 2), (2, 3), (3, 4), (4, 5), (5, 6), (7, 8), (9, 10), (8, 4), (2, 7), (8, 9)):
+            # a host layer's side marks follow its selection; an HBM layer
+            # records them right after 1 and marks 2-4 right before 5
+            order = ((2, 7), (8, 9)) if host else ((1, 7), (8, 9), (10, 2))
+            for a, b in ((0, 1), (1, 2), (2, 3), (3, 4), (4, 5), (5, 6), (7, 8), (9, 10), (8, 4)) + order:
                 assert m[a].elapsed_time(m[b]) >= -1e-3, (l, a, b)       # ms; timer granularity
             if l + 1 < len(specs):
                 assert m[6].elapsed_time(marks[(l + 1) * kvr.KVR_PIPE_MARKS]) >= -1e-3

@@ -64,12 +64,17 @@ def _classify(stmt):
         part = {"kSelScores": "scores", "kSelTopk": "topk"}.get(a[-1], "select")
         return ("kernel", a[a.index("sa") + 1], part)
     if name == "spec_select_impl":
-        return ("kernel", a[-2], "spec_select")
+        stream = a[a.index("L.ws") + 1]
+        # with the early-start words (HBM): the whole selection of the step,
+        # the attention after it reading the reused units' ids early
+        return ("kernel", stream, "spec_step_select" if "aw.ready" in a else "spec_select")
     if name == "launch_recall":
         return ("kernel", a[-2], {"2": "recall_corrected", "1": "recall_prefetch"}[a[-1]])
     if name == "launch_attn":
-        mode = a[a.index("L.corrected") + 1]
         stream = a[a.index("L.out") + 1]
+        if "L.corrected" not in a:
+            return ("kernel", stream, "attn_all")
+        mode = a[a.index("L.corrected") + 1]
         return ("kernel", stream, {"1": "attn_reused", "2": "attn_corrected"}[mode])
     raise AssertionError(f"unknown statement {stmt!r}")
 
@@ -104,10 +109,14 @@ ACCESS = {
     "topk": (("corrected", "ws"), ("sel_prev", "sel_used.c", "idx.c")),
     "spec_select": (("q_prev", "sel_prev", "maps"),
                     ("ws", "corrected", "cbar", "q_prev", "sel_prev", "sel_used", "idx.r")),
+    "spec_step_select": (("q_prev", "sel_prev"),
+                         ("ws", "corrected", "cbar", "q_prev", "sel_prev", "sel_used", "idx")),
     "recall_corrected": (("sel_prev", "sel_used", "corrected", "maps.c"), ("maps.c", "slots.c", "idx.c")),
     "recall_prefetch": (("sel_prev", "sel_used", "corrected", "maps.r"), ("maps.r", "slots.r")),
     "attn_reused": (("corrected", "idx.r", "slots.r"), ("out.r",)),
     "attn_corrected": (("corrected", "idx.c", "slots.c"), ("out.c",)),
+    # reads the early-start words in the workspace and clears them
+    "attn_all": (("idx", "ws"), ("out", "ws")),
 }
 SHARED = {"ws"}
 
@@ -199,7 +208,8 @@ def test_schedule_is_read_from_the_source():
     pro, hbm, host, epi = pipeline_schedule()
     kernels = lambda seq: [d for k, _, d in seq if k == "kernel"]
     assert kernels(pro) == ["stand_in"] and kernels(epi) == ["stand_in"]
-    assert kernels(hbm) == ["decide", "scores", "topk", "attn_reused", "attn_corrected"]
+    assert kernels(hbm) == ["spec_step_select", "attn_all"]
+    assert all(stream == "s" for _, stream, _ in hbm)
     assert kernels(host) == ["spec_select", "recall_corrected", "recall_prefetch", "attn_reused",
                              "attn_corrected"]
     assert sum(k == "mark" for k, _, _ in pro + hbm + epi) == 11
@@ -228,9 +238,13 @@ def test_join_orders_every_operation_before_what_follows():
     assert "recall_prefetch" in loose
 
 
-def _mutated(drop=None, move=None):
+def _mutated(drop=None, move=None, restream=None):
     pro, hbm, host, epi = pipeline_schedule()
     hbm, host = list(hbm), list(host)
+    if restream:
+        branch, op, stream = restream
+        seq = hbm if branch == "hbm" else host
+        seq[seq.index(op)] = (op[0], stream, op[2])
     if drop:
         branch, op = drop
         seq = hbm if branch == "hbm" else host
@@ -246,11 +260,10 @@ def _mutated(drop=None, move=None):
 @pytest.mark.parametrize("mutation,kinds", [
     (dict(drop=("host", ("wait", "s", 2))), ["host"] * 2),                       # no wait for last prefetch
     (dict(drop=("host", ("wait", "s", 1))), ["host"] * 2),                       # corrected heads don't wait
-    (dict(drop=("hbm", ("wait", "s", 1))), ["hbm"] * 2),                         # nor for their selection
+    (dict(restream=("hbm", ("kernel", "s", "attn_all"), "side")), ["hbm"] * 2),   # attention beside its selection
     (dict(drop=("host", ("wait", "pf", 1))), ["host"] * 2),                      # prefetch before selection
     (dict(move=("host", ("record", "side", 1), ("kernel", "side", "recall_corrected"))), ["host"] * 2),
-    (dict(move=("hbm", ("record", "s", 0), ("kernel", "s", "decide"))), ["hbm"] * 2),
-    (dict(move=("hbm", ("record", "s", 0), ("kernel", "s", "scores"))), ["hbm"] * 2),  # top-k before its scores
+    (dict(restream=("hbm", ("kernel", "s", "spec_step_select"), "side")), ["hbm", "host"]),  # selection off the chain
 ])
 def test_the_check_catches_a_broken_schedule(mutation, kinds):
     assert races(unroll(_mutated(**mutation), kinds, 3)) != []
