@@ -218,24 +218,34 @@ class ClockSampler:
 # ---------------------------------------------------------------- oracle leg
 
 
-def cpu_baseline(wl_name: str, seconds: float = 12.0):
-    """The fp64 oracle (as it stands) on this host: full decode steps of the
-    workload (selection + attention, summaries precomputed) until `seconds`."""
+SEGMENT = 8  # speculative steps per oracle call of the CPU baseline
+
+
+def cpu_baseline(wl_name: str, seconds: float = 12.0, with_case=False):
+    """The fp64 oracle (as it stands) on this host: speculative decode steps
+    of the workload's query trace (decision, selection and attention;
+    summaries precomputed), in segments of SEGMENT steps (each segment starts
+    from an empty state, so its first step corrects every head), until
+    `seconds`."""
     import oracle
     from kv_cache_page_build_b300 import synth
     cid, tid = WORKLOADS[wl_name]
     case = synth.make_case(cid)
-    tr = synth.make_trace(synth.WORKLOADS[tid], case)
+    wl_trace = synth.WORKLOADS[tid]
+    tr = synth.make_trace(wl_trace, case)
     summ = oracle.summaries(case.k_pool, case.page_table)
     wl = case.wl
     cores = oracle.max_threads()
+    T = tr.q.shape[0]
 
     def run(budget):
         n, t0 = 0, time.perf_counter()
         while True:
-            oracle.decode_step(tr.q[n % tr.q.shape[0]], case.k_pool, case.v_pool, case.page_table,
-                               wl.n_kv_heads, wl.top_k, summ=summ)
-            n += 1
+            i = (n // SEGMENT * SEGMENT) % T
+            seg = tr.q[i:i + SEGMENT]
+            oracle.speculative_trace(seg, case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads, wl.top_k,
+                                     wl_trace.tau, summ=summ)
+            n += seg.shape[0]
             el = time.perf_counter() - t0
             if el >= budget:
                 return n, el
@@ -247,11 +257,13 @@ def cpu_baseline(wl_name: str, seconds: float = 12.0):
         n1, el1 = run(seconds / 3)
     finally:
         oracle.set_threads(cores)
-    return {"value": n / el, "unit": "steps/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} full decode steps (batch {wl.batch}, selection + attention, fp64) of the same "
-                      f"workload in {el:.1f} s; summaries built beforehand",
-            "single_thread": {"value": round(n1 / el1, 3), "unit": "steps/s", "cores": 1,
-                              "sample": f"{n1} steps in {el1:.1f} s"}}
+    res = {"value": n / el, "unit": "steps/s", "cores": cores, "kind": "oracle",
+           "sample": f"{n} speculative decode steps (batch {wl.batch}; decision, selection and attention; fp64) "
+                     f"of the same workload's query trace in segments of {SEGMENT} steps, in {el:.1f} s; "
+                     f"summaries built beforehand",
+           "single_thread": {"value": round(n1 / el1, 3), "unit": "steps/s", "cores": 1,
+                             "sample": f"{n1} steps in {el1:.1f} s"}}
+    return (res, workload_keys(wl_name, wl, wl_trace.tau)) if with_case else res
 
 
 # ---------------------------------------------------------------- GPU leg
@@ -610,14 +622,21 @@ def hbm_kernels(r):
     }
 
 
-def hbm_config(name, r, world):
-    wl = r["wl"]
+def workload_keys(name, wl, tau):
+    """The config keys that name a workload (shared by both arms' lines)."""
     B, Hq, H, D, P, k = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.page_size, wl.top_k
     return {
         "workload": f"{name}: {B} sequences x {Hq}/{H} heads, head_dim {D}, context {wl.context}, page {P}, "
-                    f"top-k {k} pages; speculative, tau {r['tau']}",
+                    f"top-k {k} pages; speculative, tau {tau}",
         "batch": B, "n_q_heads": Hq, "n_kv_heads": H, "head_dim": D, "context": wl.context, "page_size": P,
-        "top_k": k, "tau": r["tau"], "storage": "bf16", "accumulate": "f32",
+        "top_k": k, "tau": tau, "storage": "bf16",
+    }
+
+
+def hbm_config(name, r, world):
+    return {
+        **workload_keys(name, r["wl"], r["tau"]),
+        "accumulate": "f32",
         "parallelism": f"{world} independent replica(s)" if world > 1 else "1 GPU",
         "l2": f"{r['copies']} rotating cache copies: "
               f"{(r['copies'] - 1) * (r['attn_bytes'] + r['summ_bytes']) / 2**20:.0f} MiB touched between reuses "
@@ -1214,12 +1233,12 @@ def main():
             return
         # each timed step is one full oracle decode step; the run is bounded in time
         secs = min(60.0, max(5.0, 0.5 * (args.steps + args.warmup)))
-        base = cpu_baseline(args.workload, seconds=secs)
+        base, wkeys = cpu_baseline(args.workload, seconds=secs, with_case=True)
         line = {"impl": "reference", "metric": METRIC, "value": round(base["value"], 4), "unit": "steps/s",
                 "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(1e3 / base["value"], 3), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": args.workload, "parallelism": "host cores (OpenMP)"},
+                "config": {**wkeys, "accumulate": "f64", "parallelism": "host cores (OpenMP)"},
                 "cpu_baseline": base,
                 "e2e": {"value": round(base["value"], 4), "unit": "steps/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
