@@ -336,10 +336,11 @@ __global__ void __maxnreg__(NR <= 8 ? 128 : 255)
   __syncthreads();
   // Launched as a programmatic dependent launch, the setup above overlaps
   // the previous kernel; every global read and write comes after this wait,
-  // except in an early unit (its inputs were announced; it waits at the end)
+  // except in an early unit (its inputs were announced; it waits at the end).
+  // The next kernel may be scheduled at once: its own wait covers this one.
   const bool early = s_early != 0;
-  if (!early) pdl_wait();
   if (tid == 0) pdl_launch_dependents();
+  if (!early) pdl_wait();
   // the whole cluster holds one unit, so this exit is uniform over it (no
   // thread of the cluster touches another CTA's shared memory)
   if (!attn_unit_active(filter, filter_mode, u)) {
