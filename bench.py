@@ -3,6 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload qwen3-4b-128k|llama3.1-8b-32k|qwen3-4b-128k-host]
                     [--step sequential|overlap|pipeline] [--layers L] [--no-extras]
+                    [--e2e-calls C] [--copies R] [--kernel-launches L] [--no-cpu-baseline]
 
 One step is one speculative decode step of one attention layer over a batch
 of sequences, through kvr_speculative_step (default): page scoring, then the
@@ -27,8 +28,15 @@ through --layers layers with kvr_pipeline_step instead (stand-in projection
 reads between the attentions), beside the same layers stepped one call at a
 time, and reports a per-layer latency breakdown.
 
+The line's "e2e" is the same step through the public call a serving loop
+makes with host buffers, kvr_speculative_step_host: every step reads its
+query from pinned host memory and leaves its output there, with one step in
+flight (2000 timed eager calls after 200 untimed ones, --e2e-calls); it also
+reports the rate when the host waits for every step.
+
 Prints one JSON line (rank 0).  With --impl reference the fp64 oracle is
-timed instead, on the host's cores, over a bounded sample of the workload.
+timed instead, on the host's cores, over a bounded sample of the workload
+(its speculative steps, in segments of 8 steps of the same query trace).
 """
 from __future__ import annotations
 
