@@ -170,6 +170,52 @@ def test_small_shapes_and_edges(kw):
     gh.assert_attn_close(out.cpu().numpy(), out_ref)
 
 
+@pytest.mark.parametrize("kw", [SHAPES[i] for i in (1, 2, 3, 4, 5, 7, 11)],
+                         ids=["P16", "P64", "G1", "G2", "G8", "k1", "N3000"])
+def test_speculative_steps_device_and_host_buffers(kw):
+    """Two speculative steps on one query at the edge shapes: step 0 corrects
+    every head (the oracle's decode step), step 1 (cosine 1) reuses every head,
+    whose attention starts before the top-k ends.  kvr_speculative_step on
+    device buffers and kvr_speculative_step_host on page-locked ones give the
+    same bits."""
+    case, dc = small_case(**kw)
+    wl = case.wl
+    B, Hq, H, D, k = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.top_k
+    sel_ref, _, out_ref = oracle.decode_step(case.q, case.k_pool, case.v_pool, case.page_table, H, k)
+    q_host = torch.from_numpy(np.ascontiguousarray(case.q).view(np.int16)).pin_memory()
+    runs = []
+    for host in (False, True):
+        q_prev = torch.zeros((B, Hq, D), dtype=torch.int16, device="cuda")
+        sel_prev = torch.zeros((B, H, k), dtype=torch.int32, device="cuda")
+        st = kvr.kvr_spec_state(q_prev.data_ptr(), sel_prev.data_ptr(), 0)
+        corr = torch.empty((B, H), dtype=torch.uint8, device="cuda")
+        used = torch.empty((B, H, k), dtype=torch.int32, device="cuda")
+        used_phys = torch.empty_like(used)
+        ws = gh.workspace(dc.dims, k, kvr.KVR_OP_STEP_HOST if host else kvr.KVR_OP_STEP).fill_(0xA5)
+        steps = []
+        for t in range(2):
+            if host:
+                out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32).pin_memory()
+                kvr.kvr_speculative_step_host(dc.dims, st, q_host, dc.summaries(), dc.page_table, dc.k_pool,
+                                              dc.v_pool, k, 0.8, 0.0, out, corr, None, used, used_phys, ws,
+                                              ws.numel())
+            else:
+                out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+                kvr.kvr_speculative_step(dc.dims, st, dc.q, dc.summaries(), dc.page_table, dc.k_pool, dc.v_pool,
+                                         k, 0.8, 0.0, out, corr, None, used, used_phys, ws, ws.numel())
+            torch.cuda.synchronize()
+            steps.append((out.cpu().clone(), corr.cpu().clone(), used.cpu().clone(), sel_prev.cpu().clone()))
+        runs.append(steps)
+    for t in range(2):
+        for a, b in zip(runs[0][t], runs[1][t]):
+            assert torch.equal(a, b), f"step {t}"
+        out, corr, used, sel_new = runs[0][t]
+        assert bool(corr.all()) == (t == 0) and bool((corr == 0).all()) == (t == 1)
+        np.testing.assert_array_equal(used.numpy(), sel_ref)
+        np.testing.assert_array_equal(sel_new.numpy(), sel_ref)
+        gh.assert_attn_close(out.numpy(), out_ref)
+
+
 def test_explicit_scale():
     case, dc = small_case()
     wl = case.wl
