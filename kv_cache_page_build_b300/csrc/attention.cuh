@@ -380,7 +380,7 @@ __global__ void __maxnreg__(NR <= 8 ? 128 : 255)
 #pragma unroll
           for (int r = 0; r < kIdRounds; ++r) {
             const int j = lane + 32 * r;
-            idv[w][r] = j < n ? __ldg(sel_lu + (a + j) / CPP) : -1;
+            idv[w][r] = j < n ? __ldcg(sel_lu + (a + j) / CPP) : -1;
           }
         }
 #pragma unroll
@@ -420,7 +420,7 @@ __global__ void __maxnreg__(NR <= 8 ? 128 : 255)
           const int id = i < kAttnIds ? s_ids[lane][i] : __ldcg(sel_u + pos / CPP);
           int nv, pos0 = 0;
           if (causal) {  // tokens below the sequence's length, from the logical position
-            const int lid = i < kAttnIds ? s_lids[lane][i] : __ldg(sel_lu + pos / CPP);
+            const int lid = i < kAttnIds ? s_lids[lane][i] : __ldcg(sel_lu + pos / CPP);
             pos0 = lid * P + (pos % CPP) * Cfg::C;
             nv = lid >= 0 ? min(Cfg::C, max(0, L - pos0)) : 0;
           } else {

@@ -14,8 +14,9 @@
 // first host reads before the dependency wait, so that their latency
 // overlaps the kernel before it (the host buffer is no kernel's output, and
 // the staged copy may still be read by the previous step until the wait);
-// it stores only after the wait.  It lets the next kernel launch at once:
-// that kernel's own dependency wait covers this kernel's completion.
+// it stores only after the wait.  It does not let the next kernel launch
+// early: that kernel reads the staged query through the read-only path,
+// which is only safe for data no kernel still running writes.
 #pragma once
 
 #include "common.cuh"
@@ -26,7 +27,6 @@ constexpr int kStageThreads = 256;
 
 __global__ void __launch_bounds__(kStageThreads)
     k_stage_in(const uint4 *__restrict__ host, uint4 *__restrict__ dst, uint64_t n16) {
-  if (threadIdx.x == 0) pdl_launch_dependents();
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kStageThreads;
   uint64_t i = static_cast<uint64_t>(blockIdx.x) * kStageThreads + threadIdx.x;
   uint4 v = make_uint4(0u, 0u, 0u, 0u);

@@ -230,6 +230,8 @@ __global__ void __launch_bounds__(kScThreads, kScCPS)
         for (int kk = 0; kk < 8; ++kk) {
 #pragma unroll
           for (int hlf = 0; hlf < 2; ++hlf) {
+            // q is written by no kernel that lets this one start before it
+            // ends, so the read-only path is safe for it
             const uint32_t w = on ? __ldg(qrow + 8 * kk + 4 * hlf + tq) : 0u;
             // per bf16 half: all ones where the sign bit is set
             const uint32_t neg = ((w >> 15) & 0x00010001u) * 0xffffu;
@@ -398,6 +400,7 @@ __global__ void __launch_bounds__(NT, NT == 512 && KPT <= 8 ? 2 : 1)
   __shared__ __align__(16) uint32_t s_hist[2][kSelBins];
   __shared__ uint32_t s_w1[NW], s_w2[NW];
   __shared__ uint32_t s_bin, s_bin_above, s_bin_cnt;
+  __shared__ uint32_t s_cand[32], s_ncand;  // the last few keys of [L, R], ranked by one warp
   __shared__ float s_cos[8];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -486,6 +489,7 @@ __global__ void __launch_bounds__(NT, NT == 512 && KPT <= 8 ? 2 : 1)
     }
   }
   for (int i = tid; i < 2 * kSelBins; i += NT) (&s_hist[0][0])[i] = 0u;
+  if (tid == 0) s_ncand = 0u;
   pdl_wait();  // the scores of k_page_scores are complete and visible
   if (spec.enabled && spec.decided) corrected = spec.corrected[unit] != 0;  // k_spec_decide's decision
 
@@ -493,7 +497,10 @@ __global__ void __launch_bounds__(NT, NT == 512 && KPT <= 8 ? 2 : 1)
   const float *row = ws_scores + unit * N;
   float sv[KPT];
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) sv[j] = base + 32 * j < Nv ? __ldg(row + base + 32 * j) : 0.f;
+  // at L2, never through the read-only path: k_page_scores writes them while
+  // this kernel is already resident (programmatic dependent launch), so a
+  // read-only cache could still hold an earlier call's lines
+  for (int j = 0; j < KPT; ++j) sv[j] = base + 32 * j < Nv ? __ldcg(row + base + 32 * j) : 0.f;
   uint32_t key[KPT];
   uint32_t kmn = 0xffffffffu, kmx = 0u;
 #pragma unroll
@@ -535,6 +542,37 @@ __global__ void __launch_bounds__(NT, NT == 512 && KPT <= 8 ? 2 : 1)
   int buf = 0;
 #pragma unroll 1
   while (cnt != need && L != R) {
+    if (cnt <= 32u) {
+      // few keys left in [L, R] (usually after one round): one warp ranks
+      // them instead of another histogram pass.  The need-th largest value v
+      // of the interval has gt keys above it and eq equal to it, with
+      // gt < need <= gt + eq; then L = R = v, and need - gt of the eq keys
+      // equal to v are taken (the first by page id, in the compaction).
+#pragma unroll
+      for (int j = 0; j < KPT; ++j)
+        if (base + 32 * j < Nv && key[j] >= L && key[j] <= R) s_cand[atomicAdd(&s_ncand, 1u)] = key[j];
+      __syncthreads();
+      if (warp == 0) {
+        const uint32_t c = s_ncand;  // == cnt
+        const uint32_t mine = lane < static_cast<int>(c) ? s_cand[lane] : 0u;
+        uint32_t gt = 0u, eq = 0u;
+        for (uint32_t o = 0; o < c; ++o) {
+          const uint32_t x = __shfl_sync(0xffffffffu, mine, static_cast<int>(o));
+          gt += x > mine ? 1u : 0u;
+          eq += x == mine ? 1u : 0u;
+        }
+        if (lane < static_cast<int>(c) && gt < need && need <= gt + eq) {  // lanes of v write the same
+          s_bin = mine;
+          s_bin_above = gt;
+          s_bin_cnt = eq;
+        }
+      }
+      __syncthreads();
+      L = R = s_bin;
+      need -= s_bin_above;
+      cnt = s_bin_cnt;
+      break;
+    }
     const uint32_t span = R - L;
     const int shift = span < kSelBins ? 0 : (32 - __clz(span)) - 11;
     uint32_t *hist = s_hist[buf];

@@ -216,6 +216,22 @@ def test_speculative_steps_device_and_host_buffers(kw):
         gh.assert_attn_close(out.numpy(), out_ref)
 
 
+@pytest.mark.parametrize("cid", [2, 3])
+def test_repeated_selections_on_one_workspace_match_the_oracle(cid):
+    """Eight selections in a row on one workspace each give the oracle's
+    top-k.  The top-k kernel is resident while the scoring kernel before it
+    still writes the scores (programmatic dependent launch), so it must read
+    them at L2: through the read-only cache, lines of an earlier call's
+    scores were served and most repeated selections differed."""
+    case, dc, summ = accepted_case(cid)
+    wl = case.wl
+    want = oracle.topk(oracle.scores(case.q, *summ), wl.top_k)
+    ws = gh.workspace(dc.dims, wl.top_k, kvr.KVR_OP_SELECT)
+    for rep in range(8):
+        sel, _, _ = gh.select(dc, ws=ws)
+        np.testing.assert_array_equal(sel.cpu().numpy(), want, err_msg=f"run {rep}")
+
+
 def test_explicit_scale():
     case, dc = small_case()
     wl = case.wl
