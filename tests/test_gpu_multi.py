@@ -106,6 +106,39 @@ def test_llama_shapes_several_queries(T):
     check(case, qs, lens, ref, *run(case, qs, lens, T))
 
 
+def test_repeated_several_query_steps_on_one_workspace():
+    """The selection and the causal attention of a step of 4 queries, run
+    eight times back to back on one workspace, each time against the oracle:
+    the attention is resident while the selection still writes the logical
+    ids it reads (programmatic dependent launch), so it reads them at L2."""
+    wl = synth.WORKLOADS[2]
+    lens = wl.n_pages * wl.page_size - np.array([0, 1, 5, 17, 31, 32, 33, 300])
+    T = 4
+    case, qs, lens, ref = make(wl, T, lens)
+    dc = gh.DevCase(case)
+    L = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    summ = torch.zeros((wl.batch, wl.n_kv_heads, wl.n_pages, 2, wl.head_dim), dtype=torch.int16, device="cuda")
+    kvr.kvr_build_summaries_len(dc.dims, dc.k_pool, dc.page_table, L, summ)
+    k = wl.top_k
+    q = gh.t16(qs)
+    ws = gh.workspace(dc.dims, k, kvr.KVR_OP_STEP)
+    first = None
+    for rep in range(8):
+        sel = torch.full((wl.batch, wl.n_kv_heads, k), -7, dtype=torch.int32, device="cuda")
+        sel_phys = torch.full_like(sel, -7)
+        out = torch.full((wl.batch, T, wl.n_q_heads, wl.head_dim), float("nan"), dtype=torch.float32, device="cuda")
+        kvr.kvr_select_pages_multi(dc.dims, q, T, summ, dc.page_table, L, k, sel, sel_phys, None, ws, ws.numel())
+        kvr.kvr_sparse_decode_attn_multi(dc.dims, q, T, dc.k_pool, dc.v_pool, dc.page_table, L, sel, sel_phys, k, 0.0,
+                                         out, kvr.KVR_DTYPE_F32, ws, ws.numel())
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(sel.cpu().numpy(), ref[0], err_msg=f"run {rep}")
+        if first is None:
+            gh.assert_attn_close(out.cpu().numpy(), ref[2])
+            first = out.clone()
+        else:
+            assert torch.equal(out, first), f"run {rep}"
+
+
 @pytest.mark.parametrize("T", [1, 2, 4])
 def test_bf16_output_is_the_fp32_output_rounded(T):
     """KVR_DTYPE_BF16 stores the fp32 result rounded to nearest even once:

@@ -216,6 +216,30 @@ def test_speculative_steps_device_and_host_buffers(kw):
         gh.assert_attn_close(out.numpy(), out_ref)
 
 
+def test_alternating_selections_and_attention_on_one_workspace():
+    """Selection and attention for two queries in turn, twelve times on one
+    workspace: each run gives the oracle's selection and its query's bits of
+    the first run (no kernel reads what an earlier call left)."""
+    case, dc, summ = accepted_case(2)
+    wl = case.wl
+    q_np = [case.q, synth.make_multi_queries(case, 1)[:, 0]]
+    qs = [gh.t16(x) for x in q_np]
+    want = [oracle.topk(oracle.scores(x, *summ), wl.top_k) for x in q_np]
+    ws = gh.workspace(dc.dims, wl.top_k, kvr.KVR_OP_STEP)
+    first = {}
+    for rep in range(12):
+        i = rep % 2
+        sel, sel_phys, _ = gh.select(dc, q=qs[i], ws=ws)
+        out = gh.attention(dc, sel_phys, q=qs[i], ws=ws)
+        torch.cuda.synchronize()
+        if i == 0:  # the accepted query keeps the top-k margins
+            np.testing.assert_array_equal(sel.cpu().numpy(), want[0], err_msg=f"run {rep}")
+        if i not in first:
+            first[i] = (sel.clone(), out.clone())
+        else:
+            assert torch.equal(sel, first[i][0]) and torch.equal(out, first[i][1]), f"run {rep}"
+
+
 @pytest.mark.parametrize("cid", [2, 3])
 def test_repeated_selections_on_one_workspace_match_the_oracle(cid):
     """Eight selections in a row on one workspace each give the oracle's
