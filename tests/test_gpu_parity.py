@@ -111,6 +111,28 @@ def test_all_scores_equal_selects_lowest_ids(n_pages):
     np.testing.assert_array_equal(sel_phys.cpu().numpy()[0], c2.page_table[0, want[0]])
 
 
+def test_ties_across_the_warps_of_the_top_k():
+    """4000 pages, ranked by one CTA whose warps each hold a contiguous block
+    of 256 pages.  Every page holds the keys of the lowest-scoring page
+    except ten near the end, which hold those of the highest-scoring one.
+    With k = 1100 the selection is the 1090 lowest ids of the tie, which run
+    across five blocks, then the ten, last in page order: both counts that a
+    block takes from the blocks below it are exercised."""
+    wl = synth.custom(batch=1, n_q_heads=4, n_kv_heads=1, head_dim=128, page_size=16, n_pages=4000, top_k=1100)
+    case = synth.make_case(wl)
+    s = oracle.scores(case.q, *oracle.summaries(case.k_pool, case.page_table))[0, 0]
+    lo, hi = case.page_table[0, np.argmin(s)], case.page_table[0, np.argmax(s)]
+    hot = np.arange(3500, 3510)
+    c2 = synth.Case(**{**case.__dict__, "k_pool": case.k_pool.copy()})
+    c2.k_pool[:] = case.k_pool[lo]
+    c2.k_pool[c2.page_table[0, hot]] = case.k_pool[hi]
+    want = oracle.topk(oracle.scores(c2.q, *oracle.summaries(c2.k_pool, c2.page_table)), wl.top_k)
+    np.testing.assert_array_equal(want[0, 0], np.concatenate([np.arange(wl.top_k - hot.size), hot]))
+    sel, sel_phys, _ = gh.select(gh.DevCase(c2))
+    np.testing.assert_array_equal(sel.cpu().numpy(), want)
+    np.testing.assert_array_equal(sel_phys.cpu().numpy()[0, 0], c2.page_table[0, want[0, 0]])
+
+
 # ---------------------------------------------------------------- attention
 
 @pytest.mark.parametrize("cid", [1, 2, 3])
