@@ -214,3 +214,44 @@ def test_lengths_for_other_group_sizes(n_q_heads, n_kv_heads):
     kvr.kvr_sparse_decode_attn_len(dc.dims, dc.q, dc.k_pool, dc.v_pool, dc.page_table, L, sel_phys, 5, 0.0, out,
                                    wa, wa.numel())
     gh.assert_attn_close(out.cpu().numpy(), out_ref)
+
+
+def accept_started(lens, P, k):
+    """Row b's query is kept when its top-k boundary among the sequence's
+    started pages (summaries over the written tokens) has a margin of at
+    least the oracle's, so that the fp32 and fp64 selections agree."""
+    def accept(case, b):
+        nv = -(-int(lens[b]) // P)
+        if nv <= k:  # every started page is selected: no boundary
+            return True
+        summ = oracle.summaries(case.k_pool, case.page_table[b:b + 1], seq_len=lens[b:b + 1])
+        s = oracle.scores(case.q[b:b + 1], *summ)[..., :nv]
+        return bool(np.all(oracle.topk_margin(s, k) >= oracle.MARGIN))
+    return accept
+
+
+@pytest.mark.parametrize("n_pages", [1500, 3000, 5000, 9000])
+def test_lengths_at_the_larger_top_k_shapes(n_pages):
+    """Selection over started pages at the page counts of the top-k's larger
+    shapes (256 threads x 8 keys, 512 x 8, 512 x 16, 1024 x 16): a full
+    sequence, one ending inside a page halfway, and one with fewer started
+    pages than k (its last slots -1)."""
+    P, k = 16, 64
+    lens = np.array([n_pages * P, n_pages * P // 2 + 5, 40 * P - 3], dtype=np.int32)
+    wl = synth.custom(batch=3, n_q_heads=4, n_kv_heads=1, head_dim=128, page_size=P, n_pages=n_pages, top_k=k)
+    case = synth.make_case(wl, accept=accept_started(lens, P, k))
+    dc = gh.DevCase(case)
+    L = torch.tensor(lens, device="cuda")
+    summ = dev_summaries(dc, L)
+    kmin, kmax = oracle.summaries(case.k_pool, case.page_table, seq_len=lens)
+    check_summaries(summ, kmin, kmax, lens, P)
+    sel_ref = oracle.topk(oracle.scores(case.q, kmin, kmax), k, n_valid=oracle.valid_pages(lens, P)[:, None])
+    assert (sel_ref[2, 0, 40:] == -1).all() and (sel_ref[2, 0, :40] == np.arange(40)).all()
+    sel = torch.full((wl.batch, wl.n_kv_heads, k), -7, dtype=torch.int32, device="cuda")
+    sel_phys = torch.full_like(sel, -7)
+    ws = gh.workspace(dc.dims, k, kvr.KVR_OP_SELECT)
+    kvr.kvr_select_pages_len(dc.dims, dc.q, summ, dc.page_table, L, k, sel, sel_phys, None, ws, ws.numel())
+    np.testing.assert_array_equal(sel.cpu().numpy(), sel_ref)
+    phys_ref = np.where(sel_ref >= 0, np.take_along_axis(case.page_table[:, None, :], np.maximum(sel_ref, 0),
+                                                         axis=2), -1)
+    np.testing.assert_array_equal(sel_phys.cpu().numpy(), phys_ref)
