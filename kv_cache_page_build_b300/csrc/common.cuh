@@ -32,24 +32,6 @@ __device__ __forceinline__ void set_status(uint32_t bits) { atomicOr(&g_status, 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-__device__ __forceinline__ void unpack8(const uint4 &v, float *f) {
-  f[0] = bf_lo(v.x); f[1] = bf_hi(v.x);
-  f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
-  f[4] = bf_lo(v.z); f[5] = bf_hi(v.z);
-  f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
-}
-
-// bf16 pair (low half = even channel) -> the two fp32 values as a float2
-__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
-  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
-// Named barrier over the first `count` threads of the CTA (ids 1..15; 0 is
-// __syncthreads).
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -253,10 +235,6 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// The two halves of cluster_sync, for work between them.
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
 // Arrive without memory ordering: only says "this thread has started", for
 // the handshake that must precede any access to another CTA's shared memory.
 __device__ __forceinline__ void cluster_arrive_relaxed() {
@@ -273,18 +251,6 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t a, int rank) {
   return r;
 }
 
-// Atomic add on a 32-bit word in the shared memory of a CTA of the cluster
-// (address from cluster_map); returns the old value.
-__device__ __forceinline__ uint32_t atom_add_cluster_u32(uint32_t a, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(a), "r"(v) : "memory");
-  return old;
-}
-
-__device__ __forceinline__ void st_cluster_f32(uint32_t a, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
-}
-
 __device__ __forceinline__ void st_cluster_f32x4(uint32_t a, float4 v) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v.x), "f"(v.y),
                "f"(v.z), "f"(v.w)
@@ -293,27 +259,6 @@ __device__ __forceinline__ void st_cluster_f32x4(uint32_t a, float4 v) {
 
 __device__ __forceinline__ void st_cluster_f32x2(uint32_t a, float2 v) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(v.x), "f"(v.y) : "memory");
-}
-
-__device__ __forceinline__ float ld_cluster_f32(uint32_t a) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t a) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(a)
-               : "memory");
-  return v;
-}
-
-__device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t a) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
-  return v;
 }
 
 // ---------------------------------------------------------------- block scan
