@@ -278,13 +278,17 @@ def test_repeated_selections_on_one_workspace_match_the_oracle(cid):
         np.testing.assert_array_equal(sel.cpu().numpy(), want, err_msg=f"run {rep}")
 
 
-def test_explicit_scale():
+@pytest.mark.parametrize("scale", [0.05, 1.0])
+def test_explicit_scale(scale):
+    """A flatter softmax (0.05) and a nearly one-hot one (1.0: logits with a
+    standard deviation near 11, so a few tokens carry almost all the weight
+    and most weights underflow to zero), merged across the split workers."""
     case, dc = small_case()
     wl = case.wl
     sel_ref, _, _ = oracle.decode_step(case.q, case.k_pool, case.v_pool, case.page_table, wl.n_kv_heads, wl.top_k)
-    ref = oracle.attention(case.q, case.k_pool, case.v_pool, case.page_table, sel_ref, scale=0.05)
+    ref = oracle.attention(case.q, case.k_pool, case.v_pool, case.page_table, sel_ref, scale=scale)
     _, sel_phys, _ = gh.select(dc)
-    gh.assert_attn_close(gh.attention(dc, sel_phys, scale=0.05).cpu().numpy(), ref)
+    gh.assert_attn_close(gh.attention(dc, sel_phys, scale=scale).cpu().numpy(), ref)
 
 
 def test_repeatable_with_junk_filled_workspace():
