@@ -502,16 +502,18 @@ __global__ void __maxnreg__(NR <= 8 ? 128 : 255)
 #pragma unroll 1
     for (int i = 0; i < n; ++i) {
       const int s = cw * R + i % R;  // this warp's stages in turn
-      bool have = false, landed = false;
-      if (__shfl_sync(0xffffffffu, s_abort, 0) == 0) {  // warp-uniform
+      // a chunk that has landed is taken at once; only a wait looks at the
+      // abort flag first (after an abort nothing more lands), then waits
+      // with the bound in force (warp-uniform throughout)
+      bool landed = __all_sync(0xffffffffu, mbar_try_wait(&full[s], static_cast<uint32_t>((i / R) & 1)));
+      if (!landed && __shfl_sync(0xffffffffu, s_abort, 0) == 0) {
         const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((i / R) & 1), wait_ns);
-        if (__all_sync(0xffffffffu, ok)) {
+        if (__all_sync(0xffffffffu, ok))
           landed = true;
-          have = s_ok[s] != 0;
-        } else if (lane == 0) {
+        else if (lane == 0)
           s_abort = 1;
-        }
       }
+      const bool have = landed && s_ok[s] != 0;
       if (have) {
         const int nv = s_nv[s];
         int lim[CB][2];

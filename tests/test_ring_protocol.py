@@ -137,6 +137,19 @@ def test_protocol_is_read_from_the_source(kernel):
 
 
 @pytest.mark.parametrize("kernel", sorted(SOURCES))
+def test_consumer_fast_path_tests_the_same_phase(kernel):
+    """Where a consumer first tests its stage without waiting (a chunk that
+    has landed is taken at once), the test uses the same parity as the
+    modelled wait, so the model covers both paths."""
+    code = _code(open(os.path.join(ROOT, "kv_cache_page_build_b300", "csrc", SOURCES[kernel])).read())
+    fast = re.findall(r"mbar_try_wait\(&full\[s\], static_cast<uint32_t>\((.+?)\)\)", code)
+    for expr in fast:
+        assert expr == protocol_of(kernel).text["consumer"]
+    if kernel == "k_sparse_decode":
+        assert fast, "the attention's consumers test a landed chunk first"
+
+
+@pytest.mark.parametrize("kernel", sorted(SOURCES))
 @pytest.mark.parametrize("R", [1, 2, 3, 6])
 def test_every_read_sees_its_own_chunk(kernel, R):
     p = protocol_of(kernel)
